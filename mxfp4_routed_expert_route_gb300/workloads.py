@@ -1,0 +1,152 @@
+"""Seeded synthetic inputs for the MXFP4 routed expert linear.
+
+This module only draws random inputs. It holds none of the layer's arithmetic
+(no nibble decode, no scale, no dot product), so the CUDA path and the CPU
+oracle can both be fed from it without sharing any of the method.
+
+Shapes follow the problem statement ("MXFP4 Routed Expert Linear", Kimi K3,
+tensortonic formal statement): tokens (T, I), packed weights (E, O, G, 16)
+uint8, scale bytes (E, O, G) uint8, selected experts (T, K), mixture weights
+(T, K), shared output (T, O), with I = 32 G.
+
+Recipe (the same for every named workload):
+  * numpy ``default_rng(seed)``; bytes are drawn on the host, then uploaded.
+  * packed bytes uniform over 0..255 (``rng.bytes``);
+  * scale bytes uniform over the stated inclusive range;
+  * x and y_shared ~ N(0, 1), rounded to nearest-even bf16 where the
+    workload is bf16;
+  * mixture weights = softmax of N(0, 1) logits over the K picks, stored fp32;
+  * uniform picks: K distinct experts per token, uniformly at random;
+  * Zipf picks: popularity r^-s over ranks 1..E, ranks mapped to expert ids by
+    a seeded permutation, K distinct picks per token by Gumbel-top-K (the
+    same law as successive sampling without replacement).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+
+@dataclass
+class Workload:
+    name: str
+    T: int
+    E: int
+    K: int
+    I: int
+    O: int
+    dtype: torch.dtype            # token / shared-output / output dtype
+    x: torch.Tensor               # (T, I) dtype, CPU
+    packed: torch.Tensor          # (E, O, G, 16) uint8, CPU
+    scales: torch.Tensor          # (E, O, G) uint8, CPU
+    sel: torch.Tensor             # (T, K) int32, CPU
+    p: torch.Tensor               # (T, K) float32, CPU
+    y_shared: torch.Tensor        # (T, O) dtype, CPU
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def G(self) -> int:
+        return self.I // 32
+
+    def device_tensors(self, device) -> dict:
+        """Copies of every input on ``device`` (weights included)."""
+        return {k: getattr(self, k).to(device) for k in
+                ("x", "packed", "scales", "sel", "p", "y_shared")}
+
+
+# The five named workloads: (T, E, K, I, O, dtype, scale range, pick law).
+CONFIGS = {
+    "tiny_fp32": dict(T=4, E=4, K=2, I=64, O=8, dtype=torch.float32,
+                      scale_lo=120, scale_hi=134, picks="uniform", seed=0),
+    "decode": dict(T=8, E=128, K=4, I=2880, O=5760, dtype=torch.bfloat16,
+                   scale_lo=118, scale_hi=124, picks="uniform", seed=1),
+    "prefill": dict(T=4096, E=128, K=4, I=2880, O=5760, dtype=torch.bfloat16,
+                    scale_lo=118, scale_hi=124, picks="uniform", seed=2),
+    "wide_decode": dict(T=16, E=384, K=8, I=7168, O=4096, dtype=torch.bfloat16,
+                        scale_lo=116, scale_hi=124, picks="uniform", seed=3),
+    "skewed_prefill": dict(T=8192, E=384, K=8, I=7168, O=4096,
+                           dtype=torch.bfloat16, scale_lo=116, scale_hi=124,
+                           picks="zipf", zipf_s=1.2, seed=4),
+}
+
+
+def _normal(rng, shape, dtype):
+    a = rng.standard_normal(shape, dtype=np.float32)
+    t = torch.from_numpy(a)
+    return t.to(dtype) if dtype != torch.float32 else t
+
+
+def uniform_picks(rng, T: int, E: int, K: int) -> np.ndarray:
+    """K distinct expert ids per token, uniformly at random."""
+    if K == 0 or T == 0:
+        return np.zeros((T, K), dtype=np.int32)
+    keys = rng.random((T, E))
+    return np.argsort(keys, axis=1, kind="stable")[:, :K].astype(np.int32)
+
+
+def zipf_picks(rng, T: int, E: int, K: int, s: float) -> np.ndarray:
+    """K distinct picks per token from Zipf(s) popularity (Gumbel-top-K)."""
+    ranks = np.arange(1, E + 1, dtype=np.float64)
+    logw = -s * np.log(ranks)
+    perm = rng.permutation(E)              # rank r -> expert id perm[r]
+    logw_by_id = np.empty(E)
+    logw_by_id[perm] = logw
+    g = rng.gumbel(size=(T, E))
+    keys = logw_by_id[None, :] + g
+    return np.argsort(-keys, axis=1, kind="stable")[:, :K].astype(np.int32)
+
+
+def softmax_weights(rng, T: int, K: int) -> np.ndarray:
+    logits = rng.standard_normal((T, K))
+    if K == 0:
+        return np.zeros((T, 0), dtype=np.float32)
+    z = np.exp(logits - logits.max(axis=1, keepdims=True))
+    return (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+def random_bytes(rng, n: int) -> np.ndarray:
+    return np.frombuffer(rng.bytes(n), dtype=np.uint8).copy()
+
+
+def make(T: int, E: int, K: int, I: int, O: int, dtype=torch.bfloat16,
+         scale_lo: int = 118, scale_hi: int = 124, picks: str = "uniform",
+         seed: int = 0, zipf_s: float = 1.2, name: str = "custom",
+         sel: np.ndarray | None = None) -> Workload:
+    """Draw one workload. ``sel`` may be supplied to fix the routing."""
+    if I % 32:
+        raise ValueError("I must be a multiple of 32")
+    G = I // 32
+    rng = np.random.default_rng(seed)
+    packed = random_bytes(rng, E * O * G * 16).reshape(E, O, G, 16)
+    scales = rng.integers(scale_lo, scale_hi + 1, size=(E, O, G),
+                          dtype=np.int64).astype(np.uint8)
+    x = _normal(rng, (T, I), dtype)
+    y_shared = _normal(rng, (T, O), dtype)
+    if sel is None:
+        if picks == "uniform":
+            sel = uniform_picks(rng, T, E, K)
+        elif picks == "zipf":
+            sel = zipf_picks(rng, T, E, K, zipf_s)
+        else:
+            raise ValueError(picks)
+    p = softmax_weights(rng, T, K)
+    return Workload(name=name, T=T, E=E, K=K, I=I, O=O, dtype=dtype, x=x,
+                    packed=torch.from_numpy(packed),
+                    scales=torch.from_numpy(scales),
+                    sel=torch.from_numpy(np.ascontiguousarray(sel, dtype=np.int32)),
+                    p=torch.from_numpy(p), y_shared=y_shared,
+                    meta=dict(seed=seed, picks=picks, scale_range=(scale_lo, scale_hi)))
+
+
+def named(name: str) -> Workload:
+    cfg = dict(CONFIGS[name])
+    return make(name=name, **cfg)
+
+
+def experts_touched(sel: torch.Tensor, E: int) -> int:
+    """Number of distinct expert ids in ``sel`` (a count, not layer math)."""
+    s = sel.reshape(-1).to(torch.int64)
+    s = s[(s >= 0) & (s < E)]
+    return int(torch.unique(s).numel())
