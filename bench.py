@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP4 routed expert linear on one GB300 (or N replicas).
+
+One step = one call of the whole path (routing bucketer, routed expert
+linear, combine) over one batch of the named workload, inputs resident in HBM.
+Default workload: decode (T=8 tokens, E=128 experts, K=4, I=2880, O=5760,
+bf16 tokens, MXFP4 weights), uniform distinct picks, seeded synthetic data.
+
+Prints one JSON line (rank 0). The path does not exchange data between
+GPUs: with --gpus N every rank runs its own replica (weak scaling) and the
+value is the bytes all ranks moved divided by the slowest rank's time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle, timed
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "routed-expert GB/s and TFLOP/s at 1 GB300, % of HBM/bf16 roofline"
+FLUSH_BYTES = 512 << 20          # > 129 MB of L2: written between steps
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------- accounting ----
+def token_bytes(wl):
+    import torch
+    return 2 if wl.dtype == torch.bfloat16 else 4
+
+
+def per_expert_bytes(wl):
+    G = wl.I // 32
+    return wl.O * G * 16 + wl.O * G           # packed bytes + scale bytes
+
+
+def path_bytes(wl, U, T=None):
+    """Algorithmic bytes of the whole path: selected experts' packed bytes and
+    scales, tokens, shared output read, output written, routing (sel + p)."""
+    T = wl.T if T is None else T
+    bx = token_bytes(wl)
+    return U * per_expert_bytes(wl) + T * wl.I * bx + 2 * T * wl.O * bx + T * wl.K * 8
+
+
+def linear_bytes(wl, U):
+    """Algorithmic bytes of the routed linear kernel: selected weights + tokens."""
+    return U * per_expert_bytes(wl) + wl.T * wl.I * token_bytes(wl)
+
+
+def path_flops(wl, T=None):
+    T = wl.T if T is None else T
+    return 2 * T * wl.K * wl.O * wl.I
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+LINEAR_SOURCES = ["mxfp4_routed_expert_route_gb300/csrc/gemv.cu",
+                  "mxfp4_routed_expert_route_gb300/csrc/common.cuh",
+                  "mxfp4_routed_expert_route_gb300/csrc/internal.h"]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source and this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[kernel]
+    except (OSError, ValueError, KeyError):
+        return None
+    if d.get("workload") != workload or d.get("source_sha256") != source_digest(LINEAR_SOURCES):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------- clocks ----
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str, interval_ms: int = 20):
+        self.cmd = ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}",
+                    "--format=csv,noheader,nounits", "-lms", str(interval_ms)]
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)              # let the first sample land before the load
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(device_index):
+    import torch
+    props = torch.cuda.get_device_properties(device_index)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        s = str(uuid)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    return vis.split(",")[device_index] if vis else str(device_index)
+
+
+# -------------------------------------------------------------- oracle -----
+def oracle_sample_time(wl, rows):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.expert_linear(wl.x, wl.packed, wl.scales, wl.sel, wl.p, wl.y_shared,
+                         rows=rows)
+    return time.perf_counter() - t0
+
+
+def sample_bytes(wl, rows):
+    import numpy as np
+    sel = wl.sel.numpy()[rows]
+    U = len(np.unique(sel[(sel >= 0) & (sel < wl.E)]))
+    return path_bytes(wl, U, T=len(rows))
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    """The oracle as it stands on this host's cores, on a bounded token sample."""
+    import numpy as np
+    import oracle
+    one = oracle_sample_time(wl, np.array([0]))
+    n = int(max(1, min(wl.T, budget_s / max(one, 1e-6))))
+    rows = np.arange(n)
+    t = oracle_sample_time(wl, rows)
+    return {"value": sample_bytes(wl, rows) / t / 1e9, "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"tokens 0..{n - 1} of the {wl.name} batch ({n}/{wl.T}), "
+                      f"all O={wl.O} rows, one run of {t:.2f} s"}
+
+
+def run_reference(args, rank):
+    """Reference arm: the float64 CPU oracle, timed as it stands."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from mxfp4_routed_expert_route_gb300 import workloads
+    oracle.build()
+    wl = workloads.named(args.workload)
+    one = oracle_sample_time(wl, np.array([0]))
+    budget = 120.0
+    n = int(max(1, min(wl.T, budget / max(one * (args.steps + args.warmup), 1e-9))))
+    rows = np.arange(n)
+    for _ in range(args.warmup):
+        oracle_sample_time(wl, rows)
+    times = [oracle_sample_time(wl, rows) for _ in range(args.steps)]
+    mean = sum(times) / len(times)
+    value = sample_bytes(wl, rows) / mean / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "K": wl.K, "I": wl.I,
+                   "O": wl.O, "sample_tokens": n, "seed": wl.meta["seed"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"tokens 0..{n - 1} of the {wl.name} batch per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- ours -----
+def run_ours(args, rank, world):
+    import ctypes
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from mxfp4_routed_expert_route_gb300 import (_native, build, mxfp4_expert_linear,
+                                                 workloads)
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    lib = _native.load()
+
+    wl = workloads.named(args.workload)
+    U = workloads.experts_touched(wl.sel, wl.E)
+    d = wl.device_tensors(dev)
+    out = torch.empty((wl.T, wl.O), dtype=wl.dtype, device=dev)
+    from mxfp4_routed_expert_route_gb300 import workspace_size
+    ws = torch.empty(max(1, workspace_size(wl.T, wl.E, wl.I, wl.O, wl.K, wl.dtype)),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"],
+                            d["y_shared"], out=out, workspace=ws)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+
+    def new_event():
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(stream)                 # creates the underlying CUDA event
+        return ev
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        flush.zero_()
+        step()
+    ev = [(new_event(), new_event()) for _ in range(K)]
+    lin = [(new_event(), new_event()) for _ in range(K)]
+    barrier()
+
+    sampler = ClockSampler(gpu_id_for(local))
+    sampler.start()
+    launches0 = lib.mxfp4el_kernel_launches()
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        lib.mxfp4el_set_stage_events(_native.STAGE_LINEAR,
+                                     ctypes.c_void_p(lin[i][0].cuda_event),
+                                     ctypes.c_void_p(lin[i][1].cuda_event))
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    barrier()
+    wall = time.perf_counter() - t0
+    launches = lib.mxfp4el_kernel_launches() - launches0
+    clocks = sampler.stop()
+    lib.mxfp4el_set_stage_events(_native.STAGE_LINEAR, None, None)
+
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    lin_ms = [a.elapsed_time(b) for a, b in lin]
+    total_s = sum(step_ms) / 1e3
+    t_local = torch.tensor([total_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
+    t_max = float(t_local.item())
+
+    # End to end through the public API: pinned host inputs in, result out.
+    x_h = wl.x.pin_memory()
+    sel_h, p_h, ys_h = wl.sel.pin_memory(), wl.p.pin_memory(), wl.y_shared.pin_memory()
+    out_h = torch.empty((wl.T, wl.O), dtype=wl.dtype).pin_memory()
+    x_d, sel_d, p_d, ys_d = (torch.empty_like(t, device=dev) for t in (x_h, sel_h, p_h, ys_h))
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        sel_d.copy_(sel_h, non_blocking=True)
+        p_d.copy_(p_h, non_blocking=True)
+        ys_d.copy_(ys_h, non_blocking=True)
+        mxfp4_expert_linear(x_d, d["packed"], d["scales"], sel_d, p_d, ys_d, out=out,
+                            workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(W):
+        flush.zero_()
+        e2e_step()
+    e2e_ev = [(new_event(), new_event()) for _ in range(K)]
+    barrier()
+    for i in range(K):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    barrier()
+    e2e_s = sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3
+    e2e_t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    h2d = sum(t.numel() * t.element_size() for t in (x_h, sel_h, p_h, ys_h))
+    d2h = out_h.numel() * out_h.element_size()
+
+    if rank != 0:
+        return
+    peaks, peaks_src = load_peaks()
+    bytes_step = path_bytes(wl, U)
+    flops_step = path_flops(wl)
+    value = world * bytes_step * K / t_max / 1e9
+    tflops = world * flops_step * K / t_max / 1e12
+    ms_step = t_max / K * 1e3
+    t_roof = max(bytes_step / (peaks["hbm_gbs"] * 1e9),
+                 flops_step / (peaks["bf16_tflops"] * 1e12))
+    lin_mean_s = sum(lin_ms) / len(lin_ms) / 1e3
+    lin_bytes = linear_bytes(wl, U)
+    achieved = lin_bytes / lin_mean_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "K": wl.K, "I": wl.I,
+                   "O": wl.O, "tokens": "bf16" if token_bytes(wl) == 2 else "fp32",
+                   "weights": "mxfp4 (e2m1 codes + e8m0 scale per 32)",
+                   "picks": wl.meta["picks"], "experts_touched": U,
+                   "seed": wl.meta["seed"], "parallelism": f"replicas x{world}",
+                   "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)"},
+        "tflops": tflops,
+        "path_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_step * 1e3,
+                          "frac": t_roof / (ms_step / 1e3), "bytes_alg": bytes_step,
+                          "flops_alg": flops_step, "peaks": peaks_src},
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel (routed expert linear)",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": f"hbm_gbs of {peaks_src}",
+                     "bytes_per_launch": lin_bytes, "launch_us": lin_mean_s * 1e6,
+                     "traffic": ncu_traffic("gemv_kernel", wl.name)},
+        "e2e": {"value": world * bytes_step * K / float(e2e_t.item()) / 1e9,
+                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": float(e2e_t.item()) / K * 1e3},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "wall_s": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * mxfp4_expert_linear.h -- C ABI of the MXFP4 routed expert linear for GB300.
+ *
+ * The operation (problem statement "MXFP4 Routed Expert Linear", Kimi K3,
+ * sections "What is stored in one group" through "Route, weight, and add the
+ * shared path"; the same problem stated formally as "MXFP4 Experts" on
+ * tensortonic):
+ *
+ *   W_e[o, 32 g + 2 j    ] = LUT[ b & 15 ] * 2^(s - 127)
+ *   W_e[o, 32 g + 2 j + 1] = LUT[ b >> 4 ] * 2^(s - 127)
+ *         b = packed_weights[e, o, g, j],  s = scale_bytes[e, o, g]
+ *   LUT   = { 0, .5, 1, 1.5, 2, 3, 4, 6, -0, -.5, -1, -1.5, -2, -3, -4, -6 }
+ *   out[t, :] = shared_output[t, :] + sum_{k < K} p[t, k] * W_{sel[t, k]} x[t, :]
+ *
+ * Only the experts some token selects are ever read ("Decode only selected
+ * experts"). The K routed contributions are added onto the shared output in
+ * slot order k = 0, 1, ..., K-1 in float32, then rounded once to the token
+ * dtype, so a call is deterministic: the same inputs give the same bits.
+ *
+ * Everything here is plain C: pointers, sizes and status codes. Every pointer
+ * argument of the compute calls is a DEVICE pointer (CUDA global memory of
+ * the device current on the calling thread) owned by the caller; the library
+ * never frees or retains them. Inputs are never written ("Requirements": do
+ * not mutate packed weights, routing data, or shared output). All GPU work is
+ * enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and
+ * the calls return without waiting for it.
+ *
+ * Dense row-major layouts (no padding, element strides as listed):
+ *   latent_tokens     (T, I)          token dtype (fp32 or bf16)
+ *   packed_weights    (E, O, G, 16)   uint8, G = I / 32
+ *   scale_bytes       (E, O, G)       uint8 (E8M0 exponent, bias 127)
+ *   selected_experts  (T, K)          int32 or int64 expert ids
+ *   mixture_weights   (T, K)          float32
+ *   shared_output     (T, O)          token dtype
+ *   out               (T, O)          token dtype, written by the call
+ */
+#ifndef MXFP4_EXPERT_LINEAR_H
+#define MXFP4_EXPERT_LINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. 0 is success; every error is negative and is returned before
+ * any GPU work is enqueued, except MXFP4EL_ERR_CUDA, which reports a failed
+ * launch or allocation (work enqueued before it may have run). */
+#define MXFP4EL_OK                     0
+#define MXFP4EL_ERR_INVALID_ARGUMENT  -1  /* null pointer, negative size,
+                                             I <= 0 or I % 32 != 0          */
+#define MXFP4EL_ERR_UNSUPPORTED_DTYPE -2  /* token or index dtype not listed */
+#define MXFP4EL_ERR_ALIAS             -3  /* out overlaps an input           */
+#define MXFP4EL_ERR_WORKSPACE         -4  /* caller workspace too small or
+                                             misaligned                      */
+#define MXFP4EL_ERR_CUDA              -5  /* a CUDA call failed              */
+#define MXFP4EL_ERR_TOO_LARGE         -6  /* a size exceeds the library limit */
+
+/* Token dtype: latent_tokens, shared_output and out share it ("Preserve the
+ * latent token dtype"). */
+#define MXFP4EL_DTYPE_F32   0
+#define MXFP4EL_DTYPE_BF16  1
+
+/* Dtype of selected_experts. */
+#define MXFP4EL_INDEX_I32   0
+#define MXFP4EL_INDEX_I64   1
+
+/*
+ * mxfp4_expert_linear -- the routed expert linear on one GPU.
+ *
+ * Sizes: T tokens, E experts, I input width (a positive multiple of 32,
+ * "Constraints"), O output width, K picks per token. T, E, O, K >= 0.
+ * T == 0 or O == 0 enqueues nothing. K == 0 copies shared_output to out.
+ *
+ * selected_experts: the pages require valid ids. An id outside [0, E) is
+ * not read from memory: that (t, k) pair contributes nothing, and it is
+ * counted in a per-device error counter read by mxfp4el_device_errors().
+ * A token may repeat an id; each slot is then added separately.
+ *
+ * mixture_weights are used as given (the pages state they sum to one per
+ * token; nothing renormalises them).
+ *
+ * Scratch memory (routing lists and one float32 partial per (pair, row),
+ * see mxfp4_expert_linear_workspace_size) is owned by the library: one
+ * grow-only buffer per (device, stream), grown with the stream-ordered
+ * cudaFreeAsync/cudaMallocAsync on `stream` the first time a call needs
+ * more, and kept until the process exits. A call that would grow it while
+ * `stream` is being captured into a CUDA graph returns MXFP4EL_ERR_WORKSPACE
+ * instead: make a first call of the largest size before capturing, or use
+ * mxfp4_expert_linear_with_workspace. Calls on one stream are ordered; calls
+ * on different streams use different buffers.
+ *
+ * Returns MXFP4EL_OK or one of the negative codes above.
+ */
+int mxfp4_expert_linear(const void* latent_tokens,
+                        const uint8_t* packed_weights,
+                        const uint8_t* scale_bytes,
+                        const void* selected_experts,
+                        const float* mixture_weights,
+                        const void* shared_output,
+                        void* out,
+                        int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                        int token_dtype, int index_dtype,
+                        void* stream);
+
+/*
+ * Bytes of scratch one call of these sizes needs when the caller supplies it
+ * (mxfp4_expert_linear_with_workspace). Returns 0 for a no-op call and
+ * (size_t)-1 for sizes the library rejects.
+ */
+size_t mxfp4_expert_linear_workspace_size(int64_t T, int64_t E, int64_t I,
+                                          int64_t O, int64_t K,
+                                          int token_dtype);
+
+/*
+ * Same operation with caller-owned scratch: `workspace` is a device buffer of
+ * at least mxfp4_expert_linear_workspace_size(...) bytes, 256-byte aligned.
+ * The library allocates nothing. The call may overwrite all of it; it must
+ * not overlap any argument, and two calls in flight at once (on different
+ * streams) must not share it. Errors as mxfp4_expert_linear, plus
+ * MXFP4EL_ERR_WORKSPACE when the buffer is too small or misaligned.
+ */
+int mxfp4_expert_linear_with_workspace(const void* latent_tokens,
+                                       const uint8_t* packed_weights,
+                                       const uint8_t* scale_bytes,
+                                       const void* selected_experts,
+                                       const float* mixture_weights,
+                                       const void* shared_output,
+                                       void* out,
+                                       int64_t T, int64_t E, int64_t I,
+                                       int64_t O, int64_t K,
+                                       int token_dtype, int index_dtype,
+                                       void* workspace,
+                                       size_t workspace_bytes,
+                                       void* stream);
+
+/*
+ * Synchronises `stream`, then returns in *bad_pairs the number of (t, k)
+ * pairs with an expert id outside [0, E) seen on the current device since the
+ * last call of this function, and resets that count to zero.
+ */
+int mxfp4el_device_errors(void* stream, int64_t* bad_pairs);
+
+/*
+ * Instrumentation for benchmarks. Stage ids name the kernels a call launches,
+ * in launch order. Once events are set for a stage, every later call records
+ * `start_event` on its stream just before that stage's kernel launch and
+ * `end_event` just after it (cudaEvent_t handles the caller created on the
+ * current device). NULL, NULL clears a stage. The setting is process-wide and
+ * not thread-safe against concurrent calls; it does not change any result.
+ * Returns MXFP4EL_ERR_INVALID_ARGUMENT for an unknown stage.
+ */
+#define MXFP4EL_STAGE_ROUTE    0   /* routing bucketer              */
+#define MXFP4EL_STAGE_LINEAR   1   /* routed expert linear (GEMV)   */
+#define MXFP4EL_STAGE_COMBINE  2   /* weighted combine onto y_shared */
+#define MXFP4EL_NUM_STAGES     3
+int mxfp4el_set_stage_events(int stage, void* start_event, void* end_event);
+
+/* Kernel launches this process has made through the library so far. */
+int64_t mxfp4el_kernel_launches(void);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* mxfp4el_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int mxfp4el_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_EXPERT_LINEAR_H */

@@ -1,0 +1,120 @@
+"""MXFP4 routed expert linear on GB300 (sm_103a).
+
+    y_t = y_shared_t + sum_k p[t, k] * W_{sel[t, k]} x_t
+
+with every expert matrix stored as packed E2M1 nibbles (low nibble first)
+and one E8M0 scale byte per (expert, output row, 32-value group), as in the
+problem statement "MXFP4 Routed Expert Linear" (Kimi K3).
+
+This module is the thin Python face of the C library
+``lib/libmxfp4_expert_linear.so`` (header ``include/mxfp4_expert_linear.h``):
+it checks and marshals arguments and passes raw device pointers and the
+current CUDA stream. Every step of the computation runs in the library's
+CUDA kernels; there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native
+
+__all__ = ["mxfp4_expert_linear", "workspace_size", "device_errors",
+           "LibraryNotBuilt", "MXFP4Error"]
+
+LibraryNotBuilt = _native.LibraryNotBuilt
+MXFP4Error = _native.MXFP4Error
+
+_TOKEN_DTYPES = {torch.float32: _native.DTYPE_F32,
+                 torch.bfloat16: _native.DTYPE_BF16}
+_INDEX_DTYPES = {torch.int32: _native.INDEX_I32, torch.int64: _native.INDEX_I64}
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() else None
+
+
+def workspace_size(T: int, E: int, I: int, O: int, K: int,
+                   dtype: torch.dtype = torch.bfloat16) -> int:
+    """Bytes of scratch a call of these sizes needs (caller-owned form)."""
+    n = _native.load().mxfp4_expert_linear_workspace_size(
+        T, E, I, O, K, _TOKEN_DTYPES[dtype])
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("sizes rejected by the library")
+    return n
+
+
+def mxfp4_expert_linear(latent_tokens: torch.Tensor, packed_weights: torch.Tensor,
+                        scale_bytes: torch.Tensor, selected_experts: torch.Tensor,
+                        mixture_weights: torch.Tensor, shared_output: torch.Tensor,
+                        out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """The routed and shared expert output, shaped like ``shared_output``.
+
+    Shapes: latent_tokens (T, I) fp32 or bf16; packed_weights (E, O, I/32, 16)
+    uint8; scale_bytes (E, O, I/32) uint8; selected_experts (T, K) int32 or
+    int64; mixture_weights (T, K) fp32; shared_output (T, O) in the token
+    dtype. All on one CUDA device. The result has the token's dtype and device
+    and is a new tensor unless ``out`` is given. Inputs are not modified.
+    ``workspace`` (uint8, at least :func:`workspace_size` bytes) may be
+    passed to reuse scratch; otherwise one is taken from torch's allocator.
+    """
+    x, w, s = latent_tokens, packed_weights, scale_bytes
+    sel, p, ys = selected_experts, mixture_weights, shared_output
+    if not x.is_cuda:
+        raise ValueError("latent_tokens must be a CUDA tensor")
+    dev = x.device
+    for name, t in (("packed_weights", w), ("scale_bytes", s),
+                    ("selected_experts", sel), ("mixture_weights", p),
+                    ("shared_output", ys)):
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, tokens on {dev}")
+    if x.dtype not in _TOKEN_DTYPES:
+        raise TypeError(f"unsupported token dtype {x.dtype}")
+    if ys.dtype != x.dtype:
+        raise TypeError("shared_output must have the token dtype")
+    if w.dtype != torch.uint8 or s.dtype != torch.uint8:
+        raise TypeError("packed_weights and scale_bytes must be uint8")
+    if sel.dtype not in _INDEX_DTYPES:
+        raise TypeError(f"unsupported index dtype {sel.dtype}")
+    if p.dtype != torch.float32:
+        raise TypeError("mixture_weights must be float32")
+    if x.dim() != 2 or w.dim() != 4 or s.dim() != 3 or sel.dim() != 2:
+        raise ValueError("expected x (T,I), packed (E,O,G,16), scales (E,O,G), sel (T,K)")
+    T, I = x.shape
+    E, O, G, sixteen = w.shape
+    K = sel.shape[1]
+    if sixteen != 16 or I != 32 * G or tuple(s.shape) != (E, O, G):
+        raise ValueError("packed/scale shapes do not match the token width")
+    if tuple(sel.shape) != (T, K) or tuple(p.shape) != (T, K) or tuple(ys.shape) != (T, O):
+        raise ValueError("routing or shared-output shape mismatch")
+    x, w, s, sel, p, ys = (t.contiguous() for t in (x, w, s, sel, p, ys))
+    if out is None:
+        out = torch.empty((T, O), dtype=x.dtype, device=dev)
+    elif out.shape != (T, O) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous (T, O) tensor of the token dtype")
+    lib = _native.load()
+    ws_bytes = workspace_size(T, E, I, O, K, x.dtype)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        rc = lib.mxfp4_expert_linear_with_workspace(
+            _ptr(x), _ptr(w), _ptr(s), _ptr(sel), _ptr(p), _ptr(ys), _ptr(out),
+            T, E, I, O, K, _TOKEN_DTYPES[x.dtype], _INDEX_DTYPES[sel.dtype],
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream))
+    _native.check(rc, "mxfp4_expert_linear")
+    return out
+
+
+def device_errors(device=None) -> int:
+    """Pairs with an out-of-range expert id since the last query (syncs)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    n = ctypes.c_int64(0)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        _native.check(_native.load().mxfp4el_device_errors(ctypes.c_void_p(stream),
+                                                           ctypes.byref(n)),
+                      "mxfp4el_device_errors")
+    return int(n.value)

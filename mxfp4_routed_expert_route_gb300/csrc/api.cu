@@ -1,0 +1,255 @@
+// api.cu -- the C ABI (include/mxfp4_expert_linear.h): argument checks,
+// workspace, and the launch sequence route -> GEMV -> combine on one stream.
+#include <algorithm>
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/mxfp4_expert_linear.h"
+#include "internal.h"
+
+namespace mxfp4el {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int64_t kMaxPairs = (int64_t)1 << 30;       // pair ids are int32
+constexpr int64_t kMaxDim = ((int64_t)1 << 31) - 1;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool sizes_ok(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
+  if (T > kMaxDim || E > kMaxDim || I > kMaxDim || O > kMaxDim || K > kMaxDim)
+    return false;
+  if (K > 0 && T > kMaxPairs / K) return false;
+  const int64_t P = T * K;
+  if (O > 0 && P > (((int64_t)1 << 62) / 4) / O) return false;
+  return true;
+}
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  if (an == 0 || bn == 0 || a == nullptr || b == nullptr) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+int validate(const void* x, const uint8_t* packed, const uint8_t* scales,
+             const void* sel, const float* p, const void* ys, void* out,
+             int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+             int token_dtype, int index_dtype) {
+  if (token_dtype != MXFP4EL_DTYPE_F32 && token_dtype != MXFP4EL_DTYPE_BF16)
+    return MXFP4EL_ERR_UNSUPPORTED_DTYPE;
+  if (index_dtype != MXFP4EL_INDEX_I32 && index_dtype != MXFP4EL_INDEX_I64)
+    return MXFP4EL_ERR_UNSUPPORTED_DTYPE;
+  if (T < 0 || E < 0 || O < 0 || K < 0 || I <= 0 || I % 32 != 0)
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (!sizes_ok(T, E, I, O, K)) return MXFP4EL_ERR_TOO_LARGE;
+  if (T == 0 || O == 0) return MXFP4EL_OK;
+  if (ys == nullptr || out == nullptr) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (K > 0 && (x == nullptr || sel == nullptr || p == nullptr))
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (K > 0 && E > 0 && (packed == nullptr || scales == nullptr))
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  // 128-bit loads of tokens and packed groups need 16-byte aligned bases.
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(packed)) % 16)
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  const size_t tb = token_dtype == MXFP4EL_DTYPE_BF16 ? 2 : 4;
+  const size_t ib = index_dtype == MXFP4EL_INDEX_I64 ? 8 : 4;
+  const size_t G = (size_t)I / 32;
+  const size_t out_bytes = (size_t)T * O * tb;
+  const void* inputs[] = {x, packed, scales, sel, p, ys};
+  const size_t sizes[] = {(size_t)T * I * tb, (size_t)E * O * G * 16,
+                          (size_t)E * O * G, (size_t)T * K * ib,
+                          (size_t)T * K * 4, (size_t)T * O * tb};
+  for (int i = 0; i < 6; ++i)
+    if (overlaps(out, out_bytes, inputs[i], sizes[i])) return MXFP4EL_ERR_ALIAS;
+  return MXFP4EL_OK;
+}
+
+std::atomic<int64_t> g_launches{0};
+
+struct StageEvents {
+  cudaEvent_t start = nullptr, end = nullptr;
+};
+StageEvents g_stage[MXFP4EL_NUM_STAGES];
+
+void mark(int stage, bool begin, cudaStream_t stream) {
+  const cudaEvent_t ev = begin ? g_stage[stage].start : g_stage[stage].end;
+  if (ev != nullptr) cudaEventRecord(ev, stream);
+}
+
+int run(const void* x, const uint8_t* packed, const uint8_t* scales,
+        const void* sel, const float* p, const void* ys, void* out, int64_t T,
+        int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype,
+        int index_dtype, const Workspace& ws, cudaStream_t stream) {
+  cudaError_t err;
+  if (K > 0) {
+    mark(MXFP4EL_STAGE_ROUTE, true, stream);
+    err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, stream);
+    mark(MXFP4EL_STAGE_ROUTE, false, stream);
+    if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
+    mark(MXFP4EL_STAGE_LINEAR, true, stream);
+    err = launch_gemv(x, token_dtype, packed, scales, ws.plan, ws.part, T, E,
+                      I, O, K, stream);
+    mark(MXFP4EL_STAGE_LINEAR, false, stream);
+    if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
+  }
+  mark(MXFP4EL_STAGE_COMBINE, true, stream);
+  err = launch_combine(ys, sel, index_dtype, p, ws.part, out, token_dtype, T, E,
+                       O, K, stream);
+  mark(MXFP4EL_STAGE_COMBINE, false, stream);
+  return err == cudaSuccess ? MXFP4EL_OK : MXFP4EL_ERR_CUDA;
+}
+
+// Library-owned workspace: one grow-only buffer per (device, stream).
+struct Cached {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_cache_mu;
+std::map<std::pair<int, cudaStream_t>, Cached>& cache() {
+  static auto* m = new std::map<std::pair<int, cudaStream_t>, Cached>();
+  return *m;
+}
+
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+bool carve_workspace(void* base, int64_t T, int64_t E, int64_t O, int64_t K,
+                     Workspace* ws) {
+  const int64_t P = T * K;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return base ? static_cast<char*>(base) + at : nullptr;
+  };
+  ws->plan.meta = reinterpret_cast<int*>(take(kMetaWords * sizeof(int)));
+  ws->plan.counts = reinterpret_cast<int*>(take((size_t)E * sizeof(int)));
+  ws->plan.offsets = reinterpret_cast<int*>(take((size_t)(E + 1) * sizeof(int)));
+  ws->plan.active = reinterpret_cast<int*>(take((size_t)E * sizeof(int)));
+  ws->plan.pair_list = reinterpret_cast<int*>(take((size_t)P * sizeof(int)));
+  const size_t wc_words = route_global_counter_words(E);
+  ws->wc_global = wc_words ? reinterpret_cast<int*>(take(wc_words * sizeof(int))) : nullptr;
+  ws->part = reinterpret_cast<float*>(take((size_t)P * (size_t)O * sizeof(float)));
+  ws->bytes = off;
+  return true;
+}
+
+}  // namespace mxfp4el
+
+using namespace mxfp4el;
+
+extern "C" size_t mxfp4_expert_linear_workspace_size(int64_t T, int64_t E, int64_t I,
+                                                     int64_t O, int64_t K,
+                                                     int token_dtype) {
+  if (token_dtype != MXFP4EL_DTYPE_F32 && token_dtype != MXFP4EL_DTYPE_BF16)
+    return (size_t)-1;
+  if (T < 0 || E < 0 || O < 0 || K < 0 || I <= 0 || I % 32 != 0) return (size_t)-1;
+  if (!sizes_ok(T, E, I, O, K)) return (size_t)-1;
+  if (T == 0 || O == 0) return 0;
+  Workspace ws;
+  carve_workspace(nullptr, T, E, O, K, &ws);
+  return ws.bytes;
+}
+
+extern "C" int mxfp4_expert_linear_with_workspace(
+    const void* latent_tokens, const uint8_t* packed_weights,
+    const uint8_t* scale_bytes, const void* selected_experts,
+    const float* mixture_weights, const void* shared_output, void* out,
+    int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype,
+    int index_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate(latent_tokens, packed_weights, scale_bytes, selected_experts,
+                    mixture_weights, shared_output, out, T, E, I, O, K,
+                    token_dtype, index_dtype);
+  if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
+  Workspace ws;
+  carve_workspace(nullptr, T, E, O, K, &ws);
+  if (workspace == nullptr || workspace_bytes < ws.bytes ||
+      reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return MXFP4EL_ERR_WORKSPACE;
+  carve_workspace(workspace, T, E, O, K, &ws);
+  return run(latent_tokens, packed_weights, scale_bytes, selected_experts,
+             mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
+             index_dtype, ws, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mxfp4_expert_linear(const void* latent_tokens,
+                                   const uint8_t* packed_weights,
+                                   const uint8_t* scale_bytes,
+                                   const void* selected_experts,
+                                   const float* mixture_weights,
+                                   const void* shared_output, void* out,
+                                   int64_t T, int64_t E, int64_t I, int64_t O,
+                                   int64_t K, int token_dtype, int index_dtype,
+                                   void* stream) {
+  int rc = validate(latent_tokens, packed_weights, scale_bytes, selected_experts,
+                    mixture_weights, shared_output, out, T, E, I, O, K,
+                    token_dtype, index_dtype);
+  if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
+  Workspace ws;
+  carve_workspace(nullptr, T, E, O, K, &ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MXFP4EL_ERR_CUDA;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    Cached& c = cache()[{dev, s}];
+    if (c.bytes < ws.bytes) {
+      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return MXFP4EL_ERR_CUDA;
+      if (cap != cudaStreamCaptureStatusNone) return MXFP4EL_ERR_WORKSPACE;
+      if (c.ptr) {
+        if (cudaFreeAsync(c.ptr, s) != cudaSuccess) return MXFP4EL_ERR_CUDA;
+        c.ptr = nullptr;
+        c.bytes = 0;
+      }
+      const size_t want = std::max(ws.bytes, c.bytes + c.bytes / 4);
+      if (cudaMallocAsync(&c.ptr, want, s) != cudaSuccess) {
+        c.ptr = nullptr;
+        return MXFP4EL_ERR_CUDA;
+      }
+      c.bytes = want;
+    }
+    base = c.ptr;
+  }
+  carve_workspace(base, T, E, O, K, &ws);
+  return run(latent_tokens, packed_weights, scale_bytes, selected_experts,
+             mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
+             index_dtype, ws, s);
+}
+
+extern "C" int mxfp4el_device_errors(void* stream, int64_t* bad_pairs) {
+  if (bad_pairs == nullptr) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  return read_and_reset_bad_pairs(static_cast<cudaStream_t>(stream), bad_pairs) ==
+                 cudaSuccess
+             ? MXFP4EL_OK
+             : MXFP4EL_ERR_CUDA;
+}
+
+extern "C" int mxfp4el_set_stage_events(int stage, void* start_event,
+                                        void* end_event) {
+  if (stage < 0 || stage >= MXFP4EL_NUM_STAGES) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  g_stage[stage].start = static_cast<cudaEvent_t>(start_event);
+  g_stage[stage].end = static_cast<cudaEvent_t>(end_event);
+  return MXFP4EL_OK;
+}
+
+extern "C" int64_t mxfp4el_kernel_launches(void) { return g_launches.load(); }
+
+extern "C" const char* mxfp4el_status_string(int status) {
+  switch (status) {
+    case MXFP4EL_OK: return "ok";
+    case MXFP4EL_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case MXFP4EL_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case MXFP4EL_ERR_ALIAS: return "output overlaps an input";
+    case MXFP4EL_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case MXFP4EL_ERR_CUDA: return "CUDA error";
+    case MXFP4EL_ERR_TOO_LARGE: return "size beyond library limits";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int mxfp4el_version(void) { return 100; }

@@ -1,0 +1,156 @@
+// common.cuh -- device helpers shared by the kernels of the MXFP4 routed
+// expert linear (problem statement "MXFP4 Routed Expert Linear", Kimi K3).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace mxfp4el {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// ---------------------------------------------------------------- loads ----
+// Packed weights are read exactly once per call: stream them past L1.
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Token rows are re-read by every output row: keep the default caching.
+__device__ __forceinline__ uint4 ld_u4(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// ------------------------------------------------------------ E2M1 codes ---
+// One packed byte holds two E2M1 codes: input position 2j in the low nibble
+// and 2j+1 in the high nibble ("What is stored in one group"). The hardware
+// conversion turns the low nibble into the low half of an f16x2 and the high
+// nibble into the high half; every E2M1 value is exact in f16 and in f32.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t word, uint32_t (&h)[4]) {
+  asm("{\n"
+      " .reg .b8 b0, b1, b2, b3;\n"
+      " mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      " cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      " cvt.rn.f16x2.e2m1x2 %3, b3;\n"
+      "}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(word));
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
+  float2 r;
+  asm("{\n"
+      " .reg .f16 lo, hi;\n"
+      " mov.b32 {lo, hi}, %2;\n"
+      " cvt.f32.f16 %0, lo;\n"
+      " cvt.f32.f16 %1, hi;\n"
+      "}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(h));
+  return r;
+}
+
+// d = a * b + c on two float32 lanes at once (Blackwell packed FMA).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n"
+      " .reg .b64 ra, rb, rc, rd;\n"
+      " mov.b64 ra, {%2, %3};\n"
+      " mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n"
+      " mov.b64 {%0, %1}, rd;\n"
+      "}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// ------------------------------------------------------------ E8M0 scale ---
+// The group factor 2^(s-127) ("Apply the shared group scale"), applied to a
+// float32 partial sum so that the product is exact for every byte s:
+// s = 1..254 is the normal float 2^(s-127); s = 0 is the subnormal 2^-127;
+// s = 255 (2^128, beyond float32) is applied as 2^127 after doubling the
+// partial. The caller multiplies the partial by `pre` and then by `factor`.
+struct E8M0 {
+  float factor;
+  float pre;
+};
+
+__device__ __forceinline__ E8M0 e8m0(uint32_t s) {
+  E8M0 r;
+  r.factor = __uint_as_float(min(s, 254u) << 23);
+  r.pre = 1.0f;
+  if (s == 0u) r.factor = __uint_as_float(0x00400000u);   // 2^-127
+  if (s == 255u) r.pre = 2.0f;
+  return r;
+}
+
+// ------------------------------------------------------------- tokens ------
+template <typename Tok> struct TokenIO;
+
+template <> struct TokenIO<float> {
+  // 32 consecutive token values (one group) as float32.
+  static __device__ __forceinline__ void load32(const float* p, float (&x)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint4 v = ld_u4(p + 4 * q);
+      x[4 * q + 0] = __uint_as_float(v.x);
+      x[4 * q + 1] = __uint_as_float(v.y);
+      x[4 * q + 2] = __uint_as_float(v.z);
+      x[4 * q + 3] = __uint_as_float(v.w);
+    }
+  }
+  static __device__ __forceinline__ float to_f32(float v) { return v; }
+  static __device__ __forceinline__ float from_f32(float v) { return v; }
+};
+
+template <> struct TokenIO<__nv_bfloat16> {
+  // bf16 -> f32 is exact: the bf16 bits are the top half of the f32 bits.
+  static __device__ __forceinline__ void load32(const __nv_bfloat16* p, float (&x)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 v = ld_u4(p + 8 * q);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        x[8 * q + 2 * m + 0] = __uint_as_float(w[m] << 16);
+        x[8 * q + 2 * m + 1] = __uint_as_float(w[m] & 0xffff0000u);
+      }
+    }
+  }
+  static __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f32(float v) { return __float2bfloat16_rn(v); }
+};
+
+// ------------------------------------------------------ warp reductions ----
+// Sums V = 2^L values over the 32 lanes of a warp with 2^L - 1 + (5 - L)
+// shuffles instead of 5 V: each level hands half of the remaining values to
+// the partner lane. On return every lane holds the full sum of value index
+// (lane >> (5 - L)) & (V - 1).
+template <int V>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be 2^L <= 32");
+  int off = 16;
+#pragma unroll
+  for (int half = V / 2; half >= 1; half /= 2, off /= 2) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFullMask, send, off);
+    }
+  }
+#pragma unroll
+  for (; off >= 1; off /= 2) v[0] += __shfl_xor_sync(kFullMask, v[0], off);
+  return v[0];
+}
+
+}  // namespace mxfp4el

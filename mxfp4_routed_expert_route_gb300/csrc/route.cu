@@ -1,0 +1,189 @@
+// route.cu -- the routing bucketer.
+//
+// Groups the T*K (token, slot) pairs by selected expert so that every expert
+// some token picked is read once, for all of its tokens, and no other expert
+// is read at all ("Decode only selected experts", problem statement "MXFP4
+// Routed Expert Linear", Kimi K3). It is a stable counting sort in one CTA:
+//   A. each warp owns a contiguous chunk of pairs and counts, per expert, the
+//      pairs of its chunk (warp-local counters, no atomics);
+//   B. per-expert totals, an exclusive prefix sum over experts (segment
+//      offsets), the compact ascending list of experts with at least one pair,
+//      and each warp's starting position inside every expert segment;
+//   C. each warp walks its chunk again and scatters pair ids into place.
+// Inside a segment the pairs keep their (token, slot) order. Pairs whose
+// expert id lies outside [0, E) are skipped and counted on the device.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mxfp4el {
+
+__device__ unsigned long long g_bad_pairs = 0;
+
+namespace {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+// Exclusive block-wide prefix sum of one int per thread; returns the prefix
+// and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(kFullMask, incl, off);
+    if (lane >= off) incl += n;
+  }
+  if (lane == 31) warp_buf[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_buf[lane];
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(kFullMask, wi, off);
+      if (lane >= off) wi += n;
+    }
+    warp_buf[lane] = wi - w;          // exclusive prefix of warp totals
+    if (lane == 31) warp_buf[32] = wi;
+  }
+  __syncthreads();
+  const int r = warp_buf[warp] + incl - v;
+  *total = warp_buf[32];
+  __syncthreads();
+  return r;
+}
+
+template <typename Idx>
+__global__ void __launch_bounds__(kRouteThreads, 1)
+route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
+             RoutePlan plan) {
+  extern __shared__ int smem_wc[];
+  __shared__ int warp_buf[33];
+  int* wc = wc_global != nullptr ? wc_global : smem_wc;   // [warp][expert]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lanes_below = (1u << lane) - 1u;
+
+  for (int i = threadIdx.x; i < kRouteWarps * E; i += kRouteThreads) wc[i] = 0;
+  __syncthreads();
+
+  const int64_t chunk = (P + kRouteWarps - 1) / kRouteWarps;
+  const int64_t pbeg = min(P, (int64_t)warp * chunk);
+  const int64_t pend = min(P, pbeg + chunk);
+  int* my_wc = wc + (size_t)warp * E;
+
+  // A. per-warp counts.
+  int bad = 0;
+  for (int64_t base = pbeg; base < pend; base += 32) {
+    const int64_t i = base + lane;
+    const bool in = i < pend;
+    const long long e = in ? (long long)sel[i] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    bad += (in && !valid) ? 1 : 0;
+    const unsigned peers = __match_any_sync(kFullMask, valid ? (int)e : -1);
+    if (valid && (peers & lanes_below) == 0) my_wc[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // B. totals, offsets, active list, per-warp segment starts.
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;
+  const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
+  int my_pairs = 0, my_active = 0;
+  for (int e = e0; e < e1; ++e) {
+    int c = 0;
+    for (int w = 0; w < kRouteWarps; ++w) c += wc[w * E + e];
+    plan.counts[e] = c;
+    my_pairs += c;
+    my_active += c > 0 ? 1 : 0;
+  }
+  int total_pairs, total_active;
+  int off = block_exclusive_scan(my_pairs, warp_buf, &total_pairs);
+  int act = block_exclusive_scan(my_active, warp_buf, &total_active);
+  for (int e = e0; e < e1; ++e) {
+    const int c = plan.counts[e];
+    plan.offsets[e] = off;
+    if (c > 0) plan.active[act++] = e;
+    int run = off;
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int cw = wc[w * E + e];
+      wc[w * E + e] = run;
+      run += cw;
+    }
+    off += c;
+  }
+  if (threadIdx.x == 0) {
+    plan.offsets[E] = total_pairs;
+    plan.meta[kMetaNumActive] = total_active;
+    plan.meta[kMetaNumPairs] = total_pairs;
+  }
+  __syncthreads();
+
+  // C. stable scatter of pair ids.
+  for (int64_t base = pbeg; base < pend; base += 32) {
+    const int64_t i = base + lane;
+    const bool in = i < pend;
+    const long long e = in ? (long long)sel[i] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(kFullMask, valid ? (int)e : -1);
+    int start = 0;
+    if (valid) start = my_wc[e];
+    __syncwarp();
+    if (valid) {
+      plan.pair_list[start + __popc(peers & lanes_below)] = (int)i;
+      if ((peers & lanes_below) == 0) my_wc[e] = start + __popc(peers);
+    }
+    __syncwarp();
+  }
+
+  // Invalid ids: count them for mxfp4el_device_errors().
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) bad += __shfl_xor_sync(kFullMask, bad, o);
+  if (lane == 0 && bad > 0) atomicAdd(&g_bad_pairs, (unsigned long long)bad);
+}
+
+}  // namespace
+
+size_t route_global_counter_words(int64_t E) {
+  return kRouteWarps * (size_t)E * sizeof(int) > kRouteSmemLimit
+             ? (size_t)kRouteWarps * (size_t)E : 0;
+}
+
+cudaError_t launch_route(const void* sel, int index_dtype, int64_t T, int64_t K,
+                         int64_t E, int* wc_global, const RoutePlan& plan,
+                         cudaStream_t stream) {
+  const int64_t P = T * K;
+  const size_t smem = wc_global ? 0 : kRouteWarps * (size_t)E * sizeof(int);
+  if (smem > 48 * 1024) {
+    cudaError_t err;
+    if (index_dtype == kIndexI64)
+      err = cudaFuncSetAttribute(route_kernel<int64_t>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    else
+      err = cudaFuncSetAttribute(route_kernel<int32_t>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  if (index_dtype == kIndexI64)
+    route_kernel<int64_t><<<1, kRouteThreads, smem, stream>>>(
+        static_cast<const int64_t*>(sel), P, (int)E, wc_global, plan);
+  else
+    route_kernel<int32_t><<<1, kRouteThreads, smem, stream>>>(
+        static_cast<const int32_t*>(sel), P, (int)E, wc_global, plan);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_reset_bad_pairs(cudaStream_t stream, int64_t* out) {
+  cudaError_t err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return err;
+  unsigned long long v = 0;
+  err = cudaMemcpyFromSymbol(&v, g_bad_pairs, sizeof(v));
+  if (err != cudaSuccess) return err;
+  const unsigned long long zero = 0;
+  err = cudaMemcpyToSymbol(g_bad_pairs, &zero, sizeof(zero));
+  *out = (int64_t)v;
+  return err;
+}
+
+}  // namespace mxfp4el

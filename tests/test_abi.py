@@ -1,0 +1,114 @@
+"""The C-ABI library: loads, exports what include/*.h declares, host checks.
+
+These run without a GPU: only calls that return before any CUDA work
+(argument checks, sizes, status strings) are made.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M):
+            if not m.group(0).lstrip().startswith(("#", "typedef")):
+                names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp4_routed_expert_route_gb300 import _native, build
+    build.build()
+    return _native.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert {"mxfp4_expert_linear", "mxfp4_expert_linear_with_workspace",
+            "mxfp4_expert_linear_workspace_size"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_header(lib):
+    from mxfp4_routed_expert_route_gb300 import _native
+    assert _declared_functions() == set(_native.SIGNATURES)
+
+
+def test_status_strings(lib):
+    from mxfp4_routed_expert_route_gb300 import _native as n
+    for code in (n.OK, n.ERR_INVALID_ARGUMENT, n.ERR_UNSUPPORTED_DTYPE, n.ERR_ALIAS,
+                 n.ERR_WORKSPACE, n.ERR_CUDA, n.ERR_TOO_LARGE):
+        assert lib.mxfp4el_status_string(code) not in (None, b"unknown status")
+    assert lib.mxfp4el_status_string(12345) == b"unknown status"
+    assert lib.mxfp4el_version() >= 100
+
+
+def test_header_constants_match_binding():
+    from mxfp4_routed_expert_route_gb300 import _native as n
+    text = open(os.path.join(ROOT, "include", "mxfp4_expert_linear.h")).read()
+    defs = dict(re.findall(r"#define\s+MXFP4EL_(\w+)\s+(-?\d+)", text))
+    for name, val in defs.items():
+        assert getattr(n, name) == int(val), name
+
+
+def test_workspace_size(lib):
+    ws = lib.mxfp4_expert_linear_workspace_size
+    bad = ctypes.c_size_t(-1).value
+    assert ws(0, 4, 64, 8, 2, 0) == 0
+    assert ws(4, 4, 64, 0, 2, 0) == 0
+    assert ws(4, 4, 60, 8, 2, 0) == bad            # I not a multiple of 32
+    assert ws(4, 4, 64, 8, 2, 7) == bad            # unknown dtype
+    assert ws(-1, 4, 64, 8, 2, 0) == bad
+    assert ws(1 << 40, 4, 64, 8, 2, 0) == bad       # too large
+    n = ws(8, 128, 2880, 5760, 4, 1)
+    assert n >= 8 * 4 * 5760 * 4 and n % 256 == 0
+    assert ws(8, 128, 2880, 5760, 4, 0) == n       # scratch is float32 either way
+
+
+def test_argument_checks_return_before_gpu_work(lib):
+    from mxfp4_routed_expert_route_gb300 import _native as n
+    f = lib.mxfp4_expert_linear
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake] * 7
+    assert f(*args, 4, 4, 60, 8, 2, 0, 0, None) == n.ERR_INVALID_ARGUMENT
+    assert f(*args, 4, 4, 64, 8, 2, 9, 0, None) == n.ERR_UNSUPPORTED_DTYPE
+    assert f(*args, 4, 4, 64, 8, 2, 0, 5, None) == n.ERR_UNSUPPORTED_DTYPE
+    assert f(*args, -4, 4, 64, 8, 2, 0, 0, None) == n.ERR_INVALID_ARGUMENT
+    assert f(*args, 0, 4, 64, 8, 2, 0, 0, None) == n.OK            # T == 0: no-op
+    assert f(*args, 4, 4, 64, 0, 2, 0, 0, None) == n.OK            # O == 0: no-op
+    nulls = [None] * 7
+    assert f(*nulls, 4, 4, 64, 8, 2, 0, 0, None) == n.ERR_INVALID_ARGUMENT
+    # out aliasing the shared output is refused
+    x = ctypes.c_void_p(1 << 24)
+    w = ctypes.c_void_p(1 << 28)
+    ys = ctypes.c_void_p(1 << 32)
+    assert f(x, w, fake, fake, fake, ys, ys, 4, 4, 64, 8, 2, 0, 0, None) == n.ERR_ALIAS
+    # misaligned token pointer
+    assert f(ctypes.c_void_p((1 << 24) + 4), w, fake, fake, fake, ys,
+             ctypes.c_void_p(1 << 36), 4, 4, 64, 8, 2, 0, 0, None) == n.ERR_INVALID_ARGUMENT
+    g = lib.mxfp4_expert_linear_with_workspace
+    out = ctypes.c_void_p(1 << 36)
+    assert g(x, w, fake, fake, fake, ys, out, 4, 4, 64, 8, 2, 0, 0, None, 0,
+             None) == n.ERR_WORKSPACE
+    assert g(x, w, fake, fake, fake, ys, out, 4, 4, 64, 8, 2, 0, 0,
+             ctypes.c_void_p((1 << 40) + 16), 1 << 20, None) == n.ERR_WORKSPACE
+
+
+def test_product_path_has_no_oracle_reference():
+    pkg = os.path.join(ROOT, "mxfp4_routed_expert_route_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text, f
