@@ -154,7 +154,8 @@ cudaError_t launch_route(const void* sel, int index_dtype, int64_t T, int64_t K,
                          cudaStream_t stream) {
   const int64_t P = T * K;
   const size_t smem = wc_global ? 0 : kRouteWarps * (size_t)E * sizeof(int);
-  if (smem > 48 * 1024) {
+  // Dynamic plus static shared memory above 48 KiB needs the opt-in.
+  if (smem > 40 * 1024) {
     cudaError_t err;
     if (index_dtype == kIndexI64)
       err = cudaFuncSetAttribute(route_kernel<int64_t>,
