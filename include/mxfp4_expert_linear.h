@@ -136,6 +136,47 @@ int mxfp4_expert_linear_with_workspace(const void* latent_tokens,
                                        void* stream);
 
 /*
+ * mxfp4_expert_linear_static_scratch -- the same operation for callers that
+ * cannot allocate device memory (for example a serving process whose memory
+ * budget is fixed at start-up, or a plugin of a host framework that owns
+ * every device allocation). The pages have no counterpart: it is a property
+ * of this library's interface, not of the method.
+ *
+ * Arguments, results and errors are those of mxfp4_expert_linear. The caller
+ * still passes every input and `out`; the scratch lives in a fixed device
+ * array compiled into the library, mxfp4_expert_linear_static_scratch_bytes()
+ * bytes (8 MiB) on every GPU that loads the library, held until the process
+ * exits. The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine). Sizes whose scratch
+ * (mxfp4_expert_linear_workspace_size) exceeds the array are rejected with
+ * MXFP4EL_ERR_TOO_LARGE before any GPU work. The scratch is dominated by one
+ * float32 per (token, slot, output row), so T*K*O may reach about two
+ * million: a batch of T=16 tokens, K=8, O=4096 uses about 2 MiB of it.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with the device current); make that first
+ * call before any stream capture. Every call on a device shares the one
+ * array, which keeps the previous call's contents; nothing in it needs to
+ * start at zero, because the kernels initialise everything they read. Calls
+ * that overlap on the GPU (on different streams, or from different threads
+ * without ordering) race on the array and give undefined results: order them.
+ */
+int mxfp4_expert_linear_static_scratch(const void* latent_tokens,
+                                       const uint8_t* packed_weights,
+                                       const uint8_t* scale_bytes,
+                                       const void* selected_experts,
+                                       const float* mixture_weights,
+                                       const void* shared_output,
+                                       void* out,
+                                       int64_t T, int64_t E, int64_t I,
+                                       int64_t O, int64_t K,
+                                       int token_dtype, int index_dtype,
+                                       void* stream);
+
+/* Size in bytes of the fixed scratch array of the entry point above. */
+size_t mxfp4_expert_linear_static_scratch_bytes(void);
+
+/*
  * Synchronises `stream`, then returns in *bad_pairs the number of (t, k)
  * pairs with an expert id outside [0, E) seen on the current device since the
  * last call of this function, and resets that count to zero.

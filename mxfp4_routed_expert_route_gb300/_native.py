@@ -42,6 +42,10 @@ SIGNATURES = {
     "mxfp4_expert_linear_with_workspace": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64,
                                                   _I64, _I64, _I64, _I64, _INT, _INT,
                                                   _P, _SZ, _P]),
+    "mxfp4_expert_linear_static_scratch": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64,
+                                                  _I64, _I64, _I64, _I64, _INT, _INT,
+                                                  _P]),
+    "mxfp4_expert_linear_static_scratch_bytes": (_SZ, []),
     "mxfp4el_device_errors": (_INT, [_P, ctypes.POINTER(_I64)]),
     "mxfp4el_set_stage_events": (_INT, [_INT, _P, _P]),
     "mxfp4el_kernel_launches": (_I64, []),
