@@ -149,9 +149,10 @@ int mxfp4_expert_linear_with_workspace(const void* latent_tokens,
  * exits. The call allocates nothing (no cudaMalloc, cudaFree or allocating
  * library routine). Sizes whose scratch
  * (mxfp4_expert_linear_workspace_size) exceeds the array are rejected with
- * MXFP4EL_ERR_TOO_LARGE before any GPU work. The scratch is dominated by one
- * float32 per (token, slot, output row), so T*K*O may reach about two
- * million: a batch of T=16 tokens, K=8, O=4096 uses about 2 MiB of it.
+ * MXFP4EL_ERR_TOO_LARGE before any GPU work. The scratch is dominated by
+ * float32 partial results per (token, slot, output row); for example a batch
+ * of T=8 tokens, K=4, I=2880, O=5760 needs about 2.2 MiB and fits, while
+ * T=16, K=8, I=7168, O=4096 needs about 14 MiB and is refused.
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with the device current); make that first
@@ -184,6 +185,16 @@ size_t mxfp4_expert_linear_static_scratch_bytes(void);
 int mxfp4el_device_errors(void* stream, int64_t* bad_pairs);
 
 /*
+ * Synchronises `stream`, then returns in *count the number of kernel waits
+ * (on a copy or on another warp of the same CTA) that gave up after their
+ * time limit on the current device since the last call, and resets it. Every
+ * wait in the library's kernels is bounded (2 s); a kernel whose wait gave up
+ * returns early, so the outputs of the calls involved are not valid. A
+ * healthy device always reports 0.
+ */
+int mxfp4el_wait_timeouts(void* stream, int64_t* count);
+
+/*
  * Instrumentation for benchmarks. Stage ids name the kernels a call launches,
  * in launch order. Once events are set for a stage, every later call records
  * `start_event` on its stream just before that stage's kernel launch and
@@ -192,7 +203,7 @@ int mxfp4el_device_errors(void* stream, int64_t* bad_pairs);
  * not thread-safe against concurrent calls; it does not change any result.
  * Returns MXFP4EL_ERR_INVALID_ARGUMENT for an unknown stage.
  */
-#define MXFP4EL_STAGE_ROUTE    0   /* routing bucketer              */
+#define MXFP4EL_STAGE_ROUTE    0   /* routing bucketer (+ token prep) */
 #define MXFP4EL_STAGE_LINEAR   1   /* routed expert linear (GEMV)   */
 #define MXFP4EL_STAGE_COMBINE  2   /* weighted combine onto y_shared */
 #define MXFP4EL_NUM_STAGES     3

@@ -20,7 +20,7 @@ import torch
 
 from . import _native
 
-__all__ = ["mxfp4_expert_linear", "workspace_size", "device_errors",
+__all__ = ["mxfp4_expert_linear", "workspace_size", "device_errors", "wait_timeouts",
            "LibraryNotBuilt", "MXFP4Error"]
 
 LibraryNotBuilt = _native.LibraryNotBuilt
@@ -117,4 +117,18 @@ def device_errors(device=None) -> int:
         _native.check(_native.load().mxfp4el_device_errors(ctypes.c_void_p(stream),
                                                            ctypes.byref(n)),
                       "mxfp4el_device_errors")
+    return int(n.value)
+
+
+def wait_timeouts(device=None) -> int:
+    """Kernel waits that gave up after their time limit since the last query
+    (syncs). Always 0 on a healthy device; a nonzero count means the outputs
+    of the calls since the last query are not valid."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    n = ctypes.c_int64(0)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        _native.check(_native.load().mxfp4el_wait_timeouts(ctypes.c_void_p(stream),
+                                                           ctypes.byref(n)),
+                      "mxfp4el_wait_timeouts")
     return int(n.value)

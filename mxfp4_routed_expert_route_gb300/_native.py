@@ -47,6 +47,7 @@ SIGNATURES = {
                                                   _P]),
     "mxfp4_expert_linear_static_scratch_bytes": (_SZ, []),
     "mxfp4el_device_errors": (_INT, [_P, ctypes.POINTER(_I64)]),
+    "mxfp4el_wait_timeouts": (_INT, [_P, ctypes.POINTER(_I64)]),
     "mxfp4el_set_stage_events": (_INT, [_INT, _P, _P]),
     "mxfp4el_kernel_launches": (_I64, []),
     "mxfp4el_status_string": (ctypes.c_char_p, [_INT]),

@@ -84,19 +84,23 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
         int index_dtype, const Workspace& ws, cudaStream_t stream) {
   cudaError_t err;
   if (K > 0) {
+    unsigned long long* status = device_status_words();
+    if (status == nullptr) return MXFP4EL_ERR_CUDA;
     mark(MXFP4EL_STAGE_ROUTE, true, stream);
     err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, stream);
+    if (err == cudaSuccess && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I))
+      err = launch_prep_tokens(x, ws.x16, ws.sigma, T, I, stream);
     mark(MXFP4EL_STAGE_ROUTE, false, stream);
     if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
     mark(MXFP4EL_STAGE_LINEAR, true, stream);
-    err = launch_gemv(x, token_dtype, packed, scales, ws.plan, ws.part, T, E,
-                      I, O, K, stream);
+    err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, packed, scales, ws.plan,
+                      ws.part, status, T, E, I, O, K, stream);
     mark(MXFP4EL_STAGE_LINEAR, false, stream);
     if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
   }
   mark(MXFP4EL_STAGE_COMBINE, true, stream);
-  err = launch_combine(ys, sel, index_dtype, p, ws.part, out, token_dtype, T, E,
-                       O, K, stream);
+  err = launch_combine(ys, sel, index_dtype, p, ws.part, gemv_partial_columns(I), out,
+                       token_dtype, T, E, O, K, stream);
   mark(MXFP4EL_STAGE_COMBINE, false, stream);
   return err == cudaSuccess ? MXFP4EL_OK : MXFP4EL_ERR_CUDA;
 }
@@ -116,8 +120,8 @@ std::map<std::pair<int, cudaStream_t>, Cached>& cache() {
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-bool carve_workspace(void* base, int64_t T, int64_t E, int64_t O, int64_t K,
-                     Workspace* ws) {
+bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
+                     int64_t K, int token_dtype, Workspace* ws) {
   const int64_t P = T * K;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -132,7 +136,11 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t O, int64_t K,
   ws->plan.pair_list = reinterpret_cast<int*>(take((size_t)P * sizeof(int)));
   const size_t wc_words = route_global_counter_words(E);
   ws->wc_global = wc_words ? reinterpret_cast<int*>(take(wc_words * sizeof(int))) : nullptr;
-  ws->part = reinterpret_cast<float*>(take((size_t)P * (size_t)O * sizeof(float)));
+  const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && K > 0;
+  ws->x16 = prep ? reinterpret_cast<__half*>(take((size_t)T * I * sizeof(__half))) : nullptr;
+  ws->sigma = prep ? reinterpret_cast<int*>(take((size_t)T * sizeof(int))) : nullptr;
+  const size_t ncol = (size_t)gemv_partial_columns(I);
+  ws->part = reinterpret_cast<float*>(take((size_t)P * ncol * (size_t)O * sizeof(float)));
   ws->bytes = off;
   return true;
 }
@@ -150,7 +158,7 @@ extern "C" size_t mxfp4_expert_linear_workspace_size(int64_t T, int64_t E, int64
   if (!sizes_ok(T, E, I, O, K)) return (size_t)-1;
   if (T == 0 || O == 0) return 0;
   Workspace ws;
-  carve_workspace(nullptr, T, E, O, K, &ws);
+  carve_workspace(nullptr, T, E, I, O, K, token_dtype, &ws);
   return ws.bytes;
 }
 
@@ -165,11 +173,11 @@ extern "C" int mxfp4_expert_linear_with_workspace(
                     token_dtype, index_dtype);
   if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
   Workspace ws;
-  carve_workspace(nullptr, T, E, O, K, &ws);
+  carve_workspace(nullptr, T, E, I, O, K, token_dtype, &ws);
   if (workspace == nullptr || workspace_bytes < ws.bytes ||
       reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return MXFP4EL_ERR_WORKSPACE;
-  carve_workspace(workspace, T, E, O, K, &ws);
+  carve_workspace(workspace, T, E, I, O, K, token_dtype, &ws);
   return run(latent_tokens, packed_weights, scale_bytes, selected_experts,
              mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
              index_dtype, ws, static_cast<cudaStream_t>(stream));
@@ -189,7 +197,7 @@ extern "C" int mxfp4_expert_linear(const void* latent_tokens,
                     token_dtype, index_dtype);
   if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
   Workspace ws;
-  carve_workspace(nullptr, T, E, O, K, &ws);
+  carve_workspace(nullptr, T, E, I, O, K, token_dtype, &ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MXFP4EL_ERR_CUDA;
@@ -215,7 +223,7 @@ extern "C" int mxfp4_expert_linear(const void* latent_tokens,
     }
     base = c.ptr;
   }
-  carve_workspace(base, T, E, O, K, &ws);
+  carve_workspace(base, T, E, I, O, K, token_dtype, &ws);
   return run(latent_tokens, packed_weights, scale_bytes, selected_experts,
              mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
              index_dtype, ws, s);
@@ -223,8 +231,16 @@ extern "C" int mxfp4_expert_linear(const void* latent_tokens,
 
 extern "C" int mxfp4el_device_errors(void* stream, int64_t* bad_pairs) {
   if (bad_pairs == nullptr) return MXFP4EL_ERR_INVALID_ARGUMENT;
-  return read_and_reset_bad_pairs(static_cast<cudaStream_t>(stream), bad_pairs) ==
-                 cudaSuccess
+  return read_and_reset_status(static_cast<cudaStream_t>(stream), kStatusBadPairs,
+                               bad_pairs) == cudaSuccess
+             ? MXFP4EL_OK
+             : MXFP4EL_ERR_CUDA;
+}
+
+extern "C" int mxfp4el_wait_timeouts(void* stream, int64_t* count) {
+  if (count == nullptr) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  return read_and_reset_status(static_cast<cudaStream_t>(stream), kStatusWaitTimeouts,
+                               count) == cudaSuccess
              ? MXFP4EL_OK
              : MXFP4EL_ERR_CUDA;
 }

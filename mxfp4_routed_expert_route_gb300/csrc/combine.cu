@@ -2,6 +2,9 @@
 //
 //   out[t, o] = round( y_shared[t, o] + sum_{k = 0}^{K-1} p[t, k] * part[t*K+k, o] )
 //
+// where part[t*K+k, o] is itself the sum, in column order c = 0..ncol-1, of
+// the partial results the GEMV wrote for the input-group columns.
+//
 // ("Route, weight, and add the shared path", problem statement "MXFP4 Routed
 // Expert Linear", Kimi K3: start from the shared output and add the weighted
 // routed contributions.) The sum runs in float32 in slot order k = 0..K-1 and
@@ -17,7 +20,7 @@ namespace {
 template <typename Tok, typename Idx>
 __global__ void __launch_bounds__(256)
 combine_kernel(const Tok* __restrict__ ys, const Idx* __restrict__ sel,
-               const float* __restrict__ p, const float* __restrict__ part,
+               const float* __restrict__ p, const float* __restrict__ part, int ncol,
                Tok* __restrict__ out, int64_t T, int64_t O, int K, int64_t E) {
   const int64_t n = T * O;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
@@ -28,7 +31,12 @@ combine_kernel(const Tok* __restrict__ ys, const Idx* __restrict__ sel,
     for (int k = 0; k < K; ++k) {
       const int64_t pk = t * K + k;
       const long long e = (long long)sel[pk];
-      if (e >= 0 && e < E) acc = fmaf(p[pk], part[pk * O + o], acc);
+      if (e >= 0 && e < E) {
+        const float* pp = part + pk * ncol * O + o;
+        float v = pp[0];
+        for (int c = 1; c < ncol; ++c) v += pp[(int64_t)c * O];
+        acc = fmaf(p[pk], v, acc);
+      }
     }
     out[idx] = TokenIO<Tok>::from_f32(acc);
   }
@@ -36,26 +44,26 @@ combine_kernel(const Tok* __restrict__ ys, const Idx* __restrict__ sel,
 
 template <typename Tok, typename Idx>
 cudaError_t launch_typed(const Tok* ys, const Idx* sel, const float* p,
-                         const float* part, Tok* out, int64_t T, int64_t E,
+                         const float* part, int ncol, Tok* out, int64_t T, int64_t E,
                          int64_t O, int64_t K, cudaStream_t stream) {
   const int64_t n = T * O;
   if (n == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 16);
   combine_kernel<Tok, Idx><<<(unsigned)blocks, 256, 0, stream>>>(
-      ys, sel, p, part, out, T, O, (int)K, E);
+      ys, sel, p, part, ncol, out, T, O, (int)K, E);
   note_launch();
   return cudaGetLastError();
 }
 
 template <typename Tok>
 cudaError_t launch_by_index(const Tok* ys, const void* sel, int index_dtype,
-                            const float* p, const float* part, Tok* out,
+                            const float* p, const float* part, int ncol, Tok* out,
                             int64_t T, int64_t E, int64_t O, int64_t K,
                             cudaStream_t stream) {
   if (index_dtype == kIndexI64)
-    return launch_typed(ys, static_cast<const int64_t*>(sel), p, part, out, T,
+    return launch_typed(ys, static_cast<const int64_t*>(sel), p, part, ncol, out, T,
                         E, O, K, stream);
-  return launch_typed(ys, static_cast<const int32_t*>(sel), p, part, out, T, E,
+  return launch_typed(ys, static_cast<const int32_t*>(sel), p, part, ncol, out, T, E,
                       O, K, stream);
 }
 
@@ -63,14 +71,14 @@ cudaError_t launch_by_index(const Tok* ys, const void* sel, int index_dtype,
 
 cudaError_t launch_combine(const void* y_shared, const void* sel,
                            int index_dtype, const float* p, const float* part,
-                           void* out, int token_dtype, int64_t T, int64_t E,
-                           int64_t O, int64_t K, cudaStream_t stream) {
+                           int ncol, void* out, int token_dtype, int64_t T,
+                           int64_t E, int64_t O, int64_t K, cudaStream_t stream) {
   if (token_dtype == kTokenBF16)
     return launch_by_index(static_cast<const __nv_bfloat16*>(y_shared), sel,
-                           index_dtype, p, part,
+                           index_dtype, p, part, ncol,
                            static_cast<__nv_bfloat16*>(out), T, E, O, K, stream);
   return launch_by_index(static_cast<const float*>(y_shared), sel, index_dtype,
-                         p, part, static_cast<float*>(out), T, E, O, K, stream);
+                         p, part, ncol, static_cast<float*>(out), T, E, O, K, stream);
 }
 
 }  // namespace mxfp4el

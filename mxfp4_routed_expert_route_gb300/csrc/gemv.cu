@@ -7,71 +7,441 @@
 // Kimi K3, sections "What is stored in one group" to "Reconstruct the matrix
 // in the right orientation").
 //
-// The kernel is bound by HBM: every byte of a selected expert is read once.
-//   * CTA = 8 warps over (expert slot u, tile of 8 R output rows); slots past
-//     the number of active experts exit at once.
-//   * lane = one 32-value group: a 128-bit load brings its 16 packed bytes,
-//     one byte load its scale. R rows per warp keep R loads in flight per lane
-//     and let the lane's token values be reused across the R rows.
-//   * decode in registers: the hardware E2M1 -> f16x2 conversion, widened to
-//     f32, then packed f32x2 FMAs against the token; each group's partial is
-//     scaled by its exact power of two and accumulated in float32.
-//   * the expert's tokens are taken NT at a time; within a pass the decoded
-//     group is reused for every token. A later pass re-reads the rows from L2.
-//   * one shuffle reduce-scatter sums the R x NT accumulators across lanes.
+// The work is bound by HBM: every byte of a selected expert is read once.
+//
+// gemv_stream_kernel (the main kernel): persistent CTAs, one per SM. A work
+// unit is (selected expert, tile of 16*RW consecutive output rows); the
+// tile's packed bytes, and its scale bytes, are contiguous in memory, so a
+// producer warp moves each unit with one or two 1D bulk copies (TMA engine)
+// into a ring of shared-memory stages guarded by mbarriers. Each CTA takes a
+// contiguous range of units, so it reads one expert's token list once and
+// streams consecutive memory. Sixteen consumer warps each own RW rows of the
+// tile: lane = one 32-value group, decoded in
+// registers by the hardware E2M1 -> f16x2 conversion and multiplied against
+// the token, then reduced across lanes with one shuffle reduce-scatter. The
+// expert's tokens are taken NT at a time straight from shared memory, so a
+// unit's weights are read from HBM once whatever the number of tokens.
+//
+// Arithmetic. fp32 tokens: products and sums in float32 (f32x2 FMAs).
+// bf16 tokens: each token is scaled by a power of two 2^sigma_t chosen so
+// that max|x_t| 2^sigma_t lies in [2^8, 2^9) and rounded to f16 (exact for
+// bf16 values in f16's normal range); within a group the 32 products form
+// two f16x2 chains of 8 (fma.rn.f16x2) that are added in f16, so each half
+// sums 16 products with at most 8 roundings; the two halves are widened to
+// float32, scaled by the group's exact power of two and accumulated in
+// float32. The group error is <= 8 * 2^-11 of the sum of |terms| (plus f16
+// subnormal rounding, absolute <= 2^-25 * 2^-sigma_t per token value), and
+// |partial| <= 16 * 6 * 2^9 keeps every f16 sum inside f16's range.
+//
+// gemv_direct_kernel: the same arithmetic in float32 straight from global
+// memory (no staging), for rows too wide for a shared-memory stage.
+#include <cuda_fp16.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace mxfp4el {
 namespace {
 
-constexpr int kGemvThreads = 256;
-constexpr int kGemvWarps = kGemvThreads / 32;
+constexpr int kConsumerWarps = 15;
+constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
+constexpr int kDirectThreads = 256;
+constexpr int kDirectWarps = kDirectThreads / 32;
+constexpr size_t kMaxStageBytes = 64 * 1024;
+constexpr size_t kSmemBudget = 220 * 1024;
+constexpr int kMaxStages = 8;
 
-// Dot product of one packed group (16 bytes = 32 codes) with 32 token values.
-// The result is the unscaled group partial sum_j LUT[code_j] * x_j.
-__device__ __forceinline__ float dot_group(const uint4& w, const float (&x)[32]) {
-  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+template <int V> struct Log2 { static constexpr int value = 1 + Log2<V / 2>::value; };
+template <> struct Log2<1> { static constexpr int value = 0; };
+
+// ------------------------------------------------------------ group dots ---
+// 16 packed bytes -> 16 f16x2 words: word i holds input positions 2i (low
+// half, from the low nibble) and 2i+1 (high half).
+__device__ __forceinline__ void decode_group(const uint4& v, uint32_t (&w)[16]) {
+  const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t h[4];
     e2m1x8_to_f16x2x4(words[q], h);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      // byte 4q+b holds input positions 8q+2b (low nibble) and 8q+2b+1
-      const float2 wf = f16x2_to_f32x2(h[b]);
-      const float2 xv = make_float2(x[8 * q + 2 * b], x[8 * q + 2 * b + 1]);
-      if (b & 1) a1 = ffma2(wf, xv, a1);
-      else       a0 = ffma2(wf, xv, a0);
-    }
+    for (int b = 0; b < 4; ++b) w[4 * q + b] = h[b];
+  }
+}
+
+// sum_j w_j x_j over one group: two f16x2 chains of 8 products, added in
+// f16, then the two halves widened to float32.
+__device__ __forceinline__ float dot_group_f16(const uint32_t (&w)[16], const uint32_t (&x)[16]) {
+  uint32_t a0 = hmul2(w[0], x[0]);
+  uint32_t a1 = hmul2(w[1], x[1]);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) {
+    a0 = hfma2(w[2 * i], x[2 * i], a0);
+    a1 = hfma2(w[2 * i + 1], x[2 * i + 1], a1);
+  }
+  const float2 f = f16x2_to_f32x2(hadd2(a0, a1));
+  return f.x + f.y;
+}
+
+// sum_j w_j x_j over one group in float32 (exact products).
+__device__ __forceinline__ float dot_group_f32(const uint32_t (&w)[16], const float (&x)[32]) {
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 wf = f16x2_to_f32x2(w[i]);
+    const float2 xv = make_float2(x[2 * i], x[2 * i + 1]);
+    if (i & 1) a1 = ffma2(wf, xv, a1);
+    else       a0 = ffma2(wf, xv, a0);
   }
   return (a0.x + a1.x) + (a0.y + a1.y);
 }
 
-template <int V> struct Log2 { static constexpr int value = 1 + Log2<V / 2>::value; };
-template <> struct Log2<1> { static constexpr int value = 0; };
+// Token operand of one group, per token dtype.
+template <typename Tok> struct GroupToken;
 
+template <> struct GroupToken<float> {      // fp32 tokens, used as they are
+  using Elem = float;
+  float v[32];
+  __device__ __forceinline__ void load(const float* row, int g) {
+    TokenIO<float>::load32(row + (size_t)g * 32, v);
+  }
+  __device__ __forceinline__ float dot(const uint32_t (&w)[16]) const { return dot_group_f32(w, v); }
+};
+
+template <> struct GroupToken<__half> {     // bf16 tokens, pre-scaled to f16
+  using Elem = __half;
+  uint32_t v[16];
+  __device__ __forceinline__ void load(const __half* row, int g) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = ld_u4(row + (size_t)g * 32 + 8 * q);
+      v[4 * q + 0] = u.x; v[4 * q + 1] = u.y; v[4 * q + 2] = u.z; v[4 * q + 3] = u.w;
+    }
+  }
+  __device__ __forceinline__ float dot(const uint32_t (&w)[16]) const { return dot_group_f16(w, v); }
+};
+
+// ---------------------------------------------------------- token prep -----
+// One warp per token: sigma_t from max|x_t|, then x16[t] = f16(x_t 2^sigma_t)
+// with max|x_t| 2^sigma_t in [2^8, 2^9).
+__device__ __forceinline__ void prep_token(const __nv_bfloat16* __restrict__ x,
+                                           __half* __restrict__ x16,
+                                           int* __restrict__ sigma, int t, int I, int lane) {
+  const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * I);
+  const int nvec = I / 8;
+  uint32_t m = 0;                                // max |x| as float32 bits
+  for (int i = lane; i < nvec; i += 32) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      m = max(m, (w[k] << 16) & 0x7fffffffu);
+      m = max(m, w[k] & 0x7fff0000u);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(kFullMask, m, o));
+  const int ex = (int)(m >> 23);                 // biased exponent of max|x|
+  int s = 0;
+  if (m != 0 && ex < 255) s = min(126, 135 - ex);   // max|x| 2^s in [2^8, 2^9)
+  const float up = __uint_as_float((uint32_t)(s + 127) << 23);
+  uint4* out = reinterpret_cast<uint4*>(x16 + (size_t)t * I);
+  for (int i = lane; i < nvec; i += 32) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 p = __floats2half2_rn(__uint_as_float(w[k] << 16) * up,
+                                          __uint_as_float(w[k] & 0xffff0000u) * up);
+      h[k] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    out[i] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+  if (lane == 0) sigma[t] = s;
+}
+
+__global__ void __launch_bounds__(256)
+prep_tokens_kernel(const __nv_bfloat16* __restrict__ x, __half* __restrict__ x16,
+                   int* __restrict__ sigma, int T, int I) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t < T) prep_token(x, x16, sigma, t, I, threadIdx.x & 31);
+}
+
+// ------------------------------------------------------- stream kernel -----
+struct StreamArgs {
+  const void* x;                 // float (fp32 tokens) or __half (pre-scaled)
+  const int* sigma;              // per-token power of two, bf16 tokens only
+  const uint8_t* packed;
+  const uint8_t* scales;
+  const uint8_t* scales_end;     // one past the last scale byte
+  RoutePlan plan;
+  float* part;                   // [T*K, ncol, O]
+  unsigned long long* status;    // device status words (timeouts)
+  int G, O, I, K;
+  int ncol;                      // group columns: ceil(G / 32)
+  int nsub;                      // row subsets: consumer warps per column
+  int rows_per_tile;             // nsub * RWS
+  int row_tiles;
+  int stages;
+  uint32_t stage_bytes;          // header + packed part + scale part, 128-aligned
+  uint32_t packed_stage_bytes;   // rows_per_tile * G * 16 (scales follow)
+};
+
+// Written by the producer into each stage before its copies are issued.
+struct StageHeader {
+  int e;          // expert id
+  int o0;         // first output row of the tile
+  int rows;       // rows in the tile
+  int scale_off;  // offset of the tile's first scale byte in the stage's
+                  // scale area, or -1: read the scales from global memory
+  int pad[28];    // keep the payload 128-byte aligned
+};
+static_assert(sizeof(StageHeader) == 128, "stage header is 128 bytes");
+
+template <int N> struct Pow2Ceil { static constexpr int value = 2 * Pow2Ceil<(N + 1) / 2>::value; };
+template <> struct Pow2Ceil<1> { static constexpr int value = 1; };
+
+// One pass of one consumer warp over its RWS rows of a staged tile, for NTA
+// tokens: lane = group g of the warp's column; each (row, token) gets one
+// group partial per lane, summed across the warp and stored as the column's
+// partial result. kScalesStaged: the tile's scale bytes are in shared memory
+// (else they are read from global memory).
+template <typename Elem, int RWS, int NTA, bool kScalesStaged>
+__device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToken<Elem> (&xt)[NTA],
+                                            const int (&pair)[NTA], uint32_t sp_lane,
+                                            uint32_t ss_lane, const uint8_t* gs_lane, int o0,
+                                            int rows, int rbase, int c, bool g_ok, int lane) {
+  constexpr int V = Pow2Ceil<RWS * NTA>::value;
+  constexpr int L = Log2<V>::value;
+  const int G = a.G, O = a.O;
+  const uint32_t prow = (uint32_t)G * 16u;      // bytes per packed row
+  float acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  if (g_ok) {
+#pragma unroll
+    for (int r = 0; r < RWS; ++r) {
+      if (rbase + r < rows) {
+        uint32_t w[16];
+        decode_group(lds128(sp_lane + (uint32_t)r * prow), w);
+        const uint32_t sb = kScalesStaged ? lds_u8(ss_lane + (uint32_t)(r * G))
+                                          : (uint32_t)__ldg(gs_lane + (size_t)r * G);
+        const float2 f = e8m0_split(sb);
+#pragma unroll
+        for (int j = 0; j < NTA; ++j) acc[r * NTA + j] = xt[j].dot(w) * f.x * f.y;
+      }
+    }
+  }
+  const float total = warp_reduce_scatter<V>(acc, lane);
+  if ((lane & ((1 << (5 - L)) - 1)) == 0) {
+    const int idx = (lane >> (5 - L)) & (V - 1);
+    if (idx < RWS * NTA) {
+      const int r = idx / NTA, j = idx - (idx / NTA) * NTA;
+      if (rbase + r < rows) {
+        int pj = pair[0];
+#pragma unroll
+        for (int q = 1; q < NTA; ++q) pj = (j == q) ? pair[q] : pj;
+        float val = total;
+        if (a.sigma != nullptr) {                   // undo the token's 2^sigma
+          const int sg = a.sigma[pj / a.K];
+          val *= __uint_as_float((uint32_t)(127 - sg) << 23);
+        }
+        a.part[((size_t)pj * a.ncol + c) * O + o0 + rbase + r] = val;
+      }
+    }
+  }
+}
+
+// Both scale sources for one pass (the choice is uniform per tile).
+template <typename Elem, int RWS, int NTA>
+__device__ __forceinline__ void stream_pass_any(const StreamArgs& a,
+                                                const GroupToken<Elem> (&xt)[NTA],
+                                                const int (&pair)[NTA], uint32_t sp_lane,
+                                                uint32_t ss_lane, const uint8_t* gs_lane,
+                                                bool staged, int o0, int rows, int rbase, int c,
+                                                bool g_ok, int lane) {
+  if (staged)
+    stream_pass<Elem, RWS, NTA, true>(a, xt, pair, sp_lane, ss_lane, gs_lane, o0, rows, rbase,
+                                      c, g_ok, lane);
+  else
+    stream_pass<Elem, RWS, NTA, false>(a, xt, pair, sp_lane, ss_lane, gs_lane, o0, rows, rbase,
+                                       c, g_ok, lane);
+}
+
+// Token operands (this lane's group) and pair ids of the pass starting at
+// position `base` of an expert's segment [base, seg_end).
+template <typename Elem, int NT>
+__device__ __forceinline__ void load_pass(const StreamArgs& a, GroupToken<Elem> (&xt)[NT],
+                                          int (&pair)[NT], int base, int seg_end, int g) {
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    pair[j] = a.plan.pair_list[base + min(j, seg_end - base - 1)];
+    if (g < a.G) xt[j].load(static_cast<const Elem*>(a.x) + (size_t)(pair[j] / a.K) * a.I, g);
+  }
+}
+
+template <typename Elem, int RWS, int NT>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+gemv_stream_kernel(const StreamArgs a) {
+  static_assert(NT == 1 || NT == 2, "one or two tokens per pass");
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  unsigned char* stage_base = smem + 2 * kMaxStages * sizeof(uint64_t);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // Each CTA takes one contiguous range of units, so consecutive units are
+  // consecutive row tiles of the same expert (and of consecutive memory).
+  const int num_units = a.plan.meta[kMetaNumActive] * a.row_tiles;
+  const int per_cta = num_units / (int)gridDim.x;
+  const int extra = num_units - per_cta * (int)gridDim.x;
+  const int ubeg = (int)blockIdx.x * per_cta + min((int)blockIdx.x, extra);
+  const int uend = ubeg + per_cta + ((int)blockIdx.x < extra ? 1 : 0);
+  const int G = a.G, O = a.O;
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------- producer
+    if (lane != 0) return;
+    const uint64_t policy = l2_evict_first_policy();
+    int issued = 0;
+    bool ok = true;
+    int u = ubeg / max(a.row_tiles, 1);
+    int tile = ubeg - u * a.row_tiles;
+    int e = -1, cached_u = -1;
+    for (int unit = ubeg; unit < uend; ++unit, ++issued) {
+      const int st = issued % a.stages;
+      const uint32_t round = (uint32_t)(issued / a.stages);
+      if (u != cached_u) { e = a.plan.active[u]; cached_u = u; }
+      const int o0 = tile * a.rows_per_tile;
+      const int rows = min(a.rows_per_tile, O - o0);
+      const size_t row0 = (size_t)e * O + o0;
+      const uint32_t pbytes = (uint32_t)rows * G * 16;
+      // The tile's scale bytes: copy the 16-byte-aligned span that holds
+      // them, unless that span would pass the end of the scales buffer.
+      const uintptr_t s_lo = reinterpret_cast<uintptr_t>(a.scales + row0 * G);
+      const uintptr_t s_hi = s_lo + (uintptr_t)rows * G;
+      const uintptr_t c_lo = s_lo & ~(uintptr_t)15;
+      const uintptr_t c_hi = (s_hi + 15) & ~(uintptr_t)15;
+      const bool scale_copy = c_hi <= reinterpret_cast<uintptr_t>(a.scales_end);
+      const uint32_t sbytes = scale_copy ? (uint32_t)(c_hi - c_lo) : 0u;
+      if (!mbar_wait(&empty[st], (round & 1u) ^ 1u)) { ok = false; break; }
+      unsigned char* dst = stage_base + (size_t)st * a.stage_bytes;
+      StageHeader* h = reinterpret_cast<StageHeader*>(dst);
+      h->e = e;
+      h->o0 = o0;
+      h->rows = rows;
+      h->scale_off = scale_copy ? (int)(s_lo - c_lo) : -1;
+      mbar_arrive_expect_tx(&full[st], pbytes + sbytes);     // releases the header
+      bulk_copy_g2s(dst + sizeof(StageHeader), a.packed + row0 * G * 16, pbytes, &full[st],
+                    policy);
+      if (sbytes)
+        bulk_copy_g2s(dst + sizeof(StageHeader) + a.packed_stage_bytes,
+                      reinterpret_cast<const void*>(c_lo), sbytes, &full[st], policy);
+      if (++tile == a.row_tiles) { tile = 0; ++u; }
+    }
+    if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+    // Do not leave copies in flight: wait (bounded) for the last round of
+    // every stage this thread issued.
+    for (int k = max(0, issued - a.stages); k < issued; ++k) {
+      const int st = k % a.stages;
+      if (!mbar_wait(&full[st], (uint32_t)(k / a.stages) & 1u)) {
+        atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+        break;
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------- consumers
+  // Warp (c, s): group column c (groups 32c .. 32c+31), rows s*RWS .. +RWS-1.
+  const bool working = warp < a.ncol * a.nsub;
+  const int c = warp % a.ncol, sub = warp / a.ncol;
+  const int g = c * 32 + lane;
+  const int rbase = sub * RWS;
+  int cached_e = -1, seg_beg = 0, seg_end = 0;
+  // Token operands of the expert's first pass, kept across its tiles.
+  GroupToken<Elem> x0[NT];
+  int pair0[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) pair0[j] = 0;
+
+  int it = 0;
+  for (int unit = ubeg; unit < uend; ++unit, ++it) {
+    const int st = it % a.stages;
+    const uint32_t round = (uint32_t)(it / a.stages);
+    if (!mbar_wait(&full[st], round & 1u)) {
+      if (lane == 0) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+      return;
+    }
+    const unsigned char* hp = stage_base + (size_t)st * a.stage_bytes;
+    const StageHeader* h = reinterpret_cast<const StageHeader*>(hp);
+    const int e = h->e, o0 = h->o0, rows = h->rows, scale_off = h->scale_off;
+    const unsigned char* sp = hp + sizeof(StageHeader);
+
+    if (working && rbase < rows) {
+      if (e != cached_e) {                    // new expert: its first pass
+        cached_e = e;
+        seg_beg = a.plan.offsets[e];
+        seg_end = a.plan.offsets[e + 1];
+        load_pass(a, x0, pair0, seg_beg, seg_end, g);
+      }
+      // This lane's group in row rbase of the tile: packed bytes and scale.
+      const uint32_t sp_lane =
+          smem_addr(sp) + ((uint32_t)rbase * (uint32_t)G + (uint32_t)g) * 16u;
+      const uint32_t ss_lane =
+          smem_addr(sp) + a.packed_stage_bytes + (uint32_t)(scale_off + rbase * G + g);
+      const uint8_t* gs_lane = a.scales + ((size_t)e * O + o0 + rbase) * G + g;
+      const bool staged = scale_off >= 0, g_ok = g < G;
+      for (int base = seg_beg;;) {
+        if (seg_end - base >= NT) {
+          stream_pass_any<Elem, RWS, NT>(a, x0, pair0, sp_lane, ss_lane, gs_lane, staged, o0,
+                                         rows, rbase, c, g_ok, lane);
+        } else {                              // one token left (NT == 2)
+          stream_pass_any<Elem, RWS, 1>(
+              a, reinterpret_cast<const GroupToken<Elem>(&)[1]>(x0[0]),
+              reinterpret_cast<const int(&)[1]>(pair0[0]), sp_lane, ss_lane, gs_lane, staged,
+              o0, rows, rbase, c, g_ok, lane);
+        }
+        base += NT;
+        if (base >= seg_end) break;
+        // More tokens: the cache now holds a later pass, so reload the first
+        // one at the next tile.
+        load_pass(a, x0, pair0, base, seg_end, g);
+        cached_e = -1;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+}
+
+// ------------------------------------------------------- direct kernel -----
 template <typename Tok, int R, int NT>
-__global__ void __launch_bounds__(kGemvThreads, 2)
-gemv_kernel(const Tok* __restrict__ x, const uint8_t* __restrict__ packed,
-            const uint8_t* __restrict__ scales, RoutePlan plan,
-            float* __restrict__ part, int G, int O, int I, int K,
-            int row_tiles) {
+__global__ void __launch_bounds__(kDirectThreads, 2)
+gemv_direct_kernel(const Tok* __restrict__ x, const uint8_t* __restrict__ packed,
+                   const uint8_t* __restrict__ scales, RoutePlan plan,
+                   float* __restrict__ part, int G, int O, int I, int K, int row_tiles) {
   constexpr int V = R * NT;
   constexpr int L = Log2<V>::value;
-  static_assert((1 << L) == V, "R * NT must be a power of two");
-
   const int u = blockIdx.x / row_tiles;
   const int tile = blockIdx.x - u * row_tiles;
   if (u >= plan.meta[kMetaNumActive]) return;
   const int e = plan.active[u];
-  const int seg_beg = plan.offsets[e];
-  const int seg_end = plan.offsets[e + 1];
+  const int seg_beg = plan.offsets[e], seg_end = plan.offsets[e + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int o0 = (tile * kGemvWarps + warp) * R;
+  const int o0 = (tile * kDirectWarps + warp) * R;
   if (o0 >= O) return;
-
   const uint8_t* wrow[R];
   const uint8_t* srow[R];
 #pragma unroll
@@ -80,83 +450,191 @@ gemv_kernel(const Tok* __restrict__ x, const uint8_t* __restrict__ packed,
     wrow[r] = packed + row * (size_t)G * 16;
     srow[r] = scales + row * (size_t)G;
   }
-
   for (int base = seg_beg; base < seg_end; base += NT) {
     const int nt = min(NT, seg_end - base);
     const Tok* xrow[NT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int pair = plan.pair_list[base + min(j, nt - 1)];
-      xrow[j] = x + (size_t)(pair / K) * I;
-    }
+    for (int j = 0; j < NT; ++j)
+      xrow[j] = x + (size_t)(plan.pair_list[base + min(j, nt - 1)] / K) * I;
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = 0.f;
-
     for (int g = lane; g < G; g += 32) {
-      uint4 w[R];
+      uint32_t w[R][16];
       E8M0 sc[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) w[r] = ld_stream_u4(wrow[r] + (size_t)g * 16);
-#pragma unroll
-      for (int r = 0; r < R; ++r) sc[r] = e8m0(srow[r][g]);
+      for (int r = 0; r < R; ++r) {
+        decode_group(ld_stream_u4(wrow[r] + (size_t)g * 16), w[r]);
+        sc[r] = e8m0(srow[r][g]);
+      }
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         if (j < nt) {
           float xf[32];
           TokenIO<Tok>::load32(xrow[j] + (size_t)g * 32, xf);
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const float d = dot_group(w[r], xf);
-            acc[r * NT + j] = fmaf(d * sc[r].pre, sc[r].factor, acc[r * NT + j]);
-          }
+          for (int r = 0; r < R; ++r)
+            acc[r * NT + j] = fmaf(dot_group_f32(w[r], xf) * sc[r].pre, sc[r].factor,
+                                   acc[r * NT + j]);
         }
       }
     }
-
     const float total = warp_reduce_scatter<V>(acc, lane);
     if ((lane & ((1 << (5 - L)) - 1)) == 0) {
       const int idx = (lane >> (5 - L)) & (V - 1);
       const int r = idx / NT, j = idx - (idx / NT) * NT;
-      if (j < nt && o0 + r < O) {
-        const int pair = plan.pair_list[base + j];
-        part[(size_t)pair * O + o0 + r] = total;
-      }
+      if (j < nt && o0 + r < O)
+        part[(size_t)plan.pair_list[base + j] * O + o0 + r] = total;
     }
   }
 }
 
-constexpr int kRows = 4;     // output rows per warp
-constexpr int kTokens = 4;   // tokens per pass
+// ------------------------------------------------------------- launch ------
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 152;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 152;
+  }
+  return cached[dev];
+}
 
-template <typename Tok>
-cudaError_t launch_typed(const Tok* x, const uint8_t* packed, const uint8_t* scales,
-                         const RoutePlan& plan, float* part, int64_t T, int64_t E,
-                         int64_t I, int64_t O, int64_t K, cudaStream_t stream) {
-  const int64_t rows_per_cta = (int64_t)kGemvWarps * kRows;
-  const int64_t row_tiles = (O + rows_per_cta - 1) / rows_per_cta;
-  const int64_t slots = std::min<int64_t>(E, T * K);
-  const int64_t blocks = slots * row_tiles;
-  if (blocks == 0) return cudaSuccess;
-  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  gemv_kernel<Tok, kRows, kTokens><<<(unsigned)blocks, kGemvThreads, 0, stream>>>(
-      x, packed, scales, plan, part, (int)(I / 32), (int)O, (int)I, (int)K,
-      (int)row_tiles);
+template <typename Elem, int RWS>
+cudaError_t launch_stream(StreamArgs a, size_t smem, int64_t bound_units, cudaStream_t stream) {
+  // Two tokens per pass for f16 operands; fp32 operands take twice the
+  // registers, so one.
+  constexpr int NT = sizeof(Elem) == 2 ? 2 : 1;
+  auto kern = gemv_stream_kernel<Elem, RWS, NT>;
+  static std::mutex mu;
+  static size_t opted[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && opted[dev] < smem) {
+      cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+      if (err != cudaSuccess) return err;
+      opted[dev] = smem;
+    }
+  }
+  const int64_t grid = std::min<int64_t>(num_sms(), bound_units);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(unsigned)grid, kStreamThreads, smem, stream>>>(a);
   note_launch();
   return cudaGetLastError();
 }
 
+template <typename Tok>
+cudaError_t launch_direct(const Tok* x, const uint8_t* packed, const uint8_t* scales,
+                          const RoutePlan& plan, float* part, int64_t T, int64_t E,
+                          int64_t I, int64_t O, int64_t K, cudaStream_t stream) {
+  constexpr int R = 4, NT = 4;
+  const int64_t rows_per_cta = (int64_t)kDirectWarps * R;
+  const int64_t row_tiles = (O + rows_per_cta - 1) / rows_per_cta;
+  const int64_t blocks = std::min<int64_t>(E, T * K) * row_tiles;
+  if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  gemv_direct_kernel<Tok, R, NT><<<(unsigned)blocks, kDirectThreads, 0, stream>>>(
+      x, packed, scales, plan, part, (int)(I / 32), (int)O, (int)I, (int)K, (int)row_tiles);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// Shape of the staged GEMV for a row width of G groups: group columns,
+// consumer warps per column, rows per warp. rws == 0 when the rows are too
+// wide to stage (the direct kernel runs instead).
+struct StreamShape {
+  int ncol = 0, nsub = 0, rws = 0;
+};
+
+size_t stage_bytes_for(size_t rows, int64_t G) {
+  return 128 + rows * G * 16 + ((rows * G + 15) / 16) * 16 + 16;
+}
+
+StreamShape stream_shape(int64_t G) {
+  StreamShape sh;
+  const int64_t ncol = (G + 31) / 32;
+  if (ncol > kConsumerWarps) return sh;
+  sh.ncol = (int)ncol;
+  sh.nsub = kConsumerWarps / sh.ncol;
+  for (int rws = 8; rws >= 1; rws /= 2) {
+    if (stage_bytes_for((size_t)sh.nsub * rws, G) <= kMaxStageBytes) {
+      sh.rws = rws;
+      return sh;
+    }
+  }
+  return sh;
+}
+
 }  // namespace
 
-cudaError_t launch_gemv(const void* x, int token_dtype, const uint8_t* packed,
-                        const uint8_t* scales, const RoutePlan& plan,
-                        float* part, int64_t T, int64_t E, int64_t I,
-                        int64_t O, int64_t K, cudaStream_t stream) {
-  if (token_dtype == kTokenBF16)
-    return launch_typed(static_cast<const __nv_bfloat16*>(x), packed, scales,
-                        plan, part, T, E, I, O, K, stream);
-  return launch_typed(static_cast<const float*>(x), packed, scales, plan, part,
-                      T, E, I, O, K, stream);
+int gemv_partial_columns(int64_t I) {
+  const StreamShape sh = stream_shape(I / 32);
+  return sh.rws > 0 ? sh.ncol : 1;
+}
+
+bool gemv_uses_stream(int64_t I) { return stream_shape(I / 32).rws > 0; }
+
+cudaError_t launch_prep_tokens(const void* x, __half* x16, int* sigma, int64_t T, int64_t I,
+                               cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  prep_tokens_kernel<<<(unsigned)((T + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(x), x16, sigma, (int)T, (int)I);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const int* sigma,
+                        const uint8_t* packed, const uint8_t* scales, const RoutePlan& plan,
+                        float* part, unsigned long long* status, int64_t T, int64_t E,
+                        int64_t I, int64_t O, int64_t K, cudaStream_t stream) {
+  const int64_t G = I / 32;
+  const StreamShape sh = stream_shape(G);
+  if (sh.rws == 0) {
+    if (token_dtype == kTokenBF16)
+      return launch_direct(static_cast<const __nv_bfloat16*>(x), packed, scales, plan, part,
+                           T, E, I, O, K, stream);
+    return launch_direct(static_cast<const float*>(x), packed, scales, plan, part, T, E, I,
+                         O, K, stream);
+  }
+  StreamArgs a;
+  a.x = token_dtype == kTokenBF16 ? static_cast<const void*>(x16) : x;
+  a.sigma = token_dtype == kTokenBF16 ? sigma : nullptr;
+  a.packed = packed;
+  a.scales = scales;
+  a.scales_end = scales + (size_t)E * O * G;
+  a.plan = plan;
+  a.part = part;
+  a.status = status;
+  a.G = (int)G;
+  a.O = (int)O;
+  a.I = (int)I;
+  a.K = (int)K;
+  a.ncol = sh.ncol;
+  a.nsub = sh.nsub;
+  a.rows_per_tile = sh.nsub * sh.rws;
+  a.row_tiles = (int)((O + a.rows_per_tile - 1) / a.rows_per_tile);
+  a.packed_stage_bytes = (uint32_t)((size_t)a.rows_per_tile * G * 16);
+  a.stage_bytes = (uint32_t)((stage_bytes_for(a.rows_per_tile, G) + 127) / 128 * 128);
+  a.stages = (int)std::min<size_t>(kMaxStages, kSmemBudget / a.stage_bytes);
+  const size_t smem = 2 * kMaxStages * sizeof(uint64_t) + (size_t)a.stages * a.stage_bytes;
+  const int64_t bound_units = std::min<int64_t>(E, T * K) * a.row_tiles;
+  if (bound_units > 0x7fffffff) return cudaErrorInvalidConfiguration;
+#define MXFP4EL_STREAM_CASES(ELEM)                                        \
+  switch (sh.rws) {                                                        \
+    case 8: return launch_stream<ELEM, 8>(a, smem, bound_units, stream);   \
+    case 4: return launch_stream<ELEM, 4>(a, smem, bound_units, stream);   \
+    case 2: return launch_stream<ELEM, 2>(a, smem, bound_units, stream);   \
+    default: return launch_stream<ELEM, 1>(a, smem, bound_units, stream);  \
+  }
+  if (token_dtype == kTokenBF16) { MXFP4EL_STREAM_CASES(__half) }
+  MXFP4EL_STREAM_CASES(float)
+#undef MXFP4EL_STREAM_CASES
 }
 
 }  // namespace mxfp4el

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace mxfp4el {
@@ -15,6 +16,11 @@ constexpr int kIndexI64 = 1;
 // Per-warp expert counters live in shared memory up to this many bytes and
 // in the workspace beyond it.
 constexpr size_t kRouteSmemLimit = 96 * 1024;
+
+// Device status words (one array per device, see device_status_words()).
+constexpr int kStatusBadPairs = 0;      // (t, k) pairs with an out-of-range id
+constexpr int kStatusWaitTimeouts = 1;  // kernel waits that hit their time limit
+constexpr int kStatusWords = 4;
 
 // Slots of RoutePlan::meta.
 constexpr int kMetaNumActive = 0;   // experts with at least one valid pair
@@ -34,13 +40,15 @@ struct RoutePlan {
 struct Workspace {
   RoutePlan plan;
   int* wc_global;   // per-warp counters when they do not fit in shared memory
-  float* part;      // [T*K, O] float32 routed result of every pair
+  __half* x16;      // [T, I] tokens scaled by 2^sigma_t in f16 (bf16 tokens)
+  int* sigma;       // [T] the power of two of each token (bf16 tokens)
+  float* part;      // [T*K, ncol, O] float32 partial results of every pair
   size_t bytes;     // total
 };
 
 // Offsets of every region for the given sizes; base == nullptr only sizes.
-bool carve_workspace(void* base, int64_t T, int64_t E, int64_t O, int64_t K,
-                     Workspace* ws);
+bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
+                     int64_t K, int token_dtype, Workspace* ws);
 
 size_t route_global_counter_words(int64_t E);
 
@@ -48,17 +56,34 @@ cudaError_t launch_route(const void* sel, int index_dtype, int64_t T,
                          int64_t K, int64_t E, int* wc_global,
                          const RoutePlan& plan, cudaStream_t stream);
 
-cudaError_t launch_gemv(const void* x, int token_dtype, const uint8_t* packed,
-                        const uint8_t* scales, const RoutePlan& plan,
-                        float* part, int64_t T, int64_t E, int64_t I,
-                        int64_t O, int64_t K, cudaStream_t stream);
+// True when the rows of width I fit the staged (bulk-copy) GEMV; bf16
+// tokens then need launch_prep_tokens first.
+bool gemv_uses_stream(int64_t I);
+
+// Partial results per (pair, output row) that the GEMV writes for width I:
+// one per group column of the staged kernel, 1 for the direct kernel. The
+// combine adds them in column order.
+int gemv_partial_columns(int64_t I);
+
+cudaError_t launch_prep_tokens(const void* x, __half* x16, int* sigma, int64_t T,
+                               int64_t I, cudaStream_t stream);
+
+cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16,
+                        const int* sigma, const uint8_t* packed,
+                        const uint8_t* scales, const RoutePlan& plan, float* part,
+                        unsigned long long* status, int64_t T, int64_t E,
+                        int64_t I, int64_t O, int64_t K, cudaStream_t stream);
 
 cudaError_t launch_combine(const void* y_shared, const void* sel,
                            int index_dtype, const float* p, const float* part,
-                           void* out, int token_dtype, int64_t T, int64_t E,
-                           int64_t O, int64_t K, cudaStream_t stream);
+                           int ncol, void* out, int token_dtype, int64_t T,
+                           int64_t E, int64_t O, int64_t K, cudaStream_t stream);
 
-cudaError_t read_and_reset_bad_pairs(cudaStream_t stream, int64_t* out);
+// Device address of the status words on the current device.
+unsigned long long* device_status_words();
+
+// Synchronises `stream`, reads one status word and resets it to zero.
+cudaError_t read_and_reset_status(cudaStream_t stream, int word, int64_t* out);
 
 // Counts kernel launches made by the library (process-wide).
 void note_launch();

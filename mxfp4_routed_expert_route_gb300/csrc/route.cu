@@ -12,12 +12,15 @@
 //   C. each warp walks its chunk again and scatters pair ids into place.
 // Inside a segment the pairs keep their (token, slot) order. Pairs whose
 // expert id lies outside [0, E) are skipped and counted on the device.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace mxfp4el {
 
-__device__ unsigned long long g_bad_pairs = 0;
+// Status words of this device: counts the host reads and resets.
+__device__ unsigned long long g_status[kStatusWords];
 
 namespace {
 
@@ -139,7 +142,7 @@ route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
   // Invalid ids: count them for mxfp4el_device_errors().
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) bad += __shfl_xor_sync(kFullMask, bad, o);
-  if (lane == 0 && bad > 0) atomicAdd(&g_bad_pairs, (unsigned long long)bad);
+  if (lane == 0 && bad > 0) atomicAdd(&g_status[kStatusBadPairs], (unsigned long long)bad);
 }
 
 }  // namespace
@@ -175,14 +178,29 @@ cudaError_t launch_route(const void* sel, int index_dtype, int64_t T, int64_t K,
   return cudaGetLastError();
 }
 
-cudaError_t read_and_reset_bad_pairs(cudaStream_t stream, int64_t* out) {
+unsigned long long* device_status_words() {
+  static std::mutex mu;
+  static unsigned long long* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned long long*>(p);
+  }
+  return addr[dev];
+}
+
+cudaError_t read_and_reset_status(cudaStream_t stream, int word, int64_t* out) {
   cudaError_t err = cudaStreamSynchronize(stream);
   if (err != cudaSuccess) return err;
   unsigned long long v = 0;
-  err = cudaMemcpyFromSymbol(&v, g_bad_pairs, sizeof(v));
+  const size_t off = (size_t)word * sizeof(unsigned long long);
+  err = cudaMemcpyFromSymbol(&v, g_status, sizeof(v), off);
   if (err != cudaSuccess) return err;
   const unsigned long long zero = 0;
-  err = cudaMemcpyToSymbol(g_bad_pairs, &zero, sizeof(zero));
+  err = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero), off);
   *out = (int64_t)v;
   return err;
 }

@@ -40,6 +40,7 @@ def worst_ratio(gpu_rows: torch.Tensor, want: np.ndarray, abs_terms: np.ndarray)
 def assert_parity(gpu_rows, want, abs_terms, dtype, what=""):
     assert np.all(np.isfinite(gpu_rows.detach().cpu().double().numpy())), what
     ratio = worst_ratio(gpu_rows, want, abs_terms)
+    print(f"[parity] {what or 'case'}: max err/abs_terms = {ratio:.3e} (tol {TOL[dtype]:.0e})")
     assert ratio <= TOL[dtype], f"{what}: max err/abs_terms = {ratio:.3e} > {TOL[dtype]}"
     return ratio
 

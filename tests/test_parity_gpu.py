@@ -236,3 +236,37 @@ def test_alias_is_refused():
     with pytest.raises(_native.MXFP4Error):
         mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"],
                             d["y_shared"], out=d["y_shared"])
+
+
+# ------------------------------------------------ kernel variants, numerics --
+def test_rows_too_wide_for_a_stage_use_the_direct_kernel():
+    # I = 16384 (512 groups): one row per warp no longer fits a shared-memory
+    # stage, so the unstaged GEMV runs.
+    for dtype in (torch.bfloat16, torch.float32):
+        wl = workloads.make(3, 4, 2, 16384, 40, dtype=dtype, seed=19)
+        out = run_gpu(wl)
+        want, absm, _ = oracle_rows(wl)
+        assert_parity(out, want, absm, dtype, str(dtype))
+
+
+@pytest.mark.parametrize("seed", [20, 21])
+def test_bf16_tokens_with_extreme_dynamic_range(seed):
+    # Per-token magnitudes from 2^-60 to 2^60 and per-element spread of 2^+-12
+    # stress the per-token power-of-two scaling and the f16 product chains.
+    rng = np.random.default_rng(seed)
+    T, E, K, I, O = 12, 6, 3, 640, 96
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, scale_lo=100,
+                        scale_hi=150, seed=seed)
+    tok_scale = np.ldexp(1.0, rng.integers(-60, 61, size=(T, 1)))
+    elem = np.ldexp(rng.standard_normal((T, I)), rng.integers(-12, 13, size=(T, I)))
+    wl.x = torch.from_numpy((elem * tok_scale).astype(np.float32)).to(torch.bfloat16)
+    out = run_gpu(wl)
+    want, absm, _ = oracle_rows(wl)
+    assert_parity(out, want, absm, wl.dtype)
+
+
+def test_no_kernel_wait_timed_out():
+    from mxfp4_routed_expert_route_gb300 import wait_timeouts
+    wl = workloads.make(9, 10, 3, 288, 130, dtype=torch.bfloat16, seed=22)
+    run_gpu(wl)
+    assert wait_timeouts() == 0
