@@ -86,9 +86,12 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
   if (K > 0) {
     unsigned long long* status = device_status_words();
     if (status == nullptr) return MXFP4EL_ERR_CUDA;
+    const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
+    const bool prep_in_route = prep && prep_fits_route(T, I);
+    TokenPrep tp = {prep_in_route ? x : nullptr, ws.x16, ws.sigma, I};
     mark(MXFP4EL_STAGE_ROUTE, true, stream);
-    err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, stream);
-    if (err == cudaSuccess && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I))
+    err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, tp, stream);
+    if (err == cudaSuccess && prep && !prep_in_route)
       err = launch_prep_tokens(x, ws.x16, ws.sigma, T, I, stream);
     mark(MXFP4EL_STAGE_ROUTE, false, stream);
     if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;

@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const Tok* __restrict__ ys, const Idx* __restrict__ sel,
                const float* __restrict__ p, const float* __restrict__ part, int ncol,
                Tok* __restrict__ out, int64_t T, int64_t O, int K, int64_t E) {
+  pdl_wait();                  // the GEMV's partial results are complete
   const int64_t n = T * O;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -49,10 +50,8 @@ cudaError_t launch_typed(const Tok* ys, const Idx* sel, const float* p,
   const int64_t n = T * O;
   if (n == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 16);
-  combine_kernel<Tok, Idx><<<(unsigned)blocks, 256, 0, stream>>>(
-      ys, sel, p, part, ncol, out, T, O, (int)K, E);
-  note_launch();
-  return cudaGetLastError();
+  return launch_after_previous(combine_kernel<Tok, Idx>, dim3((unsigned)blocks), dim3(256), 0,
+                               stream, ys, sel, p, part, ncol, out, T, O, (int)K, E);
 }
 
 template <typename Tok>

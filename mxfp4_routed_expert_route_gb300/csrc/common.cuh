@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace mxfp4el {
 
@@ -249,6 +250,58 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// ------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while
+// its predecessor in the stream is still running; pdl_wait() blocks until
+// the predecessor has completed and its memory is visible. Both are no-ops
+// for a normal launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------- token prep -----
+// Prepared tokens for the staged GEMV with bf16 tokens: per token t a power
+// of two 2^sigma_t and x16[t, i] = f16(x[t, i] 2^sigma_t).
+// One warp per token: sigma_t from max|x_t|, then x16[t] = f16(x_t 2^sigma_t)
+// with max|x_t| 2^sigma_t in [2^8, 2^9).
+__device__ __forceinline__ void prep_token(const __nv_bfloat16* __restrict__ x,
+                                           __half* __restrict__ x16,
+                                           int* __restrict__ sigma, int t, int I, int lane) {
+  const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * I);
+  const int nvec = I / 8;
+  uint32_t m = 0;                                // max |x| as float32 bits
+  for (int i = lane; i < nvec; i += 32) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      m = max(m, (w[k] << 16) & 0x7fffffffu);
+      m = max(m, w[k] & 0x7fff0000u);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(kFullMask, m, o));
+  const int ex = (int)(m >> 23);                 // biased exponent of max|x|
+  int s = 0;
+  if (m != 0 && ex < 255) s = min(126, 135 - ex);   // max|x| 2^s in [2^8, 2^9)
+  const float up = __uint_as_float((uint32_t)(s + 127) << 23);
+  uint4* out = reinterpret_cast<uint4*>(x16 + (size_t)t * I);
+  for (int i = lane; i < nvec; i += 32) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 p = __floats2half2_rn(__uint_as_float(w[k] << 16) * up,
+                                          __uint_as_float(w[k] & 0xffff0000u) * up);
+      h[k] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    out[i] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+  if (lane == 0) sigma[t] = s;
 }
 
 // ------------------------------------------------------ warp reductions ----

@@ -123,50 +123,15 @@ template <> struct GroupToken<__half> {     // bf16 tokens, pre-scaled to f16
 };
 
 // ---------------------------------------------------------- token prep -----
-// One warp per token: sigma_t from max|x_t|, then x16[t] = f16(x_t 2^sigma_t)
-// with max|x_t| 2^sigma_t in [2^8, 2^9).
-__device__ __forceinline__ void prep_token(const __nv_bfloat16* __restrict__ x,
-                                           __half* __restrict__ x16,
-                                           int* __restrict__ sigma, int t, int I, int lane) {
-  const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * I);
-  const int nvec = I / 8;
-  uint32_t m = 0;                                // max |x| as float32 bits
-  for (int i = lane; i < nvec; i += 32) {
-    const uint4 v = __ldg(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      m = max(m, (w[k] << 16) & 0x7fffffffu);
-      m = max(m, w[k] & 0x7fff0000u);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(kFullMask, m, o));
-  const int ex = (int)(m >> 23);                 // biased exponent of max|x|
-  int s = 0;
-  if (m != 0 && ex < 255) s = min(126, 135 - ex);   // max|x| 2^s in [2^8, 2^9)
-  const float up = __uint_as_float((uint32_t)(s + 127) << 23);
-  uint4* out = reinterpret_cast<uint4*>(x16 + (size_t)t * I);
-  for (int i = lane; i < nvec; i += 32) {
-    const uint4 v = __ldg(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t h[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __half2 p = __floats2half2_rn(__uint_as_float(w[k] << 16) * up,
-                                          __uint_as_float(w[k] & 0xffff0000u) * up);
-      h[k] = *reinterpret_cast<const uint32_t*>(&p);
-    }
-    out[i] = make_uint4(h[0], h[1], h[2], h[3]);
-  }
-  if (lane == 0) sigma[t] = s;
-}
-
 __global__ void __launch_bounds__(256)
 prep_tokens_kernel(const __nv_bfloat16* __restrict__ x, __half* __restrict__ x16,
                    int* __restrict__ sigma, int T, int I) {
+  pdl_launch_dependents();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t < T) prep_token(x, x16, sigma, t, I, threadIdx.x & 31);
+  // Finish only after the bucketer before this kernel has: the GEMV waits
+  // on this kernel alone.
+  pdl_wait();
 }
 
 // ------------------------------------------------------- stream kernel -----
@@ -210,7 +175,8 @@ template <> struct Pow2Ceil<1> { static constexpr int value = 1; };
 // (else they are read from global memory).
 template <typename Elem, int RWS, int NTA, bool kScalesStaged>
 __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToken<Elem> (&xt)[NTA],
-                                            const int (&pair)[NTA], uint32_t sp_lane,
+                                            const int (&pair)[NTA], const float (&unscale)[NTA],
+                                            uint32_t sp_lane,
                                             uint32_t ss_lane, const uint8_t* gs_lane, int o0,
                                             int rows, int rbase, int c, bool g_ok, int lane) {
   constexpr int V = Pow2Ceil<RWS * NTA>::value;
@@ -241,14 +207,13 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
       const int r = idx / NTA, j = idx - (idx / NTA) * NTA;
       if (rbase + r < rows) {
         int pj = pair[0];
+        float us = unscale[0];
 #pragma unroll
-        for (int q = 1; q < NTA; ++q) pj = (j == q) ? pair[q] : pj;
-        float val = total;
-        if (a.sigma != nullptr) {                   // undo the token's 2^sigma
-          const int sg = a.sigma[pj / a.K];
-          val *= __uint_as_float((uint32_t)(127 - sg) << 23);
+        for (int q = 1; q < NTA; ++q) {
+          pj = (j == q) ? pair[q] : pj;
+          us = (j == q) ? unscale[q] : us;
         }
-        a.part[((size_t)pj * a.ncol + c) * O + o0 + rbase + r] = val;
+        a.part[((size_t)pj * a.ncol + c) * O + o0 + rbase + r] = total * us;
       }
     }
   }
@@ -258,27 +223,33 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
 template <typename Elem, int RWS, int NTA>
 __device__ __forceinline__ void stream_pass_any(const StreamArgs& a,
                                                 const GroupToken<Elem> (&xt)[NTA],
-                                                const int (&pair)[NTA], uint32_t sp_lane,
+                                                const int (&pair)[NTA],
+                                                const float (&unscale)[NTA], uint32_t sp_lane,
                                                 uint32_t ss_lane, const uint8_t* gs_lane,
                                                 bool staged, int o0, int rows, int rbase, int c,
                                                 bool g_ok, int lane) {
   if (staged)
-    stream_pass<Elem, RWS, NTA, true>(a, xt, pair, sp_lane, ss_lane, gs_lane, o0, rows, rbase,
-                                      c, g_ok, lane);
+    stream_pass<Elem, RWS, NTA, true>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane, o0, rows,
+                                      rbase, c, g_ok, lane);
   else
-    stream_pass<Elem, RWS, NTA, false>(a, xt, pair, sp_lane, ss_lane, gs_lane, o0, rows, rbase,
-                                       c, g_ok, lane);
+    stream_pass<Elem, RWS, NTA, false>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane, o0,
+                                       rows, rbase, c, g_ok, lane);
 }
 
 // Token operands (this lane's group) and pair ids of the pass starting at
 // position `base` of an expert's segment [base, seg_end).
+// Also the factor that undoes each token's power-of-two scaling (1 for fp32
+// tokens).
 template <typename Elem, int NT>
 __device__ __forceinline__ void load_pass(const StreamArgs& a, GroupToken<Elem> (&xt)[NT],
-                                          int (&pair)[NT], int base, int seg_end, int g) {
+                                          int (&pair)[NT], float (&unscale)[NT], int base,
+                                          int seg_end, int g) {
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     pair[j] = a.plan.pair_list[base + min(j, seg_end - base - 1)];
-    if (g < a.G) xt[j].load(static_cast<const Elem*>(a.x) + (size_t)(pair[j] / a.K) * a.I, g);
+    const int t = pair[j] / a.K;
+    if (g < a.G) xt[j].load(static_cast<const Elem*>(a.x) + (size_t)t * a.I, g);
+    unscale[j] = a.sigma != nullptr ? __uint_as_float((uint32_t)(127 - a.sigma[t]) << 23) : 1.f;
   }
 }
 
@@ -292,6 +263,7 @@ gemv_stream_kernel(const StreamArgs a) {
   unsigned char* stage_base = smem + 2 * kMaxStages * sizeof(uint64_t);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -300,6 +272,7 @@ gemv_stream_kernel(const StreamArgs a) {
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();                  // the routing lists and prepared tokens are ready
 
   // Each CTA takes one contiguous range of units, so consecutive units are
   // consecutive row tiles of the same expert (and of consecutive memory).
@@ -373,8 +346,9 @@ gemv_stream_kernel(const StreamArgs a) {
   // Token operands of the expert's first pass, kept across its tiles.
   GroupToken<Elem> x0[NT];
   int pair0[NT];
+  float unscale0[NT];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) pair0[j] = 0;
+  for (int j = 0; j < NT; ++j) { pair0[j] = 0; unscale0[j] = 1.f; }
 
   int it = 0;
   for (int unit = ubeg; unit < uend; ++unit, ++it) {
@@ -394,7 +368,7 @@ gemv_stream_kernel(const StreamArgs a) {
         cached_e = e;
         seg_beg = a.plan.offsets[e];
         seg_end = a.plan.offsets[e + 1];
-        load_pass(a, x0, pair0, seg_beg, seg_end, g);
+        load_pass(a, x0, pair0, unscale0, seg_beg, seg_end, g);
       }
       // This lane's group in row rbase of the tile: packed bytes and scale.
       const uint32_t sp_lane =
@@ -405,19 +379,20 @@ gemv_stream_kernel(const StreamArgs a) {
       const bool staged = scale_off >= 0, g_ok = g < G;
       for (int base = seg_beg;;) {
         if (seg_end - base >= NT) {
-          stream_pass_any<Elem, RWS, NT>(a, x0, pair0, sp_lane, ss_lane, gs_lane, staged, o0,
-                                         rows, rbase, c, g_ok, lane);
+          stream_pass_any<Elem, RWS, NT>(a, x0, pair0, unscale0, sp_lane, ss_lane, gs_lane,
+                                         staged, o0, rows, rbase, c, g_ok, lane);
         } else {                              // one token left (NT == 2)
           stream_pass_any<Elem, RWS, 1>(
               a, reinterpret_cast<const GroupToken<Elem>(&)[1]>(x0[0]),
-              reinterpret_cast<const int(&)[1]>(pair0[0]), sp_lane, ss_lane, gs_lane, staged,
-              o0, rows, rbase, c, g_ok, lane);
+              reinterpret_cast<const int(&)[1]>(pair0[0]),
+              reinterpret_cast<const float(&)[1]>(unscale0[0]), sp_lane, ss_lane, gs_lane,
+              staged, o0, rows, rbase, c, g_ok, lane);
         }
         base += NT;
         if (base >= seg_end) break;
         // More tokens: the cache now holds a later pass, so reload the first
         // one at the next tile.
-        load_pass(a, x0, pair0, base, seg_end, g);
+        load_pass(a, x0, pair0, unscale0, base, seg_end, g);
         cached_e = -1;
       }
     }
@@ -434,6 +409,7 @@ gemv_direct_kernel(const Tok* __restrict__ x, const uint8_t* __restrict__ packed
                    float* __restrict__ part, int G, int O, int I, int K, int row_tiles) {
   constexpr int V = R * NT;
   constexpr int L = Log2<V>::value;
+  pdl_wait();
   const int u = blockIdx.x / row_tiles;
   const int tile = blockIdx.x - u * row_tiles;
   if (u >= plan.meta[kMetaNumActive]) return;
@@ -524,9 +500,7 @@ cudaError_t launch_stream(StreamArgs a, size_t smem, int64_t bound_units, cudaSt
   }
   const int64_t grid = std::min<int64_t>(num_sms(), bound_units);
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, kStreamThreads, smem, stream>>>(a);
-  note_launch();
-  return cudaGetLastError();
+  return launch_after_previous(kern, dim3((unsigned)grid), dim3(kStreamThreads), smem, stream, a);
 }
 
 template <typename Tok>
@@ -539,10 +513,9 @@ cudaError_t launch_direct(const Tok* x, const uint8_t* packed, const uint8_t* sc
   const int64_t blocks = std::min<int64_t>(E, T * K) * row_tiles;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  gemv_direct_kernel<Tok, R, NT><<<(unsigned)blocks, kDirectThreads, 0, stream>>>(
-      x, packed, scales, plan, part, (int)(I / 32), (int)O, (int)I, (int)K, (int)row_tiles);
-  note_launch();
-  return cudaGetLastError();
+  return launch_after_previous(gemv_direct_kernel<Tok, R, NT>, dim3((unsigned)blocks),
+                               dim3(kDirectThreads), 0, stream, x, packed, scales, plan, part,
+                               (int)(I / 32), (int)O, (int)I, (int)K, (int)row_tiles);
 }
 
 // Shape of the staged GEMV for a row width of G groups: group columns,
@@ -583,10 +556,9 @@ bool gemv_uses_stream(int64_t I) { return stream_shape(I / 32).rws > 0; }
 cudaError_t launch_prep_tokens(const void* x, __half* x16, int* sigma, int64_t T, int64_t I,
                                cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  prep_tokens_kernel<<<(unsigned)((T + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(x), x16, sigma, (int)T, (int)I);
-  note_launch();
-  return cudaGetLastError();
+  return launch_after_previous(prep_tokens_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0,
+                               stream, static_cast<const __nv_bfloat16*>(x), x16, sigma, (int)T,
+                               (int)I);
 }
 
 cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const int* sigma,

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -52,9 +53,23 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
 
 size_t route_global_counter_words(int64_t E);
 
+// Tokens prepared for the staged GEMV (bf16 tokens): x16 = f16(x 2^sigma).
+struct TokenPrep {
+  const void* x;    // bf16 tokens (T, I), or nullptr: nothing to prepare
+  __half* x16;
+  int* sigma;
+  int64_t I;
+};
+
+// Bucketer; also prepares the tokens in the same launch when `prep.x` is set.
 cudaError_t launch_route(const void* sel, int index_dtype, int64_t T,
                          int64_t K, int64_t E, int* wc_global,
-                         const RoutePlan& plan, cudaStream_t stream);
+                         const RoutePlan& plan, const TokenPrep& prep,
+                         cudaStream_t stream);
+
+// True when token prep for these sizes fits in the bucketer's launch.
+bool prep_fits_route(int64_t T, int64_t I);
+
 
 // True when the rows of width I fit the staged (bulk-copy) GEMV; bf16
 // tokens then need launch_prep_tokens first.
@@ -87,5 +102,26 @@ cudaError_t read_and_reset_status(cudaStream_t stream, int word, int64_t* out);
 
 // Counts kernel launches made by the library (process-wide).
 void note_launch();
+
+// Launches `kernel` so that it may start before the previous kernel on
+// `stream` finishes (programmatic stream serialization); the kernel must call
+// pdl_wait() before it reads anything that kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  if (err == cudaSuccess) note_launch();
+  return err;
+}
 
 }  // namespace mxfp4el

@@ -60,7 +60,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int* t
 template <typename Idx>
 __global__ void __launch_bounds__(kRouteThreads, 1)
 route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
-             RoutePlan plan) {
+             RoutePlan plan, int T, TokenPrep prep) {
+  pdl_launch_dependents();
   extern __shared__ int smem_wc[];
   __shared__ int warp_buf[33];
   int* wc = wc_global != nullptr ? wc_global : smem_wc;   // [warp][expert]
@@ -143,6 +144,12 @@ route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) bad += __shfl_xor_sync(kFullMask, bad, o);
   if (lane == 0 && bad > 0) atomicAdd(&g_status[kStatusBadPairs], (unsigned long long)bad);
+
+  // Token prep for the staged GEMV, one warp per token.
+  if (prep.x != nullptr)
+    for (int t = warp; t < T; t += kRouteWarps)
+      prep_token(static_cast<const __nv_bfloat16*>(prep.x), prep.x16, prep.sigma, t,
+                 (int)prep.I, lane);
 }
 
 }  // namespace
@@ -152,9 +159,11 @@ size_t route_global_counter_words(int64_t E) {
              ? (size_t)kRouteWarps * (size_t)E : 0;
 }
 
+bool prep_fits_route(int64_t T, int64_t I) { return T <= 64 && T * I <= ((int64_t)1 << 20); }
+
 cudaError_t launch_route(const void* sel, int index_dtype, int64_t T, int64_t K,
                          int64_t E, int* wc_global, const RoutePlan& plan,
-                         cudaStream_t stream) {
+                         const TokenPrep& prep, cudaStream_t stream) {
   const int64_t P = T * K;
   const size_t smem = wc_global ? 0 : kRouteWarps * (size_t)E * sizeof(int);
   // Dynamic plus static shared memory above 48 KiB needs the opt-in.
@@ -170,10 +179,10 @@ cudaError_t launch_route(const void* sel, int index_dtype, int64_t T, int64_t K,
   }
   if (index_dtype == kIndexI64)
     route_kernel<int64_t><<<1, kRouteThreads, smem, stream>>>(
-        static_cast<const int64_t*>(sel), P, (int)E, wc_global, plan);
+        static_cast<const int64_t*>(sel), P, (int)E, wc_global, plan, (int)T, prep);
   else
     route_kernel<int32_t><<<1, kRouteThreads, smem, stream>>>(
-        static_cast<const int32_t*>(sel), P, (int)E, wc_global, plan);
+        static_cast<const int32_t*>(sel), P, (int)E, wc_global, plan, (int)T, prep);
   note_launch();
   return cudaGetLastError();
 }
