@@ -2,6 +2,8 @@
 // workspace, and the launch sequence route -> GEMV -> combine on one stream.
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -78,6 +80,32 @@ void mark(int stage, bool begin, cudaStream_t stream) {
   if (ev != nullptr) cudaEventRecord(ev, stream);
 }
 
+}  // namespace
+
+LinearPath choose_path(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype) {
+  const bool tc_ok = token_dtype == MXFP4EL_DTYPE_BF16 && gemm_tc_supported(E, I, O);
+  // Test knob: MXFP4EL_PATH=gemv or gemm forces a kernel where it applies.
+  if (const char* env = std::getenv("MXFP4EL_PATH")) {
+    if (std::strcmp(env, "gemv") == 0) return LinearPath::kGemv;
+    if (std::strcmp(env, "gemm") == 0 && tc_ok) return LinearPath::kGemm;
+  }
+  if (!tc_ok) return LinearPath::kGemv;
+  // Tensor cores pay off once experts average about 16 tokens: the GEMV's
+  // CUDA-core work grows with the tokens per expert, the GEMM's MMA does not
+  // until N passes 16.
+  const int64_t P = T * K;
+  const int64_t slots = std::max<int64_t>(1, std::min<int64_t>(E, P));
+  return P >= 16 * slots ? LinearPath::kGemm : LinearPath::kGemv;
+}
+
+int linear_partial_columns(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                           int token_dtype) {
+  return choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm ? 1
+                                                                       : gemv_partial_columns(I);
+}
+
+namespace {
+
 int run(const void* x, const uint8_t* packed, const uint8_t* scales,
         const void* sel, const float* p, const void* ys, void* out, int64_t T,
         int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype,
@@ -86,7 +114,8 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
   if (K > 0) {
     unsigned long long* status = device_status_words();
     if (status == nullptr) return MXFP4EL_ERR_CUDA;
-    const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
+    const bool gemm = choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
+    const bool prep = !gemm && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
     const bool prep_in_route = prep && prep_fits_route(T, I);
     TokenPrep tp = {prep_in_route ? x : nullptr, ws.x16, ws.sigma, I};
     mark(MXFP4EL_STAGE_ROUTE, true, stream);
@@ -96,14 +125,19 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
     mark(MXFP4EL_STAGE_ROUTE, false, stream);
     if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
     mark(MXFP4EL_STAGE_LINEAR, true, stream);
-    err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, packed, scales, ws.plan,
-                      ws.part, status, T, E, I, O, K, stream);
+    if (gemm)
+      err = launch_gemm_tc(x, packed, scales, ws.plan, ws.grouped, ws.part, status, T, E, I, O,
+                           K, stream);
+    else
+      err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, packed, scales, ws.plan,
+                        ws.part, status, T, E, I, O, K, stream);
     mark(MXFP4EL_STAGE_LINEAR, false, stream);
     if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
   }
   mark(MXFP4EL_STAGE_COMBINE, true, stream);
-  err = launch_combine(ys, sel, index_dtype, p, ws.part, gemv_partial_columns(I), out,
-                       token_dtype, T, E, O, K, stream);
+  err = launch_combine(ys, sel, index_dtype, p, ws.part,
+                       linear_partial_columns(T, E, I, O, K, token_dtype), out, token_dtype, T,
+                       E, O, K, stream);
   mark(MXFP4EL_STAGE_COMBINE, false, stream);
   return err == cudaSuccess ? MXFP4EL_OK : MXFP4EL_ERR_CUDA;
 }
@@ -139,10 +173,12 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
   ws->plan.pair_list = reinterpret_cast<int*>(take((size_t)P * sizeof(int)));
   const size_t wc_words = route_global_counter_words(E);
   ws->wc_global = wc_words ? reinterpret_cast<int*>(take(wc_words * sizeof(int))) : nullptr;
-  const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && K > 0;
+  const bool gemm = K > 0 && choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
+  const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && K > 0 && !gemm;
   ws->x16 = prep ? reinterpret_cast<__half*>(take((size_t)T * I * sizeof(__half))) : nullptr;
   ws->sigma = prep ? reinterpret_cast<int*>(take((size_t)T * sizeof(int))) : nullptr;
-  const size_t ncol = (size_t)gemv_partial_columns(I);
+  ws->grouped = gemm ? take(gemm_tc_grouped_bytes(T, K, I)) : nullptr;
+  const size_t ncol = (size_t)linear_partial_columns(T, E, I, O, K, token_dtype);
   ws->part = reinterpret_cast<float*>(take((size_t)P * ncol * (size_t)O * sizeof(float)));
   ws->bytes = off;
   return true;

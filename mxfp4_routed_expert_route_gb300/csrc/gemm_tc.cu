@@ -1,0 +1,551 @@
+// gemm_tc.cu -- prefill-regime routed expert grouped GEMM on the 5th-gen
+// tensor cores (tcgen05, TMEM, TMA).
+//
+// For every selected expert e and each block of up to 192 of its tokens it
+// computes part[t*K+k, o] = sum_i W_e[o, i] x[t, i] for all output rows o,
+// with W_e decoded from MXFP4 as in the problem statement ("MXFP4 Routed
+// Expert Linear", Kimi K3): W_e[o, 32g+2j (+1)] = LUT[low (high) nibble of
+// packed[e,o,g,j]] * 2^(scales[e,o,g] - 127).
+//
+// Shape ("swap AB"): M = 128 weight rows per tile, N = the tokens of one
+// block (16..192, a multiple of 16), K = I in chunks of 64 (two groups).
+//   * A (weights) is decoded exactly to bf16 -- every E2M1 value times a
+//     power of two is a bf16 number while it stays in bf16's range -- and
+//     written straight into tensor memory: row m in TMEM lane m, two K
+//     elements per 32-bit column.
+//   * B (tokens) is a copy of x with the rows grouped by expert (written by
+//     gather_tokens_kernel); TMA loads 64-wide K chunks with the 128-byte
+//     swizzle that the K-major shared-memory descriptor describes.
+//   * tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), accumulator in TMEM.
+//
+// Warp roles in a CTA of 16 warps (one CTA per SM, persistent over units
+// (expert, token block, 128-row tile)):
+//   warp 0      TMA producer (lane 0) and TMEM allocation
+//   warp 1      MMA issuer (lane 0)
+//   warps 4-11  dequantize: thread (row m, half h) decodes group 2kc+h of
+//               row m into 16 TMEM columns
+//   warps 12-15 epilogue: TMEM -> registers -> float32 partial results
+// Two A buffers and two accumulators in TMEM let dequantize, MMA and the
+// epilogue of consecutive chunks and units overlap. Every wait is bounded;
+// a role whose wait gives up records it, stops, and the CTA still waits
+// (bounded) for its own copies and MMAs before freeing TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mxfp4el {
+namespace {
+
+constexpr int kTcThreads = 512;
+constexpr int kBM = 128;                    // weight rows per tile
+constexpr int kBK = 64;                     // K elements per stage
+constexpr int kNMax = 192;                  // tokens per block
+constexpr int kStagesMax = 6;
+constexpr uint32_t kStageB = kNMax * 128;   // token tile, 128 B per row
+constexpr uint32_t kStageA = kBM * 32;      // packed bytes, 32 B per row
+constexpr uint32_t kStageBytes = kStageB + kStageA;
+static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kDCol = 0;               // two accumulators of kNMax columns
+constexpr uint32_t kACol = 2 * kNMax;       // two A buffers of 32 columns
+constexpr int kDequantWarp0 = 4, kDequantWarps = 8, kEpiWarp0 = 12;
+constexpr int kNumLoads = 5;                // token-box heights
+__host__ __device__ constexpr int load_rows(int l) {
+  return l == 0 ? 16 : l == 1 ? 32 : l == 2 ? 64 : l == 3 ? 128 : 192;
+}
+
+struct TcArgs {
+  RoutePlan plan;
+  const uint8_t* scales;
+  const uint8_t* scales_end;
+  float* part;                   // [T*K, O]
+  unsigned long long* status;
+  int G, O, K;
+  int mtiles;                    // ceil(O / 128)
+  int stages;
+  uint32_t scale_cap;            // bytes per scale buffer
+};
+
+struct TcMaps {
+  CUtensorMap a;                 // packed weights as uint8 [E*O, G*16], box {32, 128}
+  CUtensorMap b[kNumLoads];      // grouped tokens bf16 [P, I], box {64, rows}, 128B swizzle
+};
+
+struct __align__(8) TcShared {
+  uint64_t full[kStagesMax], empty[kStagesMax];
+  uint64_t a_full[2], a_empty[2];
+  uint64_t d_full[2], d_empty[2];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int scale_off[2];              // per scale buffer: offset of the tile's first byte, or -1
+  int num_units;
+  int num_active;
+  int unit_prefix[1];            // [num_active + 1], flexible
+};
+
+// One unit of work, derived identically by every role from its index.
+struct Unit {
+  int e;          // expert id
+  int m0;         // first weight row
+  int rows;       // weight rows in the tile (<= 128)
+  int tok0;       // first position of the block in the grouped token list
+  int ntok;       // tokens in the block
+  int nmma;       // MMA N: ntok rounded up to 16
+  int load;       // token box: load_rows(load) >= nmma
+};
+
+__device__ __forceinline__ Unit unit_at(const TcArgs& a, const TcShared& sh, int idx) {
+  // Binary search the expert whose block range holds idx / mtiles.
+  const int blk = idx / a.mtiles;
+  const int mt = idx - blk * a.mtiles;
+  int lo = 0, hi = sh.num_active;         // unit_prefix[u] <= blk < unit_prefix[u + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sh.unit_prefix[mid] <= blk) lo = mid;
+    else hi = mid;
+  }
+  const int u = lo;
+  const int j = blk - sh.unit_prefix[u];
+  const int nblk = sh.unit_prefix[u + 1] - sh.unit_prefix[u];
+  Unit w;
+  w.e = a.plan.active[u];
+  const int beg = a.plan.offsets[w.e], cnt = a.plan.offsets[w.e + 1] - beg;
+  // Equal blocks, each a multiple of 16 tokens except the last.
+  const int bsz = (((cnt + nblk - 1) / nblk) + 15) / 16 * 16;
+  w.tok0 = beg + j * bsz;
+  w.ntok = min(bsz, cnt - j * bsz);
+  w.nmma = (w.ntok + 15) / 16 * 16;
+  w.load = 0;
+  while (load_rows(w.load) < w.nmma) ++w.load;
+  w.m0 = mt * kBM;
+  w.rows = min(kBM, a.O - w.m0);
+  return w;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
+// both K-major, shape M x N.
+__device__ __forceinline__ uint32_t mma_idesc(int m, int n) {
+  return (1u << 4)                       // D format: fp32
+         | (1u << 7)                     // A format: bf16
+         | (1u << 10)                    // B format: bf16
+         | ((uint32_t)(n >> 3) << 17)    // N / 8
+         | ((uint32_t)(m >> 4) << 24);   // M / 16
+}
+
+// Shared-memory descriptor of a K-major tile with the 128-byte swizzle:
+// 128-byte rows, 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu)    // start address
+         | ((uint64_t)1 << 16)                // leading byte offset (unused here)
+         | ((uint64_t)(1024 >> 4) << 32)      // stride byte offset: 8 rows
+         | ((uint64_t)1 << 46)                // descriptor version
+         | ((uint64_t)2 << 61);               // layout: 128-byte swizzle
+}
+
+// 16 packed bytes (32 codes) and their scale byte -> 16 bf16x2 words, the
+// values LUT[code] * 2^(s - 127) (low nibble in the low half). The E2M1
+// value is widened to float32 and multiplied by the two exact factors of
+// e8m0_split, so the product is exact for every byte s; converting it to
+// bf16 is exact whenever the value is a bf16 number (s = 2..253 always).
+__device__ __forceinline__ void dequant_group_bf16(const uint4& q, uint32_t s, uint32_t (&w)[16]) {
+  const float2 f = e8m0_split(s);
+  const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2x4(words[k], h);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 v = fmul2(fmul2(f16x2_to_f32x2(h[b]), make_float2(f.x, f.x)),
+                             make_float2(f.y, f.y));
+      const __nv_bfloat162 r = __floats2bfloat162_rn(v.x, v.y);
+      w[4 * k + b] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // Stages need 1024-byte alignment (128-byte swizzle atoms).
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* stages = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  unsigned char* scale_buf = stages + (size_t)a.stages * kStageBytes;
+  TcShared& sh = *reinterpret_cast<TcShared*>(scale_buf + 2 * a.scale_cap);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], kDequantWarps + 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.a_full[b], kDequantWarps);
+      mbar_init(&sh.a_empty[b], 1);
+      mbar_init(&sh.d_full[b], 1);
+      mbar_init(&sh.d_empty[b], 4);
+      mbar_init(&sh.s_full[b], 1);
+      mbar_init(&sh.s_empty[b], kDequantWarps);
+    }
+    mbar_init(&sh.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&sh.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  pdl_wait();                    // routing lists and grouped tokens are ready
+  if (warp == 2) {
+    // Units: for each active expert, ceil(count / 192) token blocks, each
+    // with mtiles row tiles.
+    const int na = a.plan.meta[kMetaNumActive];
+    int run = 0;
+    for (int base = 0; base < na; base += 32) {
+      const int u = base + lane;
+      int nb = 0;
+      if (u < na) {
+        const int e = a.plan.active[u];
+        const int cnt = a.plan.offsets[e + 1] - a.plan.offsets[e];
+        nb = (cnt + kNMax - 1) / kNMax;
+      }
+      int incl = nb;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (u < na) sh.unit_prefix[u] = run + incl - nb;
+      run += __shfl_sync(kFullMask, incl, 31);
+    }
+    if (lane == 0) {
+      sh.unit_prefix[na] = run;
+      sh.num_active = na;
+      sh.num_units = run * a.mtiles;
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = sh.tmem_base;
+  const int num_units = sh.num_units;
+  const int G = a.G, O = a.O;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_evict_first_policy();   // weights: read once
+      const uint64_t pol_x = l2_evict_last_policy();    // tokens: reread per tile
+      int chunk = 0, it = 0;
+      const int nk = G / 2;                              // chunks of 64 = 2 groups
+      for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
+        const Unit w = unit_at(a, sh, idx);
+        if (w.ntok <= 0) { --it; continue; }
+        // The tile's scale bytes, by one bulk copy of the aligned span that
+        // holds them when it stays inside the scales buffer.
+        const int sb = it & 1;
+        if (!mbar_wait(&sh.s_empty[sb], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
+        const size_t row0 = (size_t)w.e * O + w.m0;
+        const uintptr_t s_lo = reinterpret_cast<uintptr_t>(a.scales + row0 * G);
+        const uintptr_t s_hi = s_lo + (uintptr_t)w.rows * G;
+        const uintptr_t c_lo = s_lo & ~(uintptr_t)15, c_hi = (s_hi + 15) & ~(uintptr_t)15;
+        const bool copy = c_hi <= reinterpret_cast<uintptr_t>(a.scales_end) &&
+                          c_hi - c_lo <= a.scale_cap;
+        sh.scale_off[sb] = copy ? (int)(s_lo - c_lo) : -1;
+        if (copy) {
+          mbar_arrive_expect_tx(&sh.s_full[sb], (uint32_t)(c_hi - c_lo));
+          bulk_copy_g2s(scale_buf + (size_t)sb * a.scale_cap, reinterpret_cast<const void*>(c_lo),
+                        (uint32_t)(c_hi - c_lo), &sh.s_full[sb], pol_w);
+        } else {
+          mbar_arrive(&sh.s_full[sb]);
+        }
+        const uint32_t tx = kStageA + (uint32_t)load_rows(w.load) * 128u;
+        for (int kc = 0; kc < nk; ++kc, ++chunk) {
+          const int st = chunk % a.stages;
+          if (!mbar_wait(&sh.empty[st], ((uint32_t)(chunk / a.stages) & 1u) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          unsigned char* sp = stages + (size_t)st * kStageBytes;
+          mbar_arrive_expect_tx(&sh.full[st], tx);
+          tma_load_2d(sp + kStageB, &maps.a, kc * 32, (int)row0, &sh.full[st], pol_w);
+          tma_load_2d(sp, &maps.b[w.load], kc * kBK, w.tok0, &sh.full[st], pol_x);
+        }
+      }
+      if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+      // Wait (bounded) until the copies this thread issued have landed.
+      for (int k = max(0, chunk - a.stages); k < chunk; ++k)
+        if (!mbar_wait(&sh.full[k % a.stages], (uint32_t)(k / a.stages) & 1u)) break;
+      for (int k = max(0, it - 2); k < it; ++k)
+        if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)(k >> 1) & 1u)) break;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int chunk = 0, it = 0, ach = 0;
+      const int nk = G / 2;
+      for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
+        const Unit w = unit_at(a, sh, idx);
+        if (w.ntok <= 0) { --it; continue; }
+        const int db = it & 1;
+        if (!mbar_wait(&sh.d_empty[db], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t idesc = mma_idesc(kBM, w.nmma);
+        const uint32_t d_tmem = tmem + kDCol + (uint32_t)db * kNMax;
+        for (int kc = 0; kc < nk; ++kc, ++chunk, ++ach) {
+          const int st = chunk % a.stages;
+          const int ab = ach & 1;
+          if (!mbar_wait(&sh.full[st], (uint32_t)(chunk / a.stages) & 1u) ||
+              !mbar_wait(&sh.a_full[ab], (uint32_t)(ach >> 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t b_addr = smem_addr(stages + (size_t)st * kStageBytes);
+          const uint32_t a_tmem = tmem + kACol + (uint32_t)ab * 32;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
+                      (kc > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&sh.a_empty[ab]);      // A buffer free once these MMAs finish
+          tc_commit(&sh.empty[st]);        // token tile consumed
+        }
+        if (!ok) break;
+        tc_commit(&sh.d_full[db]);         // accumulator complete
+      }
+      if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+      // Do not free TMEM under running MMAs: wait (bounded) for all of them.
+      tc_commit(&sh.drain);
+      mbar_wait(&sh.drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + kDequantWarps) {
+    // -------------------------------------------------------- dequantizers
+    const int q = warp & 3;                          // TMEM lane quarter
+    const int h = (warp - kDequantWarp0) >> 2;       // group of the chunk
+    const int m = 32 * q + lane;                     // weight row in the tile
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    int chunk = 0, it = 0, ach = 0;
+    const int nk = G / 2;
+    for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
+      const Unit w = unit_at(a, sh, idx);
+      if (w.ntok <= 0) { --it; continue; }
+      const int sb = it & 1;
+      if (!mbar_wait(&sh.s_full[sb], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
+      const int soff = sh.scale_off[sb];
+      const unsigned char* srow = scale_buf + (size_t)sb * a.scale_cap + (soff < 0 ? 0 : soff) +
+                                  (size_t)min(m, w.rows - 1) * G;
+      const uint8_t* grow = a.scales + ((size_t)w.e * O + w.m0 + min(m, w.rows - 1)) * G;
+      for (int kc = 0; kc < nk; ++kc, ++chunk, ++ach) {
+        const int st = chunk % a.stages;
+        const int ab = ach & 1;
+        if (!mbar_wait(&sh.full[st], (uint32_t)(chunk / a.stages) & 1u)) { ok = false; break; }
+        const unsigned char* sp = stages + (size_t)st * kStageBytes + kStageB;
+        const uint4 pk = *reinterpret_cast<const uint4*>(sp + m * 32 + h * 16);
+        const int g = 2 * kc + h;
+        const uint32_t sbyte = soff >= 0 ? (uint32_t)srow[g] : (uint32_t)__ldg(grow + g);
+        uint32_t v[16];
+        dequant_group_bf16(pk, sbyte, v);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty[st]);   // packed bytes consumed
+        if (!mbar_wait(&sh.a_empty[ab], ((uint32_t)(ach >> 1) & 1u) ^ 1u)) { ok = false; break; }
+        tc_fence_after_sync();
+        tmem_st16(tmem + lane_base + kACol + (uint32_t)ab * 32 + (uint32_t)h * 16, v);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.a_full[ab]);
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
+    }
+    if (!ok && lane == 0) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int m = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    int it = 0;
+    for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
+      const Unit w = unit_at(a, sh, idx);
+      if (w.ntok <= 0) { --it; continue; }
+      const int db = it & 1;
+      if (!mbar_wait(&sh.d_full[db], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
+      tc_fence_after_sync();
+      const bool row_ok = m < w.rows;
+      float* out_col = a.part + w.m0 + m;
+      for (int c0 = 0; c0 < w.nmma; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_base + kDCol + (uint32_t)db * kNMax + (uint32_t)c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int n = c0 + i;
+          if (row_ok && n < w.ntok) {
+            const int pair = a.plan.pair_list[w.tok0 + n];
+            out_col[(size_t)pair * O] = __uint_as_float(v[i]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.d_empty[db]);
+    }
+    if (!ok && lane == 0) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// x rows grouped by expert: xg[pos, :] = x[pair_list[pos] / K, :].
+__global__ void __launch_bounds__(256)
+gather_tokens_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xg,
+                     RoutePlan plan, int I, int K) {
+  pdl_launch_dependents();
+  pdl_wait();                    // the bucketer's lists are ready
+  const int npairs = plan.meta[kMetaNumPairs];
+  const int vec_per_row = I / 8;
+  const int warps = blockDim.x / 32;
+  for (int pos = blockIdx.x * warps + (threadIdx.x >> 5); pos < npairs; pos += gridDim.x * warps) {
+    const int t = plan.pair_list[pos] / K;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * I);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)pos * I);
+    for (int v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int num_sms_tc() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 152;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 152;
+  }
+  return cached[dev];
+}
+
+size_t tc_shared_bytes(int stages, uint32_t scale_cap, int64_t E) {
+  return 1024 + (size_t)stages * kStageBytes + 2 * (size_t)scale_cap + sizeof(TcShared) +
+         (size_t)(E + 1) * sizeof(int);
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int64_t E, int64_t I, int64_t O) {
+  const int64_t G = I / 32;
+  if (G % 2 != 0) return false;                    // K chunks of 64
+  if (E > 4096 || E * O > 0x7fffffff) return false;
+  const uint32_t scale_cap = (uint32_t)((kBM * G + 31) / 16 * 16);
+  return tc_shared_bytes(3, scale_cap, E) <= 227 * 1024;
+}
+
+size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I) {
+  return (size_t)T * K * I * sizeof(__nv_bfloat16);
+}
+
+cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* scales,
+                           const RoutePlan& plan, void* grouped, float* part,
+                           unsigned long long* status, int64_t T, int64_t E, int64_t I,
+                           int64_t O, int64_t K, cudaStream_t stream) {
+  const int64_t G = I / 32, P = T * K;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+
+  // 1. tokens grouped by expert
+  {
+    const int64_t blocks = std::min<int64_t>((P + 7) / 8, (int64_t)num_sms_tc() * 8);
+    cudaError_t err = launch_after_previous(
+        gather_tokens_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), 0, stream,
+        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(grouped), plan, (int)I,
+        (int)K);
+    if (err != cudaSuccess) return err;
+  }
+
+  // 2. tensor maps
+  TcMaps maps;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)(G * 16), (cuuint64_t)(E * O)};
+    const cuuint64_t strides[1] = {(cuuint64_t)(G * 16)};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kBM};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  for (int l = 0; l < kNumLoads; ++l) {
+    const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)std::max<int64_t>(P, 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)(I * 2)};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)load_rows(l)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&maps.b[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, grouped, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+
+  // 3. the GEMM
+  TcArgs args;
+  args.plan = plan;
+  args.scales = scales;
+  args.scales_end = scales + (size_t)E * O * G;
+  args.part = part;
+  args.status = status;
+  args.G = (int)G;
+  args.O = (int)O;
+  args.K = (int)K;
+  args.mtiles = (int)((O + kBM - 1) / kBM);
+  args.scale_cap = (uint32_t)((kBM * G + 31) / 16 * 16);
+  int stages = kStagesMax;
+  while (stages > 2 && tc_shared_bytes(stages, args.scale_cap, E) > 227 * 1024) --stages;
+  args.stages = stages;
+  const size_t smem = tc_shared_bytes(stages, args.scale_cap, E);
+  static std::mutex mu;
+  static size_t opted[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && opted[dev] < smem) {
+      cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      opted[dev] = smem;
+    }
+  }
+  return launch_after_previous(gemm_tc_kernel, dim3((unsigned)num_sms_tc()), dim3(kTcThreads),
+                               smem, stream, maps, args);
+}
+
+}  // namespace mxfp4el

@@ -43,6 +43,7 @@ struct Workspace {
   int* wc_global;   // per-warp counters when they do not fit in shared memory
   __half* x16;      // [T, I] tokens scaled by 2^sigma_t in f16 (bf16 tokens)
   int* sigma;       // [T] the power of two of each token (bf16 tokens)
+  void* grouped;    // [T*K, I] bf16 tokens grouped by expert (tensor-core path)
   float* part;      // [T*K, ncol, O] float32 partial results of every pair
   size_t bytes;     // total
 };
@@ -50,6 +51,10 @@ struct Workspace {
 // Offsets of every region for the given sizes; base == nullptr only sizes.
 bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
                      int64_t K, int token_dtype, Workspace* ws);
+
+// Partial results per (pair, row) that the chosen linear kernel writes.
+int linear_partial_columns(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                           int token_dtype);
 
 size_t route_global_counter_words(int64_t E);
 
@@ -88,6 +93,18 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16,
                         const uint8_t* scales, const RoutePlan& plan, float* part,
                         unsigned long long* status, int64_t T, int64_t E,
                         int64_t I, int64_t O, int64_t K, cudaStream_t stream);
+
+// Prefill-regime grouped GEMM on the tensor cores (bf16 tokens).
+bool gemm_tc_supported(int64_t E, int64_t I, int64_t O);
+size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I);
+cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* scales,
+                           const RoutePlan& plan, void* grouped, float* part,
+                           unsigned long long* status, int64_t T, int64_t E, int64_t I,
+                           int64_t O, int64_t K, cudaStream_t stream);
+
+// Which kernel computes the routed linear for these sizes.
+enum class LinearPath { kGemv, kGemm };
+LinearPath choose_path(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype);
 
 cudaError_t launch_combine(const void* y_shared, const void* sel,
                            int index_dtype, const float* p, const float* part,

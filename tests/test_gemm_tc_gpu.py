@@ -1,0 +1,87 @@
+"""GPU parity of the tensor-core (tcgen05) grouped GEMM path.
+
+The library picks the tensor-core kernel for bf16 tokens when experts
+average at least 16 tokens; MXFP4EL_PATH=gemm forces it for these cases so
+that small shapes exercise every edge: output widths that are not a multiple
+of the 128-row tile, token counts around the 16-token MMA granule and the
+192-token block, a single 64-wide K chunk, and many experts.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_parity, oracle_rows, run_gpu
+from mxfp4_routed_expert_route_gb300 import wait_timeouts, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _force_gemm(monkeypatch):
+    monkeypatch.setenv("MXFP4EL_PATH", "gemm")
+
+
+def _one_expert_sel(T, K, E, hot, rng):
+    """Slot 0 of every token on expert `hot`, the other slots elsewhere."""
+    sel = np.zeros((T, K), dtype=np.int32)
+    for t in range(T):
+        others = rng.permutation([e for e in range(E) if e != hot])[:K - 1]
+        sel[t] = np.concatenate([[hot], others])
+    return torch.from_numpy(sel)
+
+
+@pytest.mark.parametrize("T,E,K,I,O", [
+    (8, 2, 1, 64, 128),        # one K chunk, one row tile
+    (40, 3, 2, 128, 200),      # row tile with 72 rows
+    (64, 4, 2, 320, 257),
+    (300, 12, 3, 256, 130),
+    (97, 5, 4, 2880, 384),     # the decode/prefill width
+])
+def test_gemm_path_matches_oracle(T, E, K, I, O):
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, seed=T + O)
+    out = run_gpu(wl)
+    torch.cuda.synchronize()
+    assert wait_timeouts() == 0
+    want, absm, _ = oracle_rows(wl)
+    assert_parity(out, want, absm, wl.dtype, f"gemm {T},{E},{K},{I},{O}")
+
+
+@pytest.mark.parametrize("ntok", [1, 15, 16, 17, 191, 192, 193, 400])
+def test_gemm_token_block_edges(ntok):
+    # Expert 1 receives exactly ntok tokens (slot 0 of each); the other
+    # slot spreads over the remaining experts.
+    rng = np.random.default_rng(ntok)
+    T, E, K, I, O = ntok, 6, 2, 128, 136
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, seed=ntok)
+    sel = _one_expert_sel(T, K, E, 1, rng)
+    out = run_gpu(wl, sel=sel)
+    torch.cuda.synchronize()
+    assert wait_timeouts() == 0
+    want, absm, _ = oracle_rows(wl, sel=sel)
+    assert_parity(out, want, absm, wl.dtype, f"ntok={ntok}")
+
+
+def test_gemm_integer_inputs_exact():
+    # Integer tokens, unit scales, one slot with weight 1, zero shared output:
+    # every product and sum is exact in float32, so the bf16 result must be
+    # the oracle's value rounded to bf16.
+    rng = np.random.default_rng(31)
+    T, E, K, I, O = 48, 3, 1, 256, 160
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, scale_lo=127,
+                        scale_hi=127, seed=31)
+    wl.x = torch.from_numpy(rng.integers(-8, 9, (T, I)).astype(np.float32)).to(torch.bfloat16)
+    wl.y_shared = torch.zeros((T, O), dtype=torch.bfloat16)
+    wl.p = torch.ones((T, K), dtype=torch.float32)
+    out = run_gpu(wl)
+    want, _, _ = oracle_rows(wl)
+    assert torch.equal(out.cpu(), torch.from_numpy(want).to(torch.bfloat16))
+
+
+def test_gemm_and_gemv_agree(monkeypatch):
+    wl = workloads.make(160, 8, 4, 512, 264, dtype=torch.bfloat16, seed=33)
+    a = run_gpu(wl)
+    monkeypatch.setenv("MXFP4EL_PATH", "gemv")
+    b = run_gpu(wl)
+    want, absm, _ = oracle_rows(wl)
+    assert_parity(a, want, absm, wl.dtype, "gemm")
+    assert_parity(b, want, absm, wl.dtype, "gemv")
