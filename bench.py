@@ -74,6 +74,18 @@ def path_flops(wl, T=None):
     return 2 * T * wl.K * wl.O * wl.I
 
 
+def workload_is_hbm_bound(wl, U, peaks):
+    return (path_bytes(wl, U) / (peaks["hbm_gbs"] * 1e9)
+            >= path_flops(wl) / (peaks["bf16_tflops"] * 1e12))
+
+
+def sample_metric(wl, rows, hbm_bound, seconds):
+    """The metric for a token sample of the workload computed in `seconds`."""
+    if hbm_bound:
+        return sample_bytes(wl, rows) / seconds / 1e9, "GB/s"
+    return path_flops(wl, T=len(rows)) / seconds / 1e12, "TFLOP/s"
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -92,9 +104,14 @@ def source_digest(files):
     return h.hexdigest()
 
 
-LINEAR_SOURCES = ["mxfp4_routed_expert_route_gb300/csrc/gemv.cu",
-                  "mxfp4_routed_expert_route_gb300/csrc/common.cuh",
-                  "mxfp4_routed_expert_route_gb300/csrc/internal.h"]
+KERNEL_SOURCES = {
+    "gemv_kernel": ["mxfp4_routed_expert_route_gb300/csrc/gemv.cu",
+                    "mxfp4_routed_expert_route_gb300/csrc/common.cuh",
+                    "mxfp4_routed_expert_route_gb300/csrc/internal.h"],
+    "gemm_tc_kernel": ["mxfp4_routed_expert_route_gb300/csrc/gemm_tc.cu",
+                       "mxfp4_routed_expert_route_gb300/csrc/common.cuh",
+                       "mxfp4_routed_expert_route_gb300/csrc/internal.h"],
+}
 
 
 def ncu_traffic(kernel, workload):
@@ -103,10 +120,10 @@ def ncu_traffic(kernel, workload):
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)[kernel]
+            d = json.load(f)[f"{kernel}/{workload}"]
     except (OSError, ValueError, KeyError):
         return None
-    if d.get("workload") != workload or d.get("source_sha256") != source_digest(LINEAR_SOURCES):
+    if d.get("source_sha256") != source_digest(KERNEL_SOURCES[kernel]):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -195,7 +212,7 @@ def sample_bytes(wl, rows):
     return path_bytes(wl, U, T=len(rows))
 
 
-def cpu_baseline(wl, budget_s=15.0):
+def cpu_baseline(wl, hbm_bound, budget_s=15.0):
     """The oracle as it stands on this host's cores, on a bounded token sample."""
     import numpy as np
     import oracle
@@ -203,7 +220,8 @@ def cpu_baseline(wl, budget_s=15.0):
     n = int(max(1, min(wl.T, budget_s / max(one, 1e-6))))
     rows = np.arange(n)
     t = oracle_sample_time(wl, rows)
-    return {"value": sample_bytes(wl, rows) / t / 1e9, "unit": "GB/s",
+    v, unit = sample_metric(wl, rows, hbm_bound, t)
+    return {"value": v, "unit": unit,
             "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"tokens 0..{n - 1} of the {wl.name} batch ({n}/{wl.T}), "
                       f"all O={wl.O} rows, one run of {t:.2f} s"}
@@ -226,18 +244,20 @@ def run_reference(args, rank):
         oracle_sample_time(wl, rows)
     times = [oracle_sample_time(wl, rows) for _ in range(args.steps)]
     mean = sum(times) / len(times)
-    value = sample_bytes(wl, rows) / mean / 1e9
+    peaks, _ = load_peaks()
+    U = workloads.experts_touched(wl.sel, wl.E)
+    value, unit = sample_metric(wl, rows, workload_is_hbm_bound(wl, U, peaks), mean)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "K": wl.K, "I": wl.I,
                    "O": wl.O, "sample_tokens": n, "seed": wl.meta["seed"]},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
                          "kind": "oracle",
                          "sample": f"tokens 0..{n - 1} of the {wl.name} batch per step"},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -365,45 +385,69 @@ def run_ours(args, rank, world):
     if rank != 0:
         return
     peaks, peaks_src = load_peaks()
+    gemm = lib.mxfp4el_linear_path(wl.T, wl.E, wl.I, wl.O, wl.K,
+                                   _native.DTYPE_BF16 if token_bytes(wl) == 2
+                                   else _native.DTYPE_F32) == _native.PATH_GEMM
     bytes_step = path_bytes(wl, U)
     flops_step = path_flops(wl)
-    value = world * bytes_step * K / t_max / 1e9
-    tflops = world * flops_step * K / t_max / 1e12
-    ms_step = t_max / K * 1e3
     t_roof = max(bytes_step / (peaks["hbm_gbs"] * 1e9),
                  flops_step / (peaks["bf16_tflops"] * 1e12))
+    hbm_bound = workload_is_hbm_bound(wl, U, peaks)
+    gbps = world * bytes_step * K / t_max / 1e9
+    tflops = world * flops_step * K / t_max / 1e12
+    value, unit = (gbps, "GB/s") if hbm_bound else (tflops, "TFLOP/s")
+    ms_step = t_max / K * 1e3
     lin_mean_s = sum(lin_ms) / len(lin_ms) / 1e3
-    lin_bytes = linear_bytes(wl, U)
-    achieved = lin_bytes / lin_mean_s / 1e9
+    if gemm:
+        kernel = "gemm_tc_kernel"
+        lin_flops = 2.0 * int((wl.sel >= 0).sum()) * wl.O * wl.I
+        achieved = lin_flops / lin_mean_s / 1e12
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        roofline = {"bound": "tensor", "kernel": "gemm_tc_kernel (routed expert grouped GEMM)",
+                    "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak,
+                    "peak_source": f"bf16_tflops_sustained of {peaks_src} "
+                                   f"(burst {peaks['bf16_tflops']}: "
+                                   f"frac {achieved / peaks['bf16_tflops']:.3f})",
+                    "flops_per_launch": lin_flops, "launch_us": lin_mean_s * 1e6}
+    else:
+        kernel = "gemv_kernel"
+        lin_bytes = linear_bytes(wl, U)
+        achieved = lin_bytes / lin_mean_s / 1e9
+        roofline = {"bound": "hbm", "kernel": "gemv_stream_kernel (routed expert linear)",
+                    "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"],
+                    "peak_source": f"hbm_gbs of {peaks_src}",
+                    "bytes_per_launch": lin_bytes, "launch_us": lin_mean_s * 1e6}
+    roofline["traffic"] = ncu_traffic(kernel, wl.name)
+    e2e_v = world * (bytes_step if hbm_bound else flops_step) * K / float(e2e_t.item())
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if gemm else "f32",
+        "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "K": wl.K, "I": wl.I,
                    "O": wl.O, "tokens": "bf16" if token_bytes(wl) == 2 else "fp32",
                    "weights": "mxfp4 (e2m1 codes + e8m0 scale per 32)",
                    "picks": wl.meta["picks"], "experts_touched": U,
                    "seed": wl.meta["seed"], "parallelism": f"replicas x{world}",
+                   "linear": "tensor-core grouped GEMM" if gemm else "CUDA-core GEMV",
                    "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)"},
-        "tflops": tflops,
+        "gbps": gbps, "tflops": tflops,
         "path_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_step * 1e3,
                           "frac": t_roof / (ms_step / 1e3), "bytes_alg": bytes_step,
-                          "flops_alg": flops_step, "peaks": peaks_src},
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel (routed expert linear)",
-                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"],
-                     "peak_source": f"hbm_gbs of {peaks_src}",
-                     "bytes_per_launch": lin_bytes, "launch_us": lin_mean_s * 1e6,
-                     "traffic": ncu_traffic("gemv_kernel", wl.name)},
-        "e2e": {"value": world * bytes_step * K / float(e2e_t.item()) / 1e9,
-                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                          "flops_alg": flops_step, "peaks": peaks_src,
+                          "bound": "hbm" if hbm_bound else "tensor"},
+        "roofline": roofline,
+        "e2e": {"value": e2e_v / (1e9 if hbm_bound else 1e12), "unit": unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": float(e2e_t.item()) / K * 1e3},
         "gpu_launches": int(launches),
         "clocks": clocks,
         "wall_s": wall,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(wl, hbm_bound)
     print(json.dumps(line), flush=True)
 
 

@@ -204,10 +204,23 @@ int mxfp4el_wait_timeouts(void* stream, int64_t* count);
  * Returns MXFP4EL_ERR_INVALID_ARGUMENT for an unknown stage.
  */
 #define MXFP4EL_STAGE_ROUTE    0   /* routing bucketer (+ token prep) */
-#define MXFP4EL_STAGE_LINEAR   1   /* routed expert linear (GEMV)   */
+#define MXFP4EL_STAGE_LINEAR   1   /* routed expert linear (GEMV or GEMM) */
 #define MXFP4EL_STAGE_COMBINE  2   /* weighted combine onto y_shared */
-#define MXFP4EL_NUM_STAGES     3
+#define MXFP4EL_STAGE_GATHER   3   /* tokens grouped by expert (GEMM path) */
+#define MXFP4EL_NUM_STAGES     4
 int mxfp4el_set_stage_events(int stage, void* start_event, void* end_event);
+
+/*
+ * Which kernel computes the routed linear for these sizes: MXFP4EL_PATH_GEMV
+ * (CUDA cores, decode regime) or MXFP4EL_PATH_GEMM (tensor cores, bf16
+ * tokens, experts averaging 16 or more tokens). Negative for sizes the
+ * library rejects. The environment variable MXFP4EL_PATH=gemv|gemm, read at
+ * every call, forces one where it applies (a testing aid).
+ */
+#define MXFP4EL_PATH_GEMV 0
+#define MXFP4EL_PATH_GEMM 1
+int mxfp4el_linear_path(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                        int token_dtype);
 
 /* Kernel launches this process has made through the library so far. */
 int64_t mxfp4el_kernel_launches(void);

@@ -24,7 +24,10 @@ ERR_TOO_LARGE = -6
 STAGE_ROUTE = 0
 STAGE_LINEAR = 1
 STAGE_COMBINE = 2
-NUM_STAGES = 3
+STAGE_GATHER = 3
+NUM_STAGES = 4
+PATH_GEMV = 0
+PATH_GEMM = 1
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
 INDEX_I32 = 0
@@ -50,6 +53,7 @@ SIGNATURES = {
     "mxfp4el_wait_timeouts": (_INT, [_P, ctypes.POINTER(_I64)]),
     "mxfp4el_set_stage_events": (_INT, [_INT, _P, _P]),
     "mxfp4el_kernel_launches": (_I64, []),
+    "mxfp4el_linear_path": (_INT, [_I64, _I64, _I64, _I64, _I64, _INT]),
     "mxfp4el_status_string": (ctypes.c_char_p, [_INT]),
     "mxfp4el_version": (_INT, []),
 }

@@ -124,6 +124,12 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
       err = launch_prep_tokens(x, ws.x16, ws.sigma, T, I, stream);
     mark(MXFP4EL_STAGE_ROUTE, false, stream);
     if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
+    if (gemm) {
+      mark(MXFP4EL_STAGE_GATHER, true, stream);
+      err = launch_gather_tokens(x, ws.plan, ws.grouped, T, I, K, stream);
+      mark(MXFP4EL_STAGE_GATHER, false, stream);
+      if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
+    }
     mark(MXFP4EL_STAGE_LINEAR, true, stream);
     if (gemm)
       err = launch_gemm_tc(x, packed, scales, ws.plan, ws.grouped, ws.part, status, T, E, I, O,
@@ -293,6 +299,16 @@ extern "C" int mxfp4el_set_stage_events(int stage, void* start_event,
 }
 
 extern "C" int64_t mxfp4el_kernel_launches(void) { return g_launches.load(); }
+
+extern "C" int mxfp4el_linear_path(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                                   int token_dtype) {
+  if (token_dtype != MXFP4EL_DTYPE_F32 && token_dtype != MXFP4EL_DTYPE_BF16)
+    return MXFP4EL_ERR_UNSUPPORTED_DTYPE;
+  if (T < 0 || E < 0 || O < 0 || K < 0 || I <= 0 || I % 32 != 0 || !sizes_ok(T, E, I, O, K))
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  return choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm ? MXFP4EL_PATH_GEMM
+                                                                       : MXFP4EL_PATH_GEMV;
+}
 
 extern "C" const char* mxfp4el_status_string(int status) {
   switch (status) {

@@ -20,12 +20,15 @@
 //
 // Warp roles in a CTA of 16 warps (one CTA per SM, persistent over units
 // (expert, token block, 128-row tile)):
-//   warp 0      TMA producer (lane 0) and TMEM allocation
+//   warp 0      producer of scales and packed weights (lane 0; a deep ring
+//               of 4 KB stages covers HBM latency) and TMEM allocation
 //   warp 1      MMA issuer (lane 0)
+//   warp 2      per-expert lists in shared memory at start
+//   warp 3      producer of token tiles (lane 0)
 //   warps 4-11  dequantize: thread (row m, half h) decodes group 2kc+h of
 //               row m into 16 TMEM columns
 //   warps 12-15 epilogue: TMEM -> registers -> float32 partial results
-// Two A buffers and two accumulators in TMEM let dequantize, MMA and the
+// Four A buffers and two accumulators in TMEM let dequantize, MMA and the
 // epilogue of consecutive chunks and units overlap. Every wait is bounded;
 // a role whose wait gives up records it, stops, and the CTA still waits
 // (bounded) for its own copies and MMAs before freeing TMEM.
@@ -44,14 +47,16 @@ constexpr int kTcThreads = 512;
 constexpr int kBM = 128;                    // weight rows per tile
 constexpr int kBK = 64;                     // K elements per stage
 constexpr int kNMax = 192;                  // tokens per block
-constexpr int kStagesMax = 6;
+constexpr int kStagesAMax = 16;            // packed-weight ring (from HBM)
+constexpr int kRing = 4;                   // token stages = TMEM A buffers
 constexpr uint32_t kStageB = kNMax * 128;   // token tile, 128 B per row
 constexpr uint32_t kStageA = kBM * 32;      // packed bytes, 32 B per row
-constexpr uint32_t kStageBytes = kStageB + kStageA;
-static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
+static_assert(kStageB % 1024 == 0 && kStageA % 1024 == 0, "stages keep 1024-byte alignment");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 0;               // two accumulators of kNMax columns
-constexpr uint32_t kACol = 2 * kNMax;       // two A buffers of 32 columns
+constexpr uint32_t kACol = 2 * kNMax;       // kRing A buffers of 32 columns
+static_assert(kACol + kRing * 32 <= kTmemCols, "TMEM budget");
+constexpr int kMaxExpertsTc = 1024;         // per-expert lists kept in shared memory
 constexpr int kDequantWarp0 = 4, kDequantWarps = 8, kEpiWarp0 = 12;
 constexpr int kNumLoads = 5;                // token-box heights
 __host__ __device__ constexpr int load_rows(int l) {
@@ -66,7 +71,7 @@ struct TcArgs {
   unsigned long long* status;
   int G, O, K;
   int mtiles;                    // ceil(O / 128)
-  int stages;
+  int stages_a;
   uint32_t scale_cap;            // bytes per scale buffer
 };
 
@@ -76,8 +81,11 @@ struct TcMaps {
 };
 
 struct __align__(8) TcShared {
-  uint64_t full[kStagesMax], empty[kStagesMax];
-  uint64_t a_full[2], a_empty[2];
+  uint64_t full_a[kStagesAMax], empty_a[kStagesAMax];
+  // Chunk ring r = chunk % kRing: token stage r and TMEM A buffer r.
+  uint64_t full_b[kRing];        // tokens landed (TMA)
+  uint64_t a_full[kRing];        // A buffer written (dequantizers)
+  uint64_t done[kRing];          // the chunk's MMAs finished: stage and buffer free
   uint64_t d_full[2], d_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t drain;
@@ -85,7 +93,24 @@ struct __align__(8) TcShared {
   int scale_off[2];              // per scale buffer: offset of the tile's first byte, or -1
   int num_units;
   int num_active;
-  int unit_prefix[1];            // [num_active + 1], flexible
+  // Per active expert u: id, first position in the grouped list, tokens,
+  // and the prefix of token blocks (unit_prefix[num_active] = all blocks).
+  int ex_id[kMaxExpertsTc];
+  int ex_beg[kMaxExpertsTc];
+  int ex_cnt[kMaxExpertsTc];
+  int unit_prefix[kMaxExpertsTc + 1];
+};
+
+// Position in a ring of n slots: slot index and the parity of its use.
+struct RingPos {
+  int idx = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++idx == n) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
 };
 
 // One unit of work, derived identically by every role from its index.
@@ -113,8 +138,8 @@ __device__ __forceinline__ Unit unit_at(const TcArgs& a, const TcShared& sh, int
   const int j = blk - sh.unit_prefix[u];
   const int nblk = sh.unit_prefix[u + 1] - sh.unit_prefix[u];
   Unit w;
-  w.e = a.plan.active[u];
-  const int beg = a.plan.offsets[w.e], cnt = a.plan.offsets[w.e + 1] - beg;
+  w.e = sh.ex_id[u];
+  const int beg = sh.ex_beg[u], cnt = sh.ex_cnt[u];
   // Equal blocks, each a multiple of 16 tokens except the last.
   const int bsz = (((cnt + nblk - 1) / nblk) + 15) / 16 * 16;
   w.tok0 = beg + j * bsz;
@@ -169,26 +194,61 @@ __device__ __forceinline__ void dequant_group_bf16(const uint4& q, uint32_t s, u
   }
 }
 
+// The dequantizer's chunk loop for one tile: thread (row m, half h) decodes
+// group 2kc+h of its row for kc = 0..nk-1 into A buffer r of the chunk ring.
+// scale(g) returns the row's scale byte of group g. Returns false if a wait
+// gave up.
+template <typename ScaleFn>
+__device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* ring_a,
+                                             int stages_a, uint32_t tmem, uint32_t lane_base,
+                                             int m, int h, int lane, int nk, RingPos& pa,
+                                             RingPos& pr, ScaleFn scale) {
+  for (int kc = 0; kc < nk; ++kc) {
+    if (!mbar_wait(&sh.full_a[pa.idx], pa.phase)) return false;
+    const uint4 pk =
+        *reinterpret_cast<const uint4*>(ring_a + (size_t)pa.idx * kStageA + m * 32 + h * 16);
+    const uint32_t sbyte = scale(2 * kc + h);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty_a[pa.idx]);     // packed bytes consumed
+    pa.next(stages_a);
+    uint32_t v[16];
+    dequant_group_bf16(pk, sbyte, v);
+    if (!mbar_wait(&sh.done[pr.idx], pr.phase ^ 1u)) return false;   // buffer free
+    tc_fence_after_sync();
+    tmem_st16(tmem + lane_base + kACol + (uint32_t)pr.idx * 32 + (uint32_t)h * 16, v);
+    tmem_wait_st();
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.a_full[pr.idx]);
+    pr.next(kRing);
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // Stages need 1024-byte alignment (128-byte swizzle atoms).
+  // Token stages need 1024-byte alignment (128-byte swizzle atoms).
   const uint32_t raw = smem_addr(smem_raw);
-  unsigned char* stages = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  unsigned char* scale_buf = stages + (size_t)a.stages * kStageBytes;
+  unsigned char* ring_b = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  unsigned char* ring_a = ring_b + (size_t)kRing * kStageB;
+  unsigned char* scale_buf = ring_a + (size_t)a.stages_a * kStageA;
   TcShared& sh = *reinterpret_cast<TcShared*>(scale_buf + 2 * a.scale_cap);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < a.stages; ++s) {
-      mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], kDequantWarps + 1);
+    for (int s = 0; s < a.stages_a; ++s) {
+      mbar_init(&sh.full_a[s], 1);
+      mbar_init(&sh.empty_a[s], kDequantWarps);
+    }
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&sh.full_b[r], 1);
+      mbar_init(&sh.a_full[r], kDequantWarps);
+      mbar_init(&sh.done[r], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sh.a_full[b], kDequantWarps);
-      mbar_init(&sh.a_empty[b], 1);
       mbar_init(&sh.d_full[b], 1);
       mbar_init(&sh.d_empty[b], 4);
       mbar_init(&sh.s_full[b], 1);
@@ -203,8 +263,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   }
   pdl_wait();                    // routing lists and grouped tokens are ready
   if (warp == 2) {
-    // Units: for each active expert, ceil(count / 192) token blocks, each
-    // with mtiles row tiles.
+    // Per active expert: id, segment and token-block count (ceil(cnt / 192));
+    // units are (expert, token block, 128-row tile).
     const int na = a.plan.meta[kMetaNumActive];
     int run = 0;
     for (int base = 0; base < na; base += 32) {
@@ -212,7 +272,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       int nb = 0;
       if (u < na) {
         const int e = a.plan.active[u];
-        const int cnt = a.plan.offsets[e + 1] - a.plan.offsets[e];
+        const int beg = a.plan.offsets[e];
+        const int cnt = a.plan.offsets[e + 1] - beg;
+        sh.ex_id[u] = e;
+        sh.ex_beg[u] = beg;
+        sh.ex_cnt[u] = cnt;
         nb = (cnt + kNMax - 1) / kNMax;
       }
       int incl = nb;
@@ -236,15 +300,15 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   const uint32_t tmem = sh.tmem_base;
   const int num_units = sh.num_units;
   const int G = a.G, O = a.O;
+  const int nk = G / 2;                              // chunks of 64 = 2 groups
   bool ok = true;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ---------------------------------------- producer A: scales + weights
     if (lane == 0) {
-      const uint64_t pol_w = l2_evict_first_policy();   // weights: read once
-      const uint64_t pol_x = l2_evict_last_policy();    // tokens: reread per tile
-      int chunk = 0, it = 0;
-      const int nk = G / 2;                              // chunks of 64 = 2 groups
+      const uint64_t pol = l2_evict_first_policy();     // weights: read once
+      int it = 0, issued = 0;
+      RingPos pa;
       for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
         const Unit w = unit_at(a, sh, idx);
         if (w.ntok <= 0) { --it; continue; }
@@ -262,36 +326,69 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         if (copy) {
           mbar_arrive_expect_tx(&sh.s_full[sb], (uint32_t)(c_hi - c_lo));
           bulk_copy_g2s(scale_buf + (size_t)sb * a.scale_cap, reinterpret_cast<const void*>(c_lo),
-                        (uint32_t)(c_hi - c_lo), &sh.s_full[sb], pol_w);
+                        (uint32_t)(c_hi - c_lo), &sh.s_full[sb], pol);
         } else {
           mbar_arrive(&sh.s_full[sb]);
         }
-        const uint32_t tx = kStageA + (uint32_t)load_rows(w.load) * 128u;
-        for (int kc = 0; kc < nk; ++kc, ++chunk) {
-          const int st = chunk % a.stages;
-          if (!mbar_wait(&sh.empty[st], ((uint32_t)(chunk / a.stages) & 1u) ^ 1u)) {
+        for (int kc = 0; kc < nk; ++kc, ++issued) {
+          if (!mbar_wait(&sh.empty_a[pa.idx], pa.phase ^ 1u)) {
             ok = false;
             break;
           }
-          unsigned char* sp = stages + (size_t)st * kStageBytes;
-          mbar_arrive_expect_tx(&sh.full[st], tx);
-          tma_load_2d(sp + kStageB, &maps.a, kc * 32, (int)row0, &sh.full[st], pol_w);
-          tma_load_2d(sp, &maps.b[w.load], kc * kBK, w.tok0, &sh.full[st], pol_x);
+          mbar_arrive_expect_tx(&sh.full_a[pa.idx], kStageA);
+          tma_load_2d(ring_a + (size_t)pa.idx * kStageA, &maps.a, kc * 32, (int)row0,
+                      &sh.full_a[pa.idx], pol);
+          pa.next(a.stages_a);
         }
       }
       if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
-      // Wait (bounded) until the copies this thread issued have landed.
-      for (int k = max(0, chunk - a.stages); k < chunk; ++k)
-        if (!mbar_wait(&sh.full[k % a.stages], (uint32_t)(k / a.stages) & 1u)) break;
+      // Wait (bounded) until the copies this thread issued have landed: the
+      // last min(issued, stages) uses of the ring, walking back from pa.
+      for (int k = 0; k < min(issued, a.stages_a); ++k) {
+        int idx = pa.idx - 1 - k;
+        uint32_t ph = pa.phase;
+        if (idx < 0) { idx += a.stages_a; ph ^= 1u; }
+        if (!mbar_wait(&sh.full_a[idx], ph)) break;
+      }
       for (int k = max(0, it - 2); k < it; ++k)
         if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)(k >> 1) & 1u)) break;
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------ producer B: tokens
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_last_policy();      // tokens: reread per tile
+      int issued = 0;
+      RingPos pr;
+      for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x) {
+        const Unit w = unit_at(a, sh, idx);
+        if (w.ntok <= 0) continue;
+        const uint32_t tx = (uint32_t)load_rows(w.load) * 128u;
+        for (int kc = 0; kc < nk; ++kc, ++issued) {
+          if (!mbar_wait(&sh.done[pr.idx], pr.phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sh.full_b[pr.idx], tx);
+          tma_load_2d(ring_b + (size_t)pr.idx * kStageB, &maps.b[w.load], kc * kBK, w.tok0,
+                      &sh.full_b[pr.idx], pol);
+          pr.next(kRing);
+        }
+      }
+      if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+      for (int k = 0; k < min(issued, kRing); ++k) {
+        int idx = pr.idx - 1 - k;
+        uint32_t ph = pr.phase;
+        if (idx < 0) { idx += kRing; ph ^= 1u; }
+        if (!mbar_wait(&sh.full_b[idx], ph)) break;
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int chunk = 0, it = 0, ach = 0;
-      const int nk = G / 2;
+      int it = 0;
+      RingPos pr;
       for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
         const Unit w = unit_at(a, sh, idx);
         if (w.ntok <= 0) { --it; continue; }
@@ -300,23 +397,21 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         tc_fence_after_sync();
         const uint32_t idesc = mma_idesc(kBM, w.nmma);
         const uint32_t d_tmem = tmem + kDCol + (uint32_t)db * kNMax;
-        for (int kc = 0; kc < nk; ++kc, ++chunk, ++ach) {
-          const int st = chunk % a.stages;
-          const int ab = ach & 1;
-          if (!mbar_wait(&sh.full[st], (uint32_t)(chunk / a.stages) & 1u) ||
-              !mbar_wait(&sh.a_full[ab], (uint32_t)(ach >> 1) & 1u)) {
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&sh.full_b[pr.idx], pr.phase) ||
+              !mbar_wait(&sh.a_full[pr.idx], pr.phase)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t b_addr = smem_addr(stages + (size_t)st * kStageBytes);
-          const uint32_t a_tmem = tmem + kACol + (uint32_t)ab * 32;
+          const uint32_t b_addr = smem_addr(ring_b + (size_t)pr.idx * kStageB);
+          const uint32_t a_tmem = tmem + kACol + (uint32_t)pr.idx * 32;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             tc_mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
                       (kc > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&sh.a_empty[ab]);      // A buffer free once these MMAs finish
-          tc_commit(&sh.empty[st]);        // token tile consumed
+          tc_commit(&sh.done[pr.idx]);     // token stage and A buffer free once these finish
+          pr.next(kRing);
         }
         if (!ok) break;
         tc_commit(&sh.d_full[db]);         // accumulator complete
@@ -333,36 +428,25 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     const int h = (warp - kDequantWarp0) >> 2;       // group of the chunk
     const int m = 32 * q + lane;                     // weight row in the tile
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    int chunk = 0, it = 0, ach = 0;
-    const int nk = G / 2;
+    int it = 0;
+    RingPos pa, pr;
     for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
       const Unit w = unit_at(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int sb = it & 1;
       if (!mbar_wait(&sh.s_full[sb], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
       const int soff = sh.scale_off[sb];
-      const unsigned char* srow = scale_buf + (size_t)sb * a.scale_cap + (soff < 0 ? 0 : soff) +
-                                  (size_t)min(m, w.rows - 1) * G;
-      const uint8_t* grow = a.scales + ((size_t)w.e * O + w.m0 + min(m, w.rows - 1)) * G;
-      for (int kc = 0; kc < nk; ++kc, ++chunk, ++ach) {
-        const int st = chunk % a.stages;
-        const int ab = ach & 1;
-        if (!mbar_wait(&sh.full[st], (uint32_t)(chunk / a.stages) & 1u)) { ok = false; break; }
-        const unsigned char* sp = stages + (size_t)st * kStageBytes + kStageB;
-        const uint4 pk = *reinterpret_cast<const uint4*>(sp + m * 32 + h * 16);
-        const int g = 2 * kc + h;
-        const uint32_t sbyte = soff >= 0 ? (uint32_t)srow[g] : (uint32_t)__ldg(grow + g);
-        uint32_t v[16];
-        dequant_group_bf16(pk, sbyte, v);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.empty[st]);   // packed bytes consumed
-        if (!mbar_wait(&sh.a_empty[ab], ((uint32_t)(ach >> 1) & 1u) ^ 1u)) { ok = false; break; }
-        tc_fence_after_sync();
-        tmem_st16(tmem + lane_base + kACol + (uint32_t)ab * 32 + (uint32_t)h * 16, v);
-        tmem_wait_st();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.a_full[ab]);
+      // The choice of scale source is the same for the whole tile: take it
+      // once, so the chunk loop holds no global load.
+      if (soff >= 0) {
+        const unsigned char* srow =
+            scale_buf + (size_t)sb * a.scale_cap + soff + (size_t)min(m, w.rows - 1) * G;
+        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, m, h, lane, nk, pa, pr,
+                          [&](int g) { return (uint32_t)srow[g]; });
+      } else {
+        const uint8_t* grow = a.scales + ((size_t)w.e * O + w.m0 + min(m, w.rows - 1)) * G;
+        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, m, h, lane, nk, pa, pr,
+                          [&](int g) { return (uint32_t)__ldg(grow + g); });
       }
       if (!ok) break;
       __syncwarp();
@@ -384,16 +468,16 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const bool row_ok = m < w.rows;
       float* out_col = a.part + w.m0 + m;
       for (int c0 = 0; c0 < w.nmma; c0 += 16) {
+        // Pair ids of these 16 columns: one load per lane, then broadcast.
+        const int my_pair = (lane < 16 && c0 + lane < w.ntok)
+                                ? a.plan.pair_list[w.tok0 + c0 + lane] : 0;
         uint32_t v[16];
         tmem_ld16(tmem + lane_base + kDCol + (uint32_t)db * kNMax + (uint32_t)c0, v);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int n = c0 + i;
-          if (row_ok && n < w.ntok) {
-            const int pair = a.plan.pair_list[w.tok0 + n];
-            out_col[(size_t)pair * O] = __uint_as_float(v[i]);
-          }
+          const int pair = __shfl_sync(kFullMask, my_pair, i);
+          if (row_ok && c0 + i < w.ntok) out_col[(size_t)pair * O] = __uint_as_float(v[i]);
         }
       }
       tc_fence_before_sync();
@@ -455,19 +539,30 @@ int num_sms_tc() {
   return cached[dev];
 }
 
-size_t tc_shared_bytes(int stages, uint32_t scale_cap, int64_t E) {
-  return 1024 + (size_t)stages * kStageBytes + 2 * (size_t)scale_cap + sizeof(TcShared) +
-         (size_t)(E + 1) * sizeof(int);
+size_t tc_shared_bytes(int stages_a, uint32_t scale_cap) {
+  return 1024 + (size_t)kRing * kStageB + (size_t)stages_a * kStageA + 2 * (size_t)scale_cap +
+         sizeof(TcShared);
 }
 
+constexpr size_t kSmemLimit = 227 * 1024;
+
 }  // namespace
+
+cudaError_t launch_gather_tokens(const void* x, const RoutePlan& plan, void* grouped,
+                                 int64_t T, int64_t I, int64_t K, cudaStream_t stream) {
+  const int64_t P = T * K;
+  const int64_t blocks = std::min<int64_t>((P + 7) / 8, (int64_t)num_sms_tc() * 8);
+  return launch_after_previous(gather_tokens_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)),
+                               dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x),
+                               static_cast<__nv_bfloat16*>(grouped), plan, (int)I, (int)K);
+}
 
 bool gemm_tc_supported(int64_t E, int64_t I, int64_t O) {
   const int64_t G = I / 32;
   if (G % 2 != 0) return false;                    // K chunks of 64
-  if (E > 4096 || E * O > 0x7fffffff) return false;
+  if (E > kMaxExpertsTc || E * O > 0x7fffffff) return false;
   const uint32_t scale_cap = (uint32_t)((kBM * G + 31) / 16 * 16);
-  return tc_shared_bytes(3, scale_cap, E) <= 227 * 1024;
+  return tc_shared_bytes(4, scale_cap) <= kSmemLimit;
 }
 
 size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I) {
@@ -482,17 +577,8 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
 
-  // 1. tokens grouped by expert
-  {
-    const int64_t blocks = std::min<int64_t>((P + 7) / 8, (int64_t)num_sms_tc() * 8);
-    cudaError_t err = launch_after_previous(
-        gather_tokens_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), 0, stream,
-        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(grouped), plan, (int)I,
-        (int)K);
-    if (err != cudaSuccess) return err;
-  }
-
-  // 2. tensor maps
+  (void)x;
+  // Tensor maps.
   TcMaps maps;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)(G * 16), (cuuint64_t)(E * O)};
@@ -515,7 +601,6 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
       return cudaErrorInvalidValue;
   }
 
-  // 3. the GEMM
   TcArgs args;
   args.plan = plan;
   args.scales = scales;
@@ -527,10 +612,11 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
   args.K = (int)K;
   args.mtiles = (int)((O + kBM - 1) / kBM);
   args.scale_cap = (uint32_t)((kBM * G + 31) / 16 * 16);
-  int stages = kStagesMax;
-  while (stages > 2 && tc_shared_bytes(stages, args.scale_cap, E) > 227 * 1024) --stages;
-  args.stages = stages;
-  const size_t smem = tc_shared_bytes(stages, args.scale_cap, E);
+  // As deep a packed-weight ring (HBM latency) as shared memory allows.
+  int sa = kStagesAMax;
+  while (sa > 4 && tc_shared_bytes(sa, args.scale_cap) > kSmemLimit) --sa;
+  args.stages_a = sa;
+  const size_t smem = tc_shared_bytes(sa, args.scale_cap);
   static std::mutex mu;
   static size_t opted[64] = {};
   int dev = 0;

@@ -97,6 +97,8 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16,
 // Prefill-regime grouped GEMM on the tensor cores (bf16 tokens).
 bool gemm_tc_supported(int64_t E, int64_t I, int64_t O);
 size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I);
+cudaError_t launch_gather_tokens(const void* x, const RoutePlan& plan, void* grouped,
+                                 int64_t T, int64_t I, int64_t K, cudaStream_t stream);
 cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* scales,
                            const RoutePlan& plan, void* grouped, float* part,
                            unsigned long long* status, int64_t T, int64_t E, int64_t I,
