@@ -18,16 +18,18 @@
 //     swizzle that the K-major shared-memory descriptor describes.
 //   * tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), accumulator in TMEM.
 //
-// Warp roles in a CTA of 16 warps (one CTA per SM, persistent over units
+// Warp roles in a CTA of 24 warps (one CTA per SM, persistent over units
 // (expert, token block, 128-row tile)):
 //   warp 0      producer of scales and packed weights (lane 0; a deep ring
 //               of 4 KB stages covers HBM latency) and TMEM allocation
-//   warp 1      MMA issuer (lane 0)
+//   warp 1      MMA issuer (the whole warp waits, one elected lane issues)
 //   warp 2      per-expert lists in shared memory at start
 //   warp 3      producer of token tiles (lane 0)
-//   warps 4-11  dequantize: thread (row m, half h) decodes group 2kc+h of
-//               row m into 16 TMEM columns
-//   warps 12-15 epilogue: TMEM -> registers -> float32 partial results
+//   warps 4-19  dequantize, in two teams of 8 warps that take alternate
+//               chunks, so one team decodes while the other waits; in a team
+//               thread (row m, half h) decodes group 2kc+h of row m into 16
+//               TMEM columns
+//   warps 20-23 epilogue: TMEM -> registers -> float32 partial results
 // Four A buffers and two accumulators in TMEM let dequantize, MMA and the
 // epilogue of consecutive chunks and units overlap. Every wait is bounded;
 // a role whose wait gives up records it, stops, and the CTA still waits
@@ -43,7 +45,7 @@
 namespace mxfp4el {
 namespace {
 
-constexpr int kTcThreads = 512;
+constexpr int kTcThreads = 768;
 constexpr int kBM = 128;                    // weight rows per tile
 constexpr int kBK = 64;                     // K elements per stage
 constexpr int kNMax = 192;                  // tokens per block
@@ -57,7 +59,7 @@ constexpr uint32_t kDCol = 0;               // two accumulators of kNMax columns
 constexpr uint32_t kACol = 2 * kNMax;       // kRing A buffers of 32 columns
 static_assert(kACol + kRing * 32 <= kTmemCols, "TMEM budget");
 constexpr int kMaxExpertsTc = 1024;         // per-expert lists kept in shared memory
-constexpr int kDequantWarp0 = 4, kDequantWarps = 8, kEpiWarp0 = 12;
+constexpr int kDequantWarp0 = 4, kDequantWarps = 16, kTeamWarps = 8, kEpiWarp0 = 20;
 constexpr int kNumLoads = 5;                // token-box heights
 __host__ __device__ constexpr int load_rows(int l) {
   return l == 0 ? 16 : l == 1 ? 32 : l == 2 ? 64 : l == 3 ? 128 : 192;
@@ -172,41 +174,108 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
          | ((uint64_t)2 << 61);               // layout: 128-byte swizzle
 }
 
-// 16 packed bytes (32 codes) and their scale byte -> 16 bf16x2 words, the
-// values LUT[code] * 2^(s - 127) (low nibble in the low half). The E2M1
-// value is widened to float32 and multiplied by the two exact factors of
-// e8m0_split, so the product is exact for every byte s; converting it to
-// bf16 is exact whenever the value is a bf16 number (s = 2..253 always).
-__device__ __forceinline__ void dequant_group_bf16(const uint4& q, uint32_t s, uint32_t (&w)[16]) {
-  const float2 f = e8m0_split(s);
-  const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t h[4];
-    e2m1x8_to_f16x2x4(words[k], h);
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float2 v = fmul2(fmul2(f16x2_to_f32x2(h[b]), make_float2(f.x, f.x)),
-                             make_float2(f.y, f.y));
-      const __nv_bfloat162 r = __floats2bfloat162_rn(v.x, v.y);
-      w[4 * k + b] = *reinterpret_cast<const uint32_t*>(&r);
-    }
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// The bf16 bit patterns of the eight magnitudes LUT[j] * 2^(s - 127),
+// j = 0..7 (0, 0.5, 1, 1.5, 2, 3, 4, 6), as byte tables for prmt: h0/h1 hold
+// the high bytes of j = 0..3 / 4..7, l0/l1 the low bytes.
+struct MagnitudeTable {
+  uint32_t h0, h1, l0, l1;
+};
+
+__device__ __forceinline__ MagnitudeTable magnitude_table(uint32_t s) {
+  uint32_t v01, v23, v45, v67;   // (v_j | v_{j+1} << 16)
+  if (s - 2u <= 250u) {
+    // 2 <= s <= 252: every nonzero magnitude times 2^(s - 127) is a normal
+    // bf16 with exponent field s - 1, s, s, s + 1, s + 1, s + 2, s + 2 and
+    // mantissa 0 or 0x40 (the factor 1.5).
+    const uint32_t t = s * 0x00800080u;            // s << 7 in both halves
+    v01 = (s - 1u) << 23;                          // 0 | 0.5
+    v23 = t + 0x00400000u;                         // 1 | 1.5
+    v45 = t + 0x00C00080u;                         // 2 | 3
+    v67 = t + 0x01400100u;                         // 4 | 6
+  } else {
+    // Subnormal or overflowing results: the exact float32 product (the two
+    // factors of e8m0_split are finite for every byte), rounded to bf16.
+    const float2 f = e8m0_split(s);
+    auto bits = [&](float m) {
+      return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((m * f.x) * f.y));
+    };
+    v01 = bits(0.5f) << 16;
+    v23 = bits(1.0f) | (bits(1.5f) << 16);
+    v45 = bits(2.0f) | (bits(3.0f) << 16);
+    v67 = bits(4.0f) | (bits(6.0f) << 16);
   }
+  return {prmt(v01, v23, 0x7531u), prmt(v45, v67, 0x7531u), prmt(v01, v23, 0x6420u),
+          prmt(v45, v67, 0x6420u)};
+}
+
+// Eight E2M1 codes (one packed word, low nibble first) -> four bf16x2 words,
+// w[i] = (value of code 2i, value of code 2i+1). The low three bits of each
+// code index the tables; prmt's sign-replicate selectors turn the code's
+// sign bit into a byte of all ones, whose top bit becomes the bf16 sign.
+__device__ __forceinline__ void decode_word(uint32_t q, const MagnitudeTable& t, uint32_t* w) {
+  const uint32_t sel_lo = q & 0x77777777u, sel_hi = sel_lo >> 16;
+  const uint32_t y = q << 4;     // byte k of y: sign of code 2k in bit 7; of q: code 2k+1
+  const uint32_t h03 = prmt(t.h0, t.h1, sel_lo) | (prmt(y, q, 0xD9C8u) & 0x80808080u);
+  const uint32_t h47 = prmt(t.h0, t.h1, sel_hi) | (prmt(y, q, 0xFBEAu) & 0x80808080u);
+  const uint32_t l03 = prmt(t.l0, t.l1, sel_lo), l47 = prmt(t.l0, t.l1, sel_hi);
+  w[0] = prmt(l03, h03, 0x5140u);
+  w[1] = prmt(l03, h03, 0x7362u);
+  w[2] = prmt(l47, h47, 0x5140u);
+  w[3] = prmt(l47, h47, 0x7362u);
+}
+
+// 16 packed bytes (32 codes) of one group and its scale byte -> 16 bf16x2
+// words, exactly LUT[code] * 2^(s - 127) wherever that is a bf16 number.
+__device__ __forceinline__ void dequant_group_bf16(const uint4& q, uint32_t s, uint32_t (&w)[16]) {
+  const MagnitudeTable t = magnitude_table(s);
+  decode_word(q.x, t, w);
+  decode_word(q.y, t, w + 4);
+  decode_word(q.z, t, w + 8);
+  decode_word(q.w, t, w + 12);
+}
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " .reg .b32 r;\n"
+      " elect.sync r|p, 0xffffffff;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}"
+      : "=r"(e));
+  return e != 0;
 }
 
 // The dequantizer's chunk loop for one tile: thread (row m, half h) decodes
-// group 2kc+h of its row for kc = 0..nk-1 into A buffer r of the chunk ring.
-// scale(g) returns the row's scale byte of group g. Returns false if a wait
-// gave up.
+// group 2kc+h of its row into A buffer r of the chunk ring, for the chunks
+// of its team (`mine` tells whether the next chunk is the team's; it flips
+// every chunk). The packed tile arrives with the 32-byte swizzle: the two
+// 16-byte halves of row m are exchanged when bit 2 of m is set, so eight
+// consecutive rows read eight different bank groups. scale(g) returns the
+// row's scale byte of group g. Returns false if a wait gave up.
 template <typename ScaleFn>
 __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* ring_a,
                                              int stages_a, uint32_t tmem, uint32_t lane_base,
-                                             int m, int h, int lane, int nk, RingPos& pa,
-                                             RingPos& pr, ScaleFn scale) {
+                                             int m, int h, int lane, int nk, bool& mine,
+                                             RingPos& pa, RingPos& pr, ScaleFn scale) {
+  const uint32_t a_off = (uint32_t)m * 32u + (uint32_t)((h ^ (m >> 2)) & 1) * 16u;
   for (int kc = 0; kc < nk; ++kc) {
+    if (!mine) {               // the other team's chunk
+      mine = true;
+      pa.next(stages_a);
+      pr.next(kRing);
+      continue;
+    }
+    mine = false;
     if (!mbar_wait(&sh.full_a[pa.idx], pa.phase)) return false;
-    const uint4 pk =
-        *reinterpret_cast<const uint4*>(ring_a + (size_t)pa.idx * kStageA + m * 32 + h * 16);
+    const uint4 pk = *reinterpret_cast<const uint4*>(ring_a + (size_t)pa.idx * kStageA + a_off);
     const uint32_t sbyte = scale(2 * kc + h);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty_a[pa.idx]);     // packed bytes consumed
@@ -241,11 +310,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages_a; ++s) {
       mbar_init(&sh.full_a[s], 1);
-      mbar_init(&sh.empty_a[s], kDequantWarps);
+      mbar_init(&sh.empty_a[s], kTeamWarps);
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&sh.full_b[r], 1);
-      mbar_init(&sh.a_full[r], kDequantWarps);
+      mbar_init(&sh.a_full[r], kTeamWarps);
       mbar_init(&sh.done[r], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -386,48 +455,54 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int it = 0;
-      RingPos pr;
-      for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
-        const Unit w = unit_at(a, sh, idx);
-        if (w.ntok <= 0) { --it; continue; }
-        const int db = it & 1;
-        if (!mbar_wait(&sh.d_empty[db], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
+    // The whole warp runs the loop and waits; one elected lane (always the
+    // same one, so its commits track its own MMAs) issues.
+    int it = 0;
+    RingPos pr;
+    for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
+      const Unit w = unit_at(a, sh, idx);
+      if (w.ntok <= 0) { --it; continue; }
+      const int db = it & 1;
+      if (!mbar_wait(&sh.d_empty[db], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
+      tc_fence_after_sync();
+      const uint32_t idesc = mma_idesc(kBM, w.nmma);
+      const uint32_t d_tmem = tmem + kDCol + (uint32_t)db * kNMax;
+      for (int kc = 0; kc < nk; ++kc) {
+        if (!mbar_wait(&sh.full_b[pr.idx], pr.phase) ||
+            !mbar_wait(&sh.a_full[pr.idx], pr.phase)) {
+          ok = false;
+          break;
+        }
         tc_fence_after_sync();
-        const uint32_t idesc = mma_idesc(kBM, w.nmma);
-        const uint32_t d_tmem = tmem + kDCol + (uint32_t)db * kNMax;
-        for (int kc = 0; kc < nk; ++kc) {
-          if (!mbar_wait(&sh.full_b[pr.idx], pr.phase) ||
-              !mbar_wait(&sh.a_full[pr.idx], pr.phase)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t b_addr = smem_addr(ring_b + (size_t)pr.idx * kStageB);
-          const uint32_t a_tmem = tmem + kACol + (uint32_t)pr.idx * 32;
+        const uint32_t b_addr = smem_addr(ring_b + (size_t)pr.idx * kStageB);
+        const uint32_t a_tmem = tmem + kACol + (uint32_t)pr.idx * 32;
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             tc_mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
                       (kc > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&sh.done[pr.idx]);     // token stage and A buffer free once these finish
-          pr.next(kRing);
         }
-        if (!ok) break;
-        tc_commit(&sh.d_full[db]);         // accumulator complete
+        __syncwarp();
+        pr.next(kRing);
       }
-      if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
-      // Do not free TMEM under running MMAs: wait (bounded) for all of them.
-      tc_commit(&sh.drain);
-      mbar_wait(&sh.drain, 0);
+      if (!ok) break;
+      if (elect_one()) tc_commit(&sh.d_full[db]);   // accumulator complete
+      __syncwarp();
     }
+    if (!ok && lane == 0) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+    // Do not free TMEM under running MMAs: wait (bounded) for all of them.
+    if (elect_one()) tc_commit(&sh.drain);
     __syncwarp();
+    mbar_wait(&sh.drain, 0);
   } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + kDequantWarps) {
     // -------------------------------------------------------- dequantizers
+    const int dw = warp - kDequantWarp0;
     const int q = warp & 3;                          // TMEM lane quarter
-    const int h = (warp - kDequantWarp0) >> 2;       // group of the chunk
+    const int h = (dw >> 2) & 1;                     // group of the chunk
     const int m = 32 * q + lane;                     // weight row in the tile
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    bool mine = dw < kTeamWarps;                     // team 0 takes the first chunk
     int it = 0;
     RingPos pa, pr;
     for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
@@ -441,11 +516,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       if (soff >= 0) {
         const unsigned char* srow =
             scale_buf + (size_t)sb * a.scale_cap + soff + (size_t)min(m, w.rows - 1) * G;
-        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, m, h, lane, nk, pa, pr,
+        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, m, h, lane, nk, mine, pa, pr,
                           [&](int g) { return (uint32_t)srow[g]; });
       } else {
         const uint8_t* grow = a.scales + ((size_t)w.e * O + w.m0 + min(m, w.rows - 1)) * G;
-        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, m, h, lane, nk, pa, pr,
+        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, m, h, lane, nk, mine, pa, pr,
                           [&](int g) { return (uint32_t)__ldg(grow + g); });
       }
       if (!ok) break;
@@ -586,7 +661,7 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
     const cuuint32_t box[2] = {32, (cuuint32_t)kBM};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
