@@ -25,10 +25,10 @@
 //   warp 1      MMA issuer (the whole warp waits, one elected lane issues)
 //   warp 2      per-expert lists in shared memory at start
 //   warp 3      producer of token tiles (lane 0)
-//   warps 4-19  dequantize, in two teams of 8 warps that take alternate
-//               chunks, so one team decodes while the other waits; in a team
-//               thread (row m, half h) decodes group 2kc+h of row m into 16
-//               TMEM columns
+//   warps 4-19  dequantize, in four teams of 4 warps: team t owns A buffer t
+//               and takes chunks t, t+4, t+8, ..., so the teams' decode,
+//               waits and stores interleave; in a team thread m (one weight
+//               row) decodes both groups of the chunk into 32 TMEM columns
 //   warps 20-23 epilogue: TMEM -> registers -> float32 partial results
 // Four A buffers and two accumulators in TMEM let dequantize, MMA and the
 // epilogue of consecutive chunks and units overlap. Every wait is bounded;
@@ -59,7 +59,8 @@ constexpr uint32_t kDCol = 0;               // two accumulators of kNMax columns
 constexpr uint32_t kACol = 2 * kNMax;       // kRing A buffers of 32 columns
 static_assert(kACol + kRing * 32 <= kTmemCols, "TMEM budget");
 constexpr int kMaxExpertsTc = 1024;         // per-expert lists kept in shared memory
-constexpr int kDequantWarp0 = 4, kDequantWarps = 16, kTeamWarps = 8, kEpiWarp0 = 20;
+constexpr int kDequantWarp0 = 4, kDequantWarps = 16, kTeamWarps = 4, kEpiWarp0 = 20;
+static_assert(kDequantWarps == kRing * kTeamWarps, "one team per A buffer");
 constexpr int kNumLoads = 5;                // token-box heights
 __host__ __device__ constexpr int load_rows(int l) {
   return l == 0 ? 16 : l == 1 ? 32 : l == 2 ? 64 : l == 3 ? 128 : 192;
@@ -253,43 +254,58 @@ __device__ __forceinline__ bool elect_one() {
   return e != 0;
 }
 
-// The dequantizer's chunk loop for one tile: thread (row m, half h) decodes
-// group 2kc+h of its row into A buffer r of the chunk ring, for the chunks
-// of its team (`mine` tells whether the next chunk is the team's; it flips
-// every chunk). The packed tile arrives with the 32-byte swizzle: the two
-// 16-byte halves of row m are exchanged when bit 2 of m is set, so eight
-// consecutive rows read eight different bank groups. scale(g) returns the
-// row's scale byte of group g. Returns false if a wait gave up.
+// A dequantizer team's place in the chunk sequence of its CTA: the global
+// index of its next chunk (chunks of earlier tiles included), that chunk's
+// packed stage and phase, and the use parity of the team's A buffer.
+struct TeamPos {
+  int next;
+  int stage;
+  uint32_t stage_phase;
+  uint32_t buf_phase;
+};
+
+// The dequantizer's chunk loop for one tile whose chunks have global indices
+// base .. base+nk-1: thread m of team t decodes groups 2kc and 2kc+1 of row
+// m into A buffer t for each of the team's chunks kc. The packed tile
+// arrives with the 32-byte swizzle: the two 16-byte halves of row m are
+// exchanged when bit 2 of m is set, so eight consecutive rows read eight
+// different bank groups. scale(g) returns the row's scale byte of group g.
+// Returns false if a wait gave up.
 template <typename ScaleFn>
 __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* ring_a,
                                              int stages_a, uint32_t tmem, uint32_t lane_base,
-                                             int m, int h, int lane, int nk, bool& mine,
-                                             RingPos& pa, RingPos& pr, ScaleFn scale) {
-  const uint32_t a_off = (uint32_t)m * 32u + (uint32_t)((h ^ (m >> 2)) & 1) * 16u;
-  for (int kc = 0; kc < nk; ++kc) {
-    if (!mine) {               // the other team's chunk
-      mine = true;
-      pa.next(stages_a);
-      pr.next(kRing);
-      continue;
-    }
-    mine = false;
-    if (!mbar_wait(&sh.full_a[pa.idx], pa.phase)) return false;
-    const uint4 pk = *reinterpret_cast<const uint4*>(ring_a + (size_t)pa.idx * kStageA + a_off);
-    const uint32_t sbyte = scale(2 * kc + h);
+                                             int team, int m, int lane, int base, int nk,
+                                             TeamPos& tp, ScaleFn scale) {
+  const uint32_t sw = (uint32_t)(m >> 2) & 1u;
+  const uint32_t off0 = (uint32_t)m * 32u + sw * 16u, off1 = (uint32_t)m * 32u + (sw ^ 1u) * 16u;
+  const uint32_t a_col = tmem + lane_base + kACol + (uint32_t)team * 32;
+  for (; tp.next < base + nk; tp.next += kRing) {
+    const int kc = tp.next - base;
+    if (!mbar_wait(&sh.full_a[tp.stage], tp.stage_phase)) return false;
+    const unsigned char* stage = ring_a + (size_t)tp.stage * kStageA;
+    const uint4 pk0 = *reinterpret_cast<const uint4*>(stage + off0);
+    const uint4 pk1 = *reinterpret_cast<const uint4*>(stage + off1);
+    const uint32_t s0 = scale(2 * kc), s1 = scale(2 * kc + 1);
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.empty_a[pa.idx]);     // packed bytes consumed
-    pa.next(stages_a);
-    uint32_t v[16];
-    dequant_group_bf16(pk, sbyte, v);
-    if (!mbar_wait(&sh.done[pr.idx], pr.phase ^ 1u)) return false;   // buffer free
+    if (lane == 0) mbar_arrive(&sh.empty_a[tp.stage]);   // packed bytes consumed
+    tp.stage += kRing;                                    // stages_a is a multiple of kRing
+    if (tp.stage >= stages_a) {
+      tp.stage -= stages_a;
+      tp.stage_phase ^= 1u;
+    }
+    uint32_t v0[16], v1[16];
+    dequant_group_bf16(pk0, s0, v0);
+    dequant_group_bf16(pk1, s1, v1);
+    // The buffer is free once the MMAs of this team's previous chunk finished.
+    if (!mbar_wait(&sh.done[team], tp.buf_phase ^ 1u)) return false;
     tc_fence_after_sync();
-    tmem_st16(tmem + lane_base + kACol + (uint32_t)pr.idx * 32 + (uint32_t)h * 16, v);
+    tmem_st16(a_col, v0);
+    tmem_st16(a_col + 16, v1);
     tmem_wait_st();
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.a_full[pr.idx]);
-    pr.next(kRing);
+    if (lane == 0) mbar_arrive(&sh.a_full[team]);
+    tp.buf_phase ^= 1u;
   }
   return true;
 }
@@ -497,14 +513,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     mbar_wait(&sh.drain, 0);
   } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + kDequantWarps) {
     // -------------------------------------------------------- dequantizers
-    const int dw = warp - kDequantWarp0;
+    const int team = (warp - kDequantWarp0) / kTeamWarps;
     const int q = warp & 3;                          // TMEM lane quarter
-    const int h = (dw >> 2) & 1;                     // group of the chunk
     const int m = 32 * q + lane;                     // weight row in the tile
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    bool mine = dw < kTeamWarps;                     // team 0 takes the first chunk
-    int it = 0;
-    RingPos pa, pr;
+    TeamPos tp{team, team, 0u, 0u};                  // chunk `team` is the team's first
+    int it = 0, base = 0;
     for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
       const Unit w = unit_at(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
@@ -516,13 +530,14 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       if (soff >= 0) {
         const unsigned char* srow =
             scale_buf + (size_t)sb * a.scale_cap + soff + (size_t)min(m, w.rows - 1) * G;
-        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, m, h, lane, nk, mine, pa, pr,
+        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk, tp,
                           [&](int g) { return (uint32_t)srow[g]; });
       } else {
         const uint8_t* grow = a.scales + ((size_t)w.e * O + w.m0 + min(m, w.rows - 1)) * G;
-        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, m, h, lane, nk, mine, pa, pr,
+        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk, tp,
                           [&](int g) { return (uint32_t)__ldg(grow + g); });
       }
+      base += nk;
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
@@ -687,9 +702,10 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
   args.K = (int)K;
   args.mtiles = (int)((O + kBM - 1) / kBM);
   args.scale_cap = (uint32_t)((kBM * G + 31) / 16 * 16);
-  // As deep a packed-weight ring (HBM latency) as shared memory allows.
+  // As deep a packed-weight ring (HBM latency) as shared memory allows, a
+  // multiple of kRing so that each dequantizer team keeps to its own stages.
   int sa = kStagesAMax;
-  while (sa > 4 && tc_shared_bytes(sa, args.scale_cap) > kSmemLimit) --sa;
+  while (sa > kRing && tc_shared_bytes(sa, args.scale_cap) > kSmemLimit) sa -= kRing;
   args.stages_a = sa;
   const size_t smem = tc_shared_bytes(sa, args.scale_cap);
   static std::mutex mu;
