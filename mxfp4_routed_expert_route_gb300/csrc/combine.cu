@@ -10,7 +10,11 @@
 // routed contributions.) The sum runs in float32 in slot order k = 0..K-1 and
 // is rounded once to the token dtype, so the result does not depend on which
 // kernel or which CTA produced each part. Pairs whose expert id is outside
-// [0, E) contribute nothing. The kernel is a grid-stride elementwise pass.
+// [0, E) contribute nothing. combine_vec_kernel gives each warp a segment of
+// 128 outputs of one token, four per lane with 16-byte loads of the
+// partial results; combine_kernel, a grid-stride elementwise pass, serves
+// widths that are not a multiple of 4 and unaligned buffers. Both evaluate
+// the same expression in the same order.
 #include "common.cuh"
 #include "internal.h"
 
@@ -43,12 +47,86 @@ combine_kernel(const Tok* __restrict__ ys, const Idx* __restrict__ sel,
   }
 }
 
+// Four consecutive token values as float32, and back (rounded once).
+__device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
+  const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+  x[0] = __uint_as_float(v.x << 16);
+  x[1] = __uint_as_float(v.x & 0xffff0000u);
+  x[2] = __uint_as_float(v.y << 16);
+  x[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+__device__ __forceinline__ void store4(float* p, const float (&x)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&x)[4]) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
+  uint2 v;
+  v.x = *reinterpret_cast<const uint32_t*>(&a);
+  v.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = v;
+}
+
+constexpr int kVecLanes = 32;   // one warp per segment of 4 * 32 outputs
+
+template <typename Tok, typename Idx>
+__global__ void __launch_bounds__(256)
+combine_vec_kernel(const Tok* __restrict__ ys, const Idx* __restrict__ sel,
+                   const float* __restrict__ p, const float* __restrict__ part, int ncol,
+                   Tok* __restrict__ out, int64_t T, int64_t O, int K, int64_t E) {
+  pdl_wait();                  // the linear kernel's partial results are complete
+  const int64_t nv = O / 4;                         // 4-wide vectors per token row
+  const int64_t segs = (nv + kVecLanes - 1) / kVecLanes;
+  const int64_t tasks = T * segs;
+  const int warps = blockDim.x / 32, lane = threadIdx.x & 31;
+  for (int64_t task = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); task < tasks;
+       task += (int64_t)gridDim.x * warps) {
+    const int64_t t = task / segs;
+    const int64_t v = (task - t * segs) * kVecLanes + lane;
+    if (v >= nv) continue;
+    const int64_t o = 4 * v;
+    float acc[4];
+    load4(ys + t * O + o, acc);
+    for (int k = 0; k < K; ++k) {
+      const int64_t pk = t * K + k;
+      const long long e = (long long)sel[pk];
+      if (e >= 0 && e < E) {
+        const float* pp = part + pk * ncol * O + o;
+        float4 s = __ldcs(reinterpret_cast<const float4*>(pp));
+        for (int c = 1; c < ncol; ++c) {
+          const float4 u = __ldcs(reinterpret_cast<const float4*>(pp + (int64_t)c * O));
+          s.x += u.x; s.y += u.y; s.z += u.z; s.w += u.w;
+        }
+        const float w = p[pk];
+        acc[0] = fmaf(w, s.x, acc[0]);
+        acc[1] = fmaf(w, s.y, acc[1]);
+        acc[2] = fmaf(w, s.z, acc[2]);
+        acc[3] = fmaf(w, s.w, acc[3]);
+      }
+    }
+    store4(out + t * O + o, acc);
+  }
+}
+
 template <typename Tok, typename Idx>
 cudaError_t launch_typed(const Tok* ys, const Idx* sel, const float* p,
                          const float* part, int ncol, Tok* out, int64_t T, int64_t E,
                          int64_t O, int64_t K, cudaStream_t stream) {
   const int64_t n = T * O;
   if (n == 0) return cudaSuccess;
+  const uintptr_t tok_align = 4 * sizeof(Tok);
+  if (O % 4 == 0 && reinterpret_cast<uintptr_t>(ys) % tok_align == 0 &&
+      reinterpret_cast<uintptr_t>(out) % tok_align == 0 &&
+      reinterpret_cast<uintptr_t>(part) % 16 == 0) {
+    const int64_t tasks = T * ((O / 4 + kVecLanes - 1) / kVecLanes);
+    const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, 152 * 8);
+    return launch_after_previous(combine_vec_kernel<Tok, Idx>, dim3((unsigned)blocks), dim3(256),
+                                 0, stream, ys, sel, p, part, ncol, out, T, O, (int)K, E);
+  }
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 16);
   return launch_after_previous(combine_kernel<Tok, Idx>, dim3((unsigned)blocks), dim3(256), 0,
                                stream, ys, sel, p, part, ncol, out, T, O, (int)K, E);

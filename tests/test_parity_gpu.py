@@ -270,3 +270,19 @@ def test_no_kernel_wait_timed_out():
     wl = workloads.make(9, 10, 3, 288, 130, dtype=torch.bfloat16, seed=22)
     run_gpu(wl)
     assert wait_timeouts() == 0
+
+
+def test_combine_vector_and_scalar_paths_agree_bitwise():
+    # The combine has a 16-byte vector path (width a multiple of 4, aligned
+    # buffers) and an elementwise path. A shared-output view that starts one
+    # element into its storage is misaligned and takes the elementwise path;
+    # both evaluate the same expression in the same order.
+    wl = workloads.make(24, 6, 3, 256, 64, dtype=torch.bfloat16, seed=41)
+    d = wl.device_tensors("cuda")
+    a = mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"], d["y_shared"])
+    store = torch.empty(wl.T * wl.O + 1, dtype=torch.bfloat16, device="cuda")
+    ys_off = store[1:].view(wl.T, wl.O)
+    ys_off.copy_(d["y_shared"])
+    assert ys_off.data_ptr() % 16 != 0
+    b = mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"], ys_off)
+    assert torch.equal(a, b)
