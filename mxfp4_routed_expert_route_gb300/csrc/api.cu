@@ -118,8 +118,9 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
     const bool prep = !gemm && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
     const bool prep_in_route = prep && prep_fits_route(T, I);
     TokenPrep tp = {prep_in_route ? x : nullptr, ws.x16, ws.sigma, I};
+    const UnitSplit split = gemm ? UnitSplit{0, 0, 0} : gemv_unit_split(T, E, I, O, K);
     mark(MXFP4EL_STAGE_ROUTE, true, stream);
-    err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, tp, stream);
+    err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, tp, split, stream);
     if (err == cudaSuccess && prep && !prep_in_route)
       err = launch_prep_tokens(x, ws.x16, ws.sigma, T, I, stream);
     mark(MXFP4EL_STAGE_ROUTE, false, stream);
@@ -184,6 +185,8 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
   ws->x16 = prep ? reinterpret_cast<__half*>(take((size_t)T * I * sizeof(__half))) : nullptr;
   ws->sigma = prep ? reinterpret_cast<int*>(take((size_t)T * sizeof(int))) : nullptr;
   ws->grouped = gemm ? take(gemm_tc_grouped_bytes(T, K, I)) : nullptr;
+  ws->plan.unit_begin =
+      K > 0 && !gemm ? reinterpret_cast<int*>(take((kMaxSplitCtas + 1) * sizeof(int))) : nullptr;
   const size_t ncol = (size_t)linear_partial_columns(T, E, I, O, K, token_dtype);
   ws->part = reinterpret_cast<float*>(take((size_t)P * ncol * (size_t)O * sizeof(float)));
   ws->bytes = off;

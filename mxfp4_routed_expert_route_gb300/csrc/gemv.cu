@@ -276,11 +276,19 @@ gemv_stream_kernel(const StreamArgs a) {
 
   // Each CTA takes one contiguous range of units, so consecutive units are
   // consecutive row tiles of the same expert (and of consecutive memory).
+  // The bucketer balances the ranges by cost (an expert's units cost more
+  // the more tokens it has); without its table the ranges are equal.
   const int num_units = a.plan.meta[kMetaNumActive] * a.row_tiles;
-  const int per_cta = num_units / (int)gridDim.x;
-  const int extra = num_units - per_cta * (int)gridDim.x;
-  const int ubeg = (int)blockIdx.x * per_cta + min((int)blockIdx.x, extra);
-  const int uend = ubeg + per_cta + ((int)blockIdx.x < extra ? 1 : 0);
+  int ubeg, uend;
+  if (a.plan.unit_begin != nullptr) {
+    ubeg = min(a.plan.unit_begin[blockIdx.x], num_units);
+    uend = min(a.plan.unit_begin[blockIdx.x + 1], num_units);
+  } else {
+    const int per_cta = num_units / (int)gridDim.x;
+    const int extra = num_units - per_cta * (int)gridDim.x;
+    ubeg = (int)blockIdx.x * per_cta + min((int)blockIdx.x, extra);
+    uend = ubeg + per_cta + ((int)blockIdx.x < extra ? 1 : 0);
+  }
   const int G = a.G, O = a.O;
 
   if (warp == kConsumerWarps) {
@@ -479,6 +487,8 @@ int num_sms() {
   return cached[dev];
 }
 
+int64_t stream_grid(int64_t bound_units) { return std::min<int64_t>(num_sms(), bound_units); }
+
 template <typename Elem, int RWS>
 cudaError_t launch_stream(StreamArgs a, size_t smem, int64_t bound_units, cudaStream_t stream) {
   // Two tokens per pass for f16 operands; fp32 operands take twice the
@@ -498,7 +508,7 @@ cudaError_t launch_stream(StreamArgs a, size_t smem, int64_t bound_units, cudaSt
       opted[dev] = smem;
     }
   }
-  const int64_t grid = std::min<int64_t>(num_sms(), bound_units);
+  const int64_t grid = stream_grid(bound_units);
   if (grid <= 0) return cudaSuccess;
   return launch_after_previous(kern, dim3((unsigned)grid), dim3(kStreamThreads), smem, stream, a);
 }
@@ -544,7 +554,41 @@ StreamShape stream_shape(int64_t G) {
   return sh;
 }
 
+// Units of the staged kernel: active experts (at most min(E, T*K)) times
+// row tiles; the tile height follows from the stream shape.
+int64_t stream_row_tiles(const StreamShape& sh, int64_t O) {
+  const int64_t rows = (int64_t)sh.nsub * sh.rws;
+  return (O + rows - 1) / rows;
+}
+
 }  // namespace
+
+// Cost of a unit beyond its tokens, in token passes. Measured on GB300: a
+// unit's time grows in proportion to its expert's tokens (the decode and the
+// bulk copy hide behind the token passes), so the split weighs tokens alone.
+#ifndef MXFP4EL_GEMV_FIXED_COST
+#define MXFP4EL_GEMV_FIXED_COST 0
+#endif
+
+UnitSplit gemv_unit_split(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
+  UnitSplit sp{0, 0, 0};
+  const StreamShape sh = stream_shape(I / 32);
+  if (sh.rws == 0 || T * K == 0 || O == 0) return sp;
+  const int64_t rt = stream_row_tiles(sh, O);
+  const int64_t bound_units = std::min<int64_t>(E, T * K) * rt;
+  const int64_t ctas = stream_grid(bound_units);
+  const int64_t fixed = MXFP4EL_GEMV_FIXED_COST;
+  // The bucketer sums costs in int32 and multiplies them by rt * ctas in
+  // int64; beyond that the kernel keeps its even split.
+  const int64_t max_cost = std::min<int64_t>(E, T * K) * fixed + T * K;
+  if (ctas <= 0 || ctas > kMaxSplitCtas || bound_units > 0x7fffffff ||
+      max_cost >= ((int64_t)1 << 31) || rt * max_cost > ((int64_t)1 << 50))
+    return sp;
+  sp.ctas = (int)ctas;
+  sp.row_tiles = (int)rt;
+  sp.fixed_cost = (int)fixed;
+  return sp;
+}
 
 int gemv_partial_columns(int64_t I) {
   const StreamShape sh = stream_shape(I / 32);
@@ -590,7 +634,9 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
   a.ncol = sh.ncol;
   a.nsub = sh.nsub;
   a.rows_per_tile = sh.nsub * sh.rws;
-  a.row_tiles = (int)((O + a.rows_per_tile - 1) / a.rows_per_tile);
+  a.row_tiles = (int)stream_row_tiles(sh, O);
+  // The bucketer wrote plan.unit_begin only if it was asked for a split.
+  if (gemv_unit_split(T, E, I, O, K).ctas == 0) a.plan.unit_begin = nullptr;
   a.packed_stage_bytes = (uint32_t)((size_t)a.rows_per_tile * G * 16);
   a.stage_bytes = (uint32_t)((stage_bytes_for(a.rows_per_tile, G) + 127) / 128 * 128);
   a.stages = (int)std::min<size_t>(kMaxStages, kSmemBudget / a.stage_bytes);

@@ -35,6 +35,21 @@ struct RoutePlan {
   int* offsets;     // [E + 1] start of each expert's segment in pair_list
   int* active;      // [E]     ascending ids of experts with count > 0
   int* pair_list;   // [T*K]   pair ids t*K + k grouped by expert, stable
+  int* unit_begin;  // [kMaxSplitCtas + 1] first GEMV unit of each CTA, when
+                    // the bucketer was asked for a cost-balanced split
+};
+
+// Cost-balanced split of the staged GEMV's units (active expert, row tile)
+// over its CTAs, computed by the bucketer: unit (u, tile) costs
+// fixed_cost + (tokens of expert u), CTA b starts at the first unit whose
+// cost prefix reaches b/ctas of the total. With equal unit counts per CTA,
+// the CTAs that drew experts with several tokens finished last and the
+// others idled. ctas == 0: no split.
+constexpr int kMaxSplitCtas = 1024;
+struct UnitSplit {
+  int ctas;
+  int row_tiles;
+  int fixed_cost;
 };
 
 // Workspace layout for one call.
@@ -66,11 +81,12 @@ struct TokenPrep {
   int64_t I;
 };
 
-// Bucketer; also prepares the tokens in the same launch when `prep.x` is set.
+// Bucketer; also prepares the tokens in the same launch when `prep.x` is
+// set, and writes plan.unit_begin when `split.ctas` > 0.
 cudaError_t launch_route(const void* sel, int index_dtype, int64_t T,
                          int64_t K, int64_t E, int* wc_global,
                          const RoutePlan& plan, const TokenPrep& prep,
-                         cudaStream_t stream);
+                         const UnitSplit& split, cudaStream_t stream);
 
 // True when token prep for these sizes fits in the bucketer's launch.
 bool prep_fits_route(int64_t T, int64_t I);
@@ -79,6 +95,10 @@ bool prep_fits_route(int64_t T, int64_t I);
 // True when the rows of width I fit the staged (bulk-copy) GEMV; bf16
 // tokens then need launch_prep_tokens first.
 bool gemv_uses_stream(int64_t I);
+
+// The split the staged GEMV wants for these sizes (ctas == 0: none, the
+// kernel then splits its units evenly).
+UnitSplit gemv_unit_split(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K);
 
 // Partial results per (pair, output row) that the GEMV writes for width I:
 // one per group column of the staged kernel, 1 for the direct kernel. The

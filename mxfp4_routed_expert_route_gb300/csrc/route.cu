@@ -60,7 +60,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int* t
 template <typename Idx>
 __global__ void __launch_bounds__(kRouteThreads, 1)
 route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
-             RoutePlan plan, int T, TokenPrep prep) {
+             RoutePlan plan, int T, TokenPrep prep, UnitSplit split) {
   pdl_launch_dependents();
   extern __shared__ int smem_wc[];
   __shared__ int warp_buf[33];
@@ -104,6 +104,7 @@ route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
   int total_pairs, total_active;
   int off = block_exclusive_scan(my_pairs, warp_buf, &total_pairs);
   int act = block_exclusive_scan(my_active, warp_buf, &total_active);
+  const int act0 = act;
   for (int e = e0; e < e1; ++e) {
     const int c = plan.counts[e];
     plan.offsets[e] = off;
@@ -120,6 +121,41 @@ route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
     plan.offsets[E] = total_pairs;
     plan.meta[kMetaNumActive] = total_active;
     plan.meta[kMetaNumPairs] = total_pairs;
+  }
+
+  // B'. Cost-balanced GEMV split: the active experts of this thread are the
+  // consecutive active slots act0, act0+1, ...; their cost prefix comes from
+  // one more scan. Every CTA boundary b < ctas lies in exactly one expert's
+  // cost interval, and that expert's thread writes it.
+  if (split.ctas > 0) {
+    int my_cost = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int c = plan.counts[e];
+      if (c > 0) my_cost += split.fixed_cost + c;
+    }
+    int total_cost;
+    int cost = block_exclusive_scan(my_cost, warp_buf, &total_cost);
+    const int64_t rt = split.row_tiles, n = split.ctas;
+    const int64_t C = rt * (int64_t)total_cost;        // total cost of all units
+    if (C == 0) {
+      for (int b = threadIdx.x; b <= split.ctas; b += kRouteThreads) plan.unit_begin[b] = 0;
+    } else {
+      int slot = act0;
+      for (int e = e0; e < e1; ++e) {
+        const int c = plan.counts[e];
+        if (c == 0) continue;
+        const int64_t cu = split.fixed_cost + c;
+        const int64_t lo = rt * cost, hi = rt * (cost + cu);   // [lo, hi) in cost units
+        // Boundaries b with b*C/n in [lo, hi).
+        for (int64_t b = (lo * n + C - 1) / C; b < n && b * C < hi * n; ++b) {
+          const int64_t tile = (b * C - lo * n + n * cu - 1) / (n * cu);
+          plan.unit_begin[b] = (int)(slot * rt + tile);
+        }
+        cost += (int)cu;
+        ++slot;
+      }
+      if (threadIdx.x == 0) plan.unit_begin[split.ctas] = (int)((int64_t)total_active * rt);
+    }
   }
   __syncthreads();
 
@@ -163,7 +199,7 @@ bool prep_fits_route(int64_t T, int64_t I) { return T <= 64 && T * I <= ((int64_
 
 cudaError_t launch_route(const void* sel, int index_dtype, int64_t T, int64_t K,
                          int64_t E, int* wc_global, const RoutePlan& plan,
-                         const TokenPrep& prep, cudaStream_t stream) {
+                         const TokenPrep& prep, const UnitSplit& split, cudaStream_t stream) {
   const int64_t P = T * K;
   const size_t smem = wc_global ? 0 : kRouteWarps * (size_t)E * sizeof(int);
   // Dynamic plus static shared memory above 48 KiB needs the opt-in.
@@ -179,10 +215,10 @@ cudaError_t launch_route(const void* sel, int index_dtype, int64_t T, int64_t K,
   }
   if (index_dtype == kIndexI64)
     route_kernel<int64_t><<<1, kRouteThreads, smem, stream>>>(
-        static_cast<const int64_t*>(sel), P, (int)E, wc_global, plan, (int)T, prep);
+        static_cast<const int64_t*>(sel), P, (int)E, wc_global, plan, (int)T, prep, split);
   else
     route_kernel<int32_t><<<1, kRouteThreads, smem, stream>>>(
-        static_cast<const int32_t*>(sel), P, (int)E, wc_global, plan, (int)T, prep);
+        static_cast<const int32_t*>(sel), P, (int)E, wc_global, plan, (int)T, prep, split);
   note_launch();
   return cudaGetLastError();
 }
