@@ -178,10 +178,11 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
   ws->plan.offsets = reinterpret_cast<int*>(take((size_t)(E + 1) * sizeof(int)));
   ws->plan.active = reinterpret_cast<int*>(take((size_t)E * sizeof(int)));
   ws->plan.pair_list = reinterpret_cast<int*>(take((size_t)P * sizeof(int)));
-  const size_t wc_words = route_global_counter_words(E);
-  ws->wc_global = wc_words ? reinterpret_cast<int*>(take(wc_words * sizeof(int))) : nullptr;
   const bool gemm = K > 0 && choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
   const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && K > 0 && !gemm;
+  const bool prep_in_route = prep && gemv_uses_stream(I) && prep_fits_route(T, I);
+  const size_t wc_words = route_global_counter_words(T, K, E, prep_in_route);
+  ws->wc_global = wc_words ? reinterpret_cast<int*>(take(wc_words * sizeof(int))) : nullptr;
   ws->x16 = prep ? reinterpret_cast<__half*>(take((size_t)T * I * sizeof(__half))) : nullptr;
   ws->sigma = prep ? reinterpret_cast<int*>(take((size_t)T * sizeof(int))) : nullptr;
   ws->grouped = gemm ? take(gemm_tc_grouped_bytes(T, K, I)) : nullptr;

@@ -72,6 +72,50 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&x)[4]) {
 }
 
 constexpr int kVecLanes = 32;   // one warp per segment of 4 * 32 outputs
+constexpr int kSlotBatch = 8;   // slots whose loads are issued together
+
+// Adds slots [k0, k0 + n) of pair row t*K (n <= kSlotBatch) to acc in slot
+// order. All ids, weights and partial-result vectors are loaded before the
+// first add, so the loads of the batch are in flight together.
+template <typename Idx>
+__device__ __forceinline__ void add_slots(const Idx* __restrict__ sel, const float* __restrict__ p,
+                                          const float* __restrict__ part, int ncol, int64_t O,
+                                          int64_t E, int64_t pk0, int n, int64_t o,
+                                          float (&acc)[4]) {
+  long long e[kSlotBatch];
+  float w[kSlotBatch];
+#pragma unroll
+  for (int j = 0; j < kSlotBatch; ++j) {
+    e[j] = j < n ? (long long)sel[pk0 + j] : -1;
+    w[j] = j < n ? p[pk0 + j] : 0.f;
+  }
+  float4 s[kSlotBatch];
+#pragma unroll
+  for (int j = 0; j < kSlotBatch; ++j) {
+    s[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e[j] >= 0 && e[j] < E)
+      s[j] = __ldcs(reinterpret_cast<const float4*>(part + (pk0 + j) * ncol * O + o));
+  }
+  for (int c = 1; c < ncol; ++c) {
+#pragma unroll
+    for (int j = 0; j < kSlotBatch; ++j) {
+      if (e[j] >= 0 && e[j] < E) {
+        const float4 u = __ldcs(
+            reinterpret_cast<const float4*>(part + ((pk0 + j) * ncol + c) * O + o));
+        s[j].x += u.x; s[j].y += u.y; s[j].z += u.z; s[j].w += u.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kSlotBatch; ++j) {
+    if (e[j] >= 0 && e[j] < E) {
+      acc[0] = fmaf(w[j], s[j].x, acc[0]);
+      acc[1] = fmaf(w[j], s[j].y, acc[1]);
+      acc[2] = fmaf(w[j], s[j].z, acc[2]);
+      acc[3] = fmaf(w[j], s[j].w, acc[3]);
+    }
+  }
+}
 
 template <typename Tok, typename Idx>
 __global__ void __launch_bounds__(256)
@@ -91,23 +135,8 @@ combine_vec_kernel(const Tok* __restrict__ ys, const Idx* __restrict__ sel,
     const int64_t o = 4 * v;
     float acc[4];
     load4(ys + t * O + o, acc);
-    for (int k = 0; k < K; ++k) {
-      const int64_t pk = t * K + k;
-      const long long e = (long long)sel[pk];
-      if (e >= 0 && e < E) {
-        const float* pp = part + pk * ncol * O + o;
-        float4 s = __ldcs(reinterpret_cast<const float4*>(pp));
-        for (int c = 1; c < ncol; ++c) {
-          const float4 u = __ldcs(reinterpret_cast<const float4*>(pp + (int64_t)c * O));
-          s.x += u.x; s.y += u.y; s.z += u.z; s.w += u.w;
-        }
-        const float w = p[pk];
-        acc[0] = fmaf(w, s.x, acc[0]);
-        acc[1] = fmaf(w, s.y, acc[1]);
-        acc[2] = fmaf(w, s.z, acc[2]);
-        acc[3] = fmaf(w, s.w, acc[3]);
-      }
-    }
+    for (int k0 = 0; k0 < K; k0 += kSlotBatch)
+      add_slots(sel, p, part, ncol, O, E, t * K + k0, min(kSlotBatch, K - k0), o, acc);
     store4(out + t * O + o, acc);
   }
 }

@@ -71,7 +71,11 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
 int linear_partial_columns(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
                            int token_dtype);
 
-size_t route_global_counter_words(int64_t E);
+// Workspace words the bucketer needs for its counters: per-warp counters
+// when they do not fit in shared memory (single CTA), or per-CTA counts
+// (many pairs, several CTAs). prep_in_route: the bucketer also prepares
+// the tokens (then it runs as one CTA).
+size_t route_global_counter_words(int64_t T, int64_t K, int64_t E, bool prep_in_route);
 
 // Tokens prepared for the staged GEMV (bf16 tokens): x16 = f16(x 2^sigma).
 struct TokenPrep {

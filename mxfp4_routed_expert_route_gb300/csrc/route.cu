@@ -12,6 +12,8 @@
 //   C. each warp walks its chunk again and scatters pair ids into place.
 // Inside a segment the pairs keep their (token, slot) order. Pairs whose
 // expert id lies outside [0, E) are skipped and counted on the device.
+// Large batches (at least 8192 pairs) run the same sort over many CTAs in
+// three kernels (count, scan, scatter); small ones keep the single launch.
 #include <mutex>
 
 #include "common.cuh"
@@ -55,6 +57,44 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int* t
   *total = warp_buf[32];
   __syncthreads();
   return r;
+}
+
+// Cost-balanced GEMV split, by the whole block after the counts and the
+// active list are known. The calling thread owns experts [e0, e1), whose
+// active ones are the consecutive active slots act0, act0+1, ...; their cost
+// prefix comes from one more scan. Every CTA boundary b < ctas lies in
+// exactly one expert's cost interval, and that expert's thread writes it.
+__device__ void write_unit_split(const RoutePlan& plan, const UnitSplit& split, int e0, int e1,
+                                 int act0, int total_active, int* warp_buf) {
+  if (split.ctas <= 0) return;
+  int my_cost = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int c = plan.counts[e];
+    if (c > 0) my_cost += split.fixed_cost + c;
+  }
+  int total_cost;
+  int cost = block_exclusive_scan(my_cost, warp_buf, &total_cost);
+  const int64_t rt = split.row_tiles, n = split.ctas;
+  const int64_t C = rt * (int64_t)total_cost;        // total cost of all units
+  if (C == 0) {
+    for (int b = threadIdx.x; b <= split.ctas; b += blockDim.x) plan.unit_begin[b] = 0;
+    return;
+  }
+  int slot = act0;
+  for (int e = e0; e < e1; ++e) {
+    const int c = plan.counts[e];
+    if (c == 0) continue;
+    const int64_t cu = split.fixed_cost + c;
+    const int64_t lo = rt * cost, hi = rt * (cost + cu);   // [lo, hi) in cost units
+    // Boundaries b with b*C/n in [lo, hi).
+    for (int64_t b = (lo * n + C - 1) / C; b < n && b * C < hi * n; ++b) {
+      const int64_t tile = (b * C - lo * n + n * cu - 1) / (n * cu);
+      plan.unit_begin[b] = (int)(slot * rt + tile);
+    }
+    cost += (int)cu;
+    ++slot;
+  }
+  if (threadIdx.x == 0) plan.unit_begin[split.ctas] = (int)((int64_t)total_active * rt);
 }
 
 template <typename Idx>
@@ -123,40 +163,8 @@ route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
     plan.meta[kMetaNumPairs] = total_pairs;
   }
 
-  // B'. Cost-balanced GEMV split: the active experts of this thread are the
-  // consecutive active slots act0, act0+1, ...; their cost prefix comes from
-  // one more scan. Every CTA boundary b < ctas lies in exactly one expert's
-  // cost interval, and that expert's thread writes it.
-  if (split.ctas > 0) {
-    int my_cost = 0;
-    for (int e = e0; e < e1; ++e) {
-      const int c = plan.counts[e];
-      if (c > 0) my_cost += split.fixed_cost + c;
-    }
-    int total_cost;
-    int cost = block_exclusive_scan(my_cost, warp_buf, &total_cost);
-    const int64_t rt = split.row_tiles, n = split.ctas;
-    const int64_t C = rt * (int64_t)total_cost;        // total cost of all units
-    if (C == 0) {
-      for (int b = threadIdx.x; b <= split.ctas; b += kRouteThreads) plan.unit_begin[b] = 0;
-    } else {
-      int slot = act0;
-      for (int e = e0; e < e1; ++e) {
-        const int c = plan.counts[e];
-        if (c == 0) continue;
-        const int64_t cu = split.fixed_cost + c;
-        const int64_t lo = rt * cost, hi = rt * (cost + cu);   // [lo, hi) in cost units
-        // Boundaries b with b*C/n in [lo, hi).
-        for (int64_t b = (lo * n + C - 1) / C; b < n && b * C < hi * n; ++b) {
-          const int64_t tile = (b * C - lo * n + n * cu - 1) / (n * cu);
-          plan.unit_begin[b] = (int)(slot * rt + tile);
-        }
-        cost += (int)cu;
-        ++slot;
-      }
-      if (threadIdx.x == 0) plan.unit_begin[split.ctas] = (int)((int64_t)total_active * rt);
-    }
-  }
+  // B'. Cost-balanced GEMV split.
+  write_unit_split(plan, split, e0, e1, act0, total_active, warp_buf);
   __syncthreads();
 
   // C. stable scatter of pair ids.
@@ -188,9 +196,188 @@ route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
                  (int)prep.I, lane);
 }
 
+// ---------------------------------------------------------------------------
+// Multi-CTA bucketer for many pairs: the same stable counting sort in three
+// kernels. CTA c owns pairs [c*kMultiChunk, (c+1)*kMultiChunk), its warps
+// contiguous sub-chunks of it.
+//   count:   per-CTA, per-expert counts -> cta_counts[e][c]
+//   scan:    one CTA: per-expert totals, exclusive prefix of cta_counts over
+//            CTAs (each CTA's first position inside every expert segment),
+//            offsets, active list, meta, GEMV split
+//   scatter: each CTA counts its chunk again per warp and scatters pair ids
+constexpr int kMultiThreads = 256;
+constexpr int kMultiWarps = kMultiThreads / 32;
+constexpr int kMultiChunk = 512;                 // pairs per CTA
+constexpr int kMultiPerWarp = kMultiChunk / kMultiWarps;
+constexpr int64_t kMultiMinPairs = 8192;         // below this one CTA is faster
+constexpr int kMultiMaxExperts = 1024;           // per-warp counters in shared memory
+
+// Per-warp counts of this CTA's chunk into wc[warp][E]; returns the warp's
+// number of invalid ids.
+template <typename Idx>
+__device__ __forceinline__ int count_chunk(const Idx* __restrict__ sel, int64_t P, int E,
+                                           int* wc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lanes_below = (1u << lane) - 1u;
+  for (int i = threadIdx.x; i < kMultiWarps * E; i += kMultiThreads) wc[i] = 0;
+  __syncthreads();
+  const int64_t pbeg = min(P, (int64_t)blockIdx.x * kMultiChunk + (int64_t)warp * kMultiPerWarp);
+  const int64_t pend = min(P, pbeg + kMultiPerWarp);
+  int* my_wc = wc + (size_t)warp * E;
+  int bad = 0;
+  for (int64_t base = pbeg; base < pend; base += 32) {
+    const int64_t i = base + lane;
+    const bool in = i < pend;
+    const long long e = in ? (long long)sel[i] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    bad += (in && !valid) ? 1 : 0;
+    const unsigned peers = __match_any_sync(kFullMask, valid ? (int)e : -1);
+    if (valid && (peers & lanes_below) == 0) my_wc[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  return bad;
+}
+
+template <typename Idx>
+__global__ void __launch_bounds__(kMultiThreads)
+route_count_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* __restrict__ cta_counts) {
+  pdl_launch_dependents();
+  extern __shared__ int wc[];                    // [kMultiWarps][E]
+  int bad = count_chunk(sel, P, E, wc);
+  const int nctas = gridDim.x;
+  for (int e = threadIdx.x; e < E; e += kMultiThreads) {
+    int c = 0;
+    for (int w = 0; w < kMultiWarps; ++w) c += wc[w * E + e];
+    cta_counts[(size_t)e * nctas + blockIdx.x] = c;
+  }
+  // Invalid ids: count them for mxfp4el_device_errors().
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) bad += __shfl_xor_sync(kFullMask, bad, o);
+  if ((threadIdx.x & 31) == 0 && bad > 0)
+    atomicAdd(&g_status[kStatusBadPairs], (unsigned long long)bad);
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+route_scan_kernel(int* __restrict__ cta_counts, int nctas, int E, RoutePlan plan,
+                  UnitSplit split) {
+  pdl_launch_dependents();
+  pdl_wait();                                    // the counts are complete
+  __shared__ int warp_buf[33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Per expert (one warp each): exclusive prefix over CTAs, in place.
+  for (int e = warp; e < E; e += kRouteWarps) {
+    int* row = cta_counts + (size_t)e * nctas;
+    int run = 0;
+    for (int c0 = 0; c0 < nctas; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nctas ? row[c] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(kFullMask, incl, off);
+        if (lane >= off) incl += n;
+      }
+      if (c < nctas) row[c] = run + incl - v;
+      run += __shfl_sync(kFullMask, incl, 31);
+    }
+    if (lane == 0) plan.counts[e] = run;
+  }
+  __syncthreads();
+  // Totals -> offsets, active list, meta (as phase B of route_kernel).
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;
+  const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
+  int my_pairs = 0, my_active = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int c = plan.counts[e];
+    my_pairs += c;
+    my_active += c > 0 ? 1 : 0;
+  }
+  int total_pairs, total_active;
+  int off = block_exclusive_scan(my_pairs, warp_buf, &total_pairs);
+  int act = block_exclusive_scan(my_active, warp_buf, &total_active);
+  const int act0 = act;
+  for (int e = e0; e < e1; ++e) {
+    const int c = plan.counts[e];
+    plan.offsets[e] = off;
+    if (c > 0) plan.active[act++] = e;
+    off += c;
+  }
+  if (threadIdx.x == 0) {
+    plan.offsets[E] = total_pairs;
+    plan.meta[kMetaNumActive] = total_active;
+    plan.meta[kMetaNumPairs] = total_pairs;
+  }
+  write_unit_split(plan, split, e0, e1, act0, total_active, warp_buf);
+}
+
+template <typename Idx>
+__global__ void __launch_bounds__(kMultiThreads)
+route_scatter_kernel(const Idx* __restrict__ sel, int64_t P, int E,
+                     const int* __restrict__ cta_bases, RoutePlan plan) {
+  pdl_launch_dependents();
+  extern __shared__ int wc[];                    // [kMultiWarps][E]
+  count_chunk(sel, P, E, wc);                    // reads only the ids
+  pdl_wait();                                    // offsets and CTA bases are ready
+  const int nctas = gridDim.x;
+  for (int e = threadIdx.x; e < E; e += kMultiThreads) {
+    int run = plan.offsets[e] + cta_bases[(size_t)e * nctas + blockIdx.x];
+    for (int w = 0; w < kMultiWarps; ++w) {
+      const int cw = wc[w * E + e];
+      wc[w * E + e] = run;
+      run += cw;
+    }
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lanes_below = (1u << lane) - 1u;
+  const int64_t pbeg = min(P, (int64_t)blockIdx.x * kMultiChunk + (int64_t)warp * kMultiPerWarp);
+  const int64_t pend = min(P, pbeg + kMultiPerWarp);
+  int* my_wc = wc + (size_t)warp * E;
+  for (int64_t base = pbeg; base < pend; base += 32) {
+    const int64_t i = base + lane;
+    const bool in = i < pend;
+    const long long e = in ? (long long)sel[i] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(kFullMask, valid ? (int)e : -1);
+    int start = 0;
+    if (valid) start = my_wc[e];
+    __syncwarp();
+    if (valid) {
+      plan.pair_list[start + __popc(peers & lanes_below)] = (int)i;
+      if ((peers & lanes_below) == 0) my_wc[e] = start + __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+int multi_ctas(int64_t P, int64_t E, bool prep) {
+  if (prep || P < kMultiMinPairs || E > kMultiMaxExperts) return 0;
+  const int64_t n = (P + kMultiChunk - 1) / kMultiChunk;
+  return n <= 0x7fffffff ? (int)n : 0;
+}
+
+template <typename Idx>
+cudaError_t launch_multi(const Idx* sel, int64_t P, int64_t E, int nctas, int* cta_counts,
+                         const RoutePlan& plan, const UnitSplit& split, cudaStream_t stream) {
+  const size_t smem = (size_t)kMultiWarps * E * sizeof(int);
+  route_count_kernel<Idx><<<nctas, kMultiThreads, smem, stream>>>(sel, P, (int)E, cta_counts);
+  note_launch();
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  err = launch_after_previous(route_scan_kernel, dim3(1), dim3(kRouteThreads), 0, stream,
+                              cta_counts, nctas, (int)E, plan, split);
+  if (err != cudaSuccess) return err;
+  return launch_after_previous(route_scatter_kernel<Idx>, dim3((unsigned)nctas),
+                               dim3(kMultiThreads), smem, stream, sel, P, (int)E,
+                               static_cast<const int*>(cta_counts), plan);
+}
+
 }  // namespace
 
-size_t route_global_counter_words(int64_t E) {
+size_t route_global_counter_words(int64_t T, int64_t K, int64_t E, bool prep_in_route) {
+  const int nctas = multi_ctas(T * K, E, prep_in_route);
+  if (nctas > 0) return (size_t)nctas * (size_t)E;
   return kRouteWarps * (size_t)E * sizeof(int) > kRouteSmemLimit
              ? (size_t)kRouteWarps * (size_t)E : 0;
 }
@@ -201,6 +388,14 @@ cudaError_t launch_route(const void* sel, int index_dtype, int64_t T, int64_t K,
                          int64_t E, int* wc_global, const RoutePlan& plan,
                          const TokenPrep& prep, const UnitSplit& split, cudaStream_t stream) {
   const int64_t P = T * K;
+  const int nctas = multi_ctas(P, E, prep.x != nullptr);
+  if (nctas > 0) {
+    if (index_dtype == kIndexI64)
+      return launch_multi(static_cast<const int64_t*>(sel), P, E, nctas, wc_global, plan, split,
+                          stream);
+    return launch_multi(static_cast<const int32_t*>(sel), P, E, nctas, wc_global, plan, split,
+                        stream);
+  }
   const size_t smem = wc_global ? 0 : kRouteWarps * (size_t)E * sizeof(int);
   // Dynamic plus static shared memory above 48 KiB needs the opt-in.
   if (smem > 40 * 1024) {

@@ -14,7 +14,7 @@ import torch
 import oracle
 from gpu_util import (TOL, assert_parity, digest, oracle_rows, run_gpu,
                       sample_rows)
-from mxfp4_routed_expert_route_gb300 import (_native, device_errors,
+from mxfp4_routed_expert_route_gb300 import (_native, device_errors, wait_timeouts,
                                              mxfp4_expert_linear, workloads)
 
 pytestmark = pytest.mark.gpu
@@ -286,3 +286,21 @@ def test_combine_vector_and_scalar_paths_agree_bitwise():
     assert ys_off.data_ptr() % 16 != 0
     b = mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"], ys_off)
     assert torch.equal(a, b)
+
+
+def test_many_pairs_gemv_path_with_invalid_ids():
+    # 9600 (token, slot) pairs: the bucketer runs as several CTAs (count,
+    # scan, scatter) and writes the GEMV's cost-balanced CTA ranges; fp32
+    # tokens keep the GEMV path. Two out-of-range ids are skipped and counted.
+    wl = workloads.make(2400, 48, 4, 96, 72, dtype=torch.float32, seed=42)
+    sel = wl.sel.clone()
+    sel[17, 2] = 48
+    sel[2399, 0] = -1
+    device_errors()                                    # reset the counter
+    out = run_gpu(wl, sel=sel)
+    assert device_errors() == 2
+    assert wait_timeouts() == 0
+    rows = sample_rows(wl, 64, seed=3)
+    rows = np.union1d(rows, [17, 2399])
+    want, absm, bad = oracle_rows(wl, rows=rows, sel=sel)
+    assert_parity(out[torch.from_numpy(rows).cuda()], want, absm, wl.dtype, "9600 pairs")
