@@ -72,43 +72,43 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&x)[4]) {
 }
 
 constexpr int kVecLanes = 32;   // one warp per segment of 4 * 32 outputs
-constexpr int kSlotBatch = 8;   // slots whose loads are issued together
+constexpr int kSlotBatch = 4;   // slots whose loads are issued together
 
 // Adds slots [k0, k0 + n) of pair row t*K (n <= kSlotBatch) to acc in slot
-// order. All ids, weights and partial-result vectors are loaded before the
-// first add, so the loads of the batch are in flight together.
+// order. All ids, weights and partial-result vectors of the batch are loaded
+// before the first add, so their loads are in flight together.
 template <typename Idx>
 __device__ __forceinline__ void add_slots(const Idx* __restrict__ sel, const float* __restrict__ p,
                                           const float* __restrict__ part, int ncol, int64_t O,
                                           int64_t E, int64_t pk0, int n, int64_t o,
                                           float (&acc)[4]) {
-  long long e[kSlotBatch];
+  bool valid[kSlotBatch];
   float w[kSlotBatch];
 #pragma unroll
   for (int j = 0; j < kSlotBatch; ++j) {
-    e[j] = j < n ? (long long)sel[pk0 + j] : -1;
+    const long long e = j < n ? (long long)sel[pk0 + j] : -1;
+    valid[j] = e >= 0 && e < E;
     w[j] = j < n ? p[pk0 + j] : 0.f;
   }
+  const int64_t row = (int64_t)ncol * O;          // floats per pair
+  const float* base = part + pk0 * row + o;
   float4 s[kSlotBatch];
 #pragma unroll
-  for (int j = 0; j < kSlotBatch; ++j) {
-    s[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (e[j] >= 0 && e[j] < E)
-      s[j] = __ldcs(reinterpret_cast<const float4*>(part + (pk0 + j) * ncol * O + o));
-  }
+  for (int j = 0; j < kSlotBatch; ++j)
+    s[j] = valid[j] ? __ldcs(reinterpret_cast<const float4*>(base + j * row))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c = 1; c < ncol; ++c) {
 #pragma unroll
     for (int j = 0; j < kSlotBatch; ++j) {
-      if (e[j] >= 0 && e[j] < E) {
-        const float4 u = __ldcs(
-            reinterpret_cast<const float4*>(part + ((pk0 + j) * ncol + c) * O + o));
+      if (valid[j]) {
+        const float4 u = __ldcs(reinterpret_cast<const float4*>(base + j * row + (int64_t)c * O));
         s[j].x += u.x; s[j].y += u.y; s[j].z += u.z; s[j].w += u.w;
       }
     }
   }
 #pragma unroll
   for (int j = 0; j < kSlotBatch; ++j) {
-    if (e[j] >= 0 && e[j] < E) {
+    if (valid[j]) {
       acc[0] = fmaf(w[j], s[j].x, acc[0]);
       acc[1] = fmaf(w[j], s[j].y, acc[1]);
       acc[2] = fmaf(w[j], s[j].z, acc[2]);
