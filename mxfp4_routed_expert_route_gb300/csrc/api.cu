@@ -115,12 +115,16 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
     unsigned long long* status = device_status_words();
     if (status == nullptr) return MXFP4EL_ERR_CUDA;
     const bool gemm = choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
-    const bool prep = !gemm && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
+    // Small batches on the GEMV: each GEMV CTA routes for itself.
+    const bool self = !gemm && gemv_self_route(T, E, I, O, K);
+    const bool prep = !gemm && !self && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
     const bool prep_in_route = prep && prep_fits_route(T, I);
     TokenPrep tp = {prep_in_route ? x : nullptr, ws.x16, ws.sigma, I};
     const UnitSplit split = gemm ? UnitSplit{0, 0, 0} : gemv_unit_split(T, E, I, O, K);
     mark(MXFP4EL_STAGE_ROUTE, true, stream);
-    err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, tp, split, stream);
+    err = cudaSuccess;
+    if (!self)
+      err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, tp, split, stream);
     if (err == cudaSuccess && prep && !prep_in_route)
       err = launch_prep_tokens(x, ws.x16, ws.sigma, T, I, stream);
     mark(MXFP4EL_STAGE_ROUTE, false, stream);
@@ -136,8 +140,8 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
       err = launch_gemm_tc(x, packed, scales, ws.plan, ws.grouped, ws.part, status, T, E, I, O,
                            K, stream);
     else
-      err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, packed, scales, ws.plan,
-                        ws.part, status, T, E, I, O, K, stream);
+      err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, sel, index_dtype, packed, scales,
+                        ws.plan, ws.part, status, T, E, I, O, K, stream);
     mark(MXFP4EL_STAGE_LINEAR, false, stream);
     if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
   }
@@ -179,7 +183,8 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
   ws->plan.active = reinterpret_cast<int*>(take((size_t)E * sizeof(int)));
   ws->plan.pair_list = reinterpret_cast<int*>(take((size_t)P * sizeof(int)));
   const bool gemm = K > 0 && choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
-  const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && K > 0 && !gemm;
+  const bool self = K > 0 && !gemm && gemv_self_route(T, E, I, O, K);
+  const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && K > 0 && !gemm && !self;
   const bool prep_in_route = prep && gemv_uses_stream(I) && prep_fits_route(T, I);
   const size_t wc_words = route_global_counter_words(T, K, E, prep_in_route);
   ws->wc_global = wc_words ? reinterpret_cast<int*>(take(wc_words * sizeof(int))) : nullptr;

@@ -37,6 +37,8 @@
 // memory (no staging), for rows too wide for a shared-memory stage.
 #include <cuda_fp16.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -119,6 +121,21 @@ template <> struct GroupToken<__half> {     // bf16 tokens, pre-scaled to f16
       v[4 * q + 0] = u.x; v[4 * q + 1] = u.y; v[4 * q + 2] = u.z; v[4 * q + 3] = u.w;
     }
   }
+  // The same values from the bf16 tokens: f16(x * up), up = 2^sigma_t, as
+  // the token prep rounds them.
+  __device__ __forceinline__ void load_scaled(const __nv_bfloat16* row, int g, float up) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = ld_u4(row + (size_t)g * 32 + 8 * q);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16) * up,
+                                            __uint_as_float(w[k] & 0xffff0000u) * up);
+        v[4 * q + k] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
+  }
   __device__ __forceinline__ float dot(const uint32_t (&w)[16]) const { return dot_group_f16(w, v); }
 };
 
@@ -152,6 +169,13 @@ struct StreamArgs {
   int stages;
   uint32_t stage_bytes;          // header + packed part + scale part, 128-aligned
   uint32_t packed_stage_bytes;   // rows_per_tile * G * 16 (scales follow)
+  // Self-routed mode (small batches): the CTA derives the routing lists
+  // from the ids itself, in shared memory, and scales bf16 tokens on load.
+  const void* sel;               // (T, K) expert ids, int32 or int64
+  int sel_i64;
+  int T, E, P;                   // P = T * K
+  int fixed_cost;                // split cost of a unit beyond its tokens
+  uint32_t route_bytes;          // bytes of the routing area in shared memory
 };
 
 // Written by the producer into each stage before its copies are issued.
@@ -167,6 +191,220 @@ static_assert(sizeof(StageHeader) == 128, "stage header is 128 bytes");
 
 template <int N> struct Pow2Ceil { static constexpr int value = 2 * Pow2Ceil<(N + 1) / 2>::value; };
 template <> struct Pow2Ceil<1> { static constexpr int value = 1; };
+
+// ------------------------------------------------- self-routed mode -------
+// For small batches each CTA builds, in shared memory, the part of the
+// routing that it needs (the bucketer's lists, computed the same way): the
+// per-expert counts and offsets, the ascending active list, its own
+// cost-balanced unit range, the pair ids of its experts in (token, slot)
+// order at their global positions, and the power-of-two scale of each of
+// its tokens. This saves the bucketer's launch on the latency-bound path.
+constexpr int kSelfMaxPairs = 1024;
+constexpr int kSelfMaxExperts = 2048;
+constexpr int kSelfMaxTokens = 1024;
+constexpr int kSigmaNeeded = -1000;            // token used by this CTA, scale pending
+
+struct SelfPlan {
+  int* off;      // [E + 1] segment offsets
+  int* run;      // [E]     next free position while placing pairs
+  int* active;   // [E]     ascending active experts
+  int* list;     // [P]     pair ids of this CTA's experts, at their global positions
+  int* sigma;    // [T]     token scale exponents (bf16 tokens)
+  int* misc;     // [8]     0: active experts, 1: first unit, 2: end unit, 3: pairs
+  int* wbuf;     // [33]    scan scratch
+};
+
+__host__ __device__ inline uint32_t self_route_bytes(int E, int P, int T) {
+  return (uint32_t)(((size_t)(E + 1) + 2 * (size_t)E + (size_t)P + (size_t)T + 8 + 33) * 4 + 127) /
+         128 * 128;
+}
+
+__device__ __forceinline__ SelfPlan self_plan(unsigned char* area, int E, int P, int T) {
+  SelfPlan sp;
+  int* w = reinterpret_cast<int*>(area);
+  sp.off = w;
+  sp.run = sp.off + (E + 1);
+  sp.active = sp.run + E;
+  sp.list = sp.active + E;
+  sp.sigma = sp.list + P;
+  sp.misc = sp.sigma + T;
+  sp.wbuf = sp.misc + 8;
+  return sp;
+}
+
+__device__ __forceinline__ long long load_id(const StreamArgs& a, int i) {
+  return a.sel_i64 ? static_cast<const long long*>(a.sel)[i]
+                   : (long long)static_cast<const int*>(a.sel)[i];
+}
+
+// Exclusive prefix sum over the block (any multiple of 32 threads up to
+// 1024); *total gets the block total.
+__device__ __forceinline__ int block_scan(int v, int* wbuf, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(kFullMask, incl, off);
+    if (lane >= off) incl += n;
+  }
+  if (lane == 31) wbuf[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nw ? wbuf[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(kFullMask, wi, off);
+      if (lane >= off) wi += n;
+    }
+    if (lane < nw) wbuf[lane] = wi - w;
+    if (lane == 31) wbuf[32] = wi;
+  }
+  __syncthreads();
+  const int r = wbuf[warp] + incl - v;
+  *total = wbuf[32];
+  __syncthreads();
+  return r;
+}
+
+// First unit of CTA b of n under the cost-balanced split (unit (u, tile)
+// costs fixed + tokens of active expert u); the same integer formula as the
+// bucketer's table.
+__device__ __forceinline__ int split_begin(const SelfPlan& sp, int na, int pairs, int64_t rt,
+                                           int fixed, int64_t b, int64_t n) {
+  if (b >= n) return (int)(na * rt);
+  const int64_t C = rt * ((int64_t)fixed * na + pairs);   // cost of all units
+  if (C == 0) return 0;
+  auto cost_before = [&](int u) { return (int64_t)fixed * u + sp.off[sp.active[u]]; };
+  // Largest u with rt * cost_before(u) * n <= b * C.
+  int lo = 0, hi = na - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (rt * cost_before(mid) * n <= b * C) lo = mid;
+    else hi = mid - 1;
+  }
+  const int u = lo;
+  const int64_t e = sp.active[u];
+  const int64_t cu = fixed + (sp.off[e + 1] - sp.off[e]);
+  const int64_t lo_cost = rt * cost_before(u);
+  const int64_t tile = (b * C - lo_cost * n + n * cu - 1) / (n * cu);
+  return (int)(u * rt + tile);
+}
+
+// Barrier of the consumer warps only (the producer does not take part).
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+}
+
+// The CTA's routing plan, by the whole block: counts, offsets, the active
+// list and this CTA's unit range (what the producer needs).
+__device__ void self_route_plan(const StreamArgs& a, const SelfPlan& sp) {
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
+  const int E = a.E, P = a.P, T = a.T;
+  for (int e = tid; e < E; e += nthr) sp.off[e] = 0;
+  for (int t = tid; t < T; t += nthr) sp.sigma[t] = 0;
+  __syncthreads();
+  // Counts (order does not matter here).
+  int bad = 0;
+  for (int i = tid; i < P; i += nthr) {
+    const long long e = load_id(a, i);
+    if (e >= 0 && e < E) atomicAdd(&sp.off[e], 1);
+    else ++bad;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) bad += __shfl_xor_sync(kFullMask, bad, o);
+  if (lane == 0 && bad > 0 && blockIdx.x == 0)     // every CTA sees them; one counts
+    atomicAdd(&a.status[kStatusBadPairs], (unsigned long long)bad);
+  __syncthreads();
+  // Offsets and the ascending active list.
+  const int per = (E + nthr - 1) / nthr;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int my_pairs = 0, my_active = 0;
+  for (int e = e0; e < e1; ++e) {
+    my_pairs += sp.off[e];
+    my_active += sp.off[e] > 0 ? 1 : 0;
+  }
+  int total_pairs, total_active;
+  int off = block_scan(my_pairs, sp.wbuf, &total_pairs);
+  int act = block_scan(my_active, sp.wbuf, &total_active);
+  for (int e = e0; e < e1; ++e) {
+    const int c = sp.off[e];
+    sp.off[e] = off;
+    if (c > 0) sp.active[act++] = e;
+    off += c;
+  }
+  if (tid == 0) {
+    sp.off[E] = total_pairs;
+    sp.misc[0] = total_active;
+    sp.misc[3] = total_pairs;
+  }
+  __syncthreads();
+  // This CTA's unit range.
+  if (tid == 0) {
+    sp.misc[1] = split_begin(sp, total_active, total_pairs, a.row_tiles, a.fixed_cost,
+                             blockIdx.x, gridDim.x);
+    sp.misc[2] = split_begin(sp, total_active, total_pairs, a.row_tiles, a.fixed_cost,
+                             blockIdx.x + 1, gridDim.x);
+  }
+  __syncthreads();
+}
+
+// The rest, by the consumer warps while the producer starts its copies:
+// the pair ids of this CTA's experts and the scales of their tokens.
+__device__ void self_route_lists(const StreamArgs& a, const SelfPlan& sp, bool bf16_tokens) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int P = a.P, T = a.T;
+  const int ubeg = sp.misc[1], uend = sp.misc[2];
+  if (ubeg >= uend) return;
+  // Pair ids of this CTA's experts (active slots ubeg/rt .. (uend-1)/rt,
+  // i.e. expert ids e_lo .. e_hi), placed in (token, slot) order by one warp.
+  const int e_lo = sp.active[ubeg / a.row_tiles], e_hi = sp.active[(uend - 1) / a.row_tiles];
+  if (warp == 0) {
+    for (int e = e_lo + lane; e <= e_hi; e += 32) sp.run[e] = sp.off[e];
+    __syncwarp();
+    const unsigned below = (1u << lane) - 1u;
+    for (int base = 0; base < P; base += 32) {
+      const int i = base + lane;
+      const long long e = i < P ? load_id(a, i) : -1;
+      const bool mine = e >= e_lo && e <= e_hi;
+      const unsigned peers = __match_any_sync(kFullMask, mine ? (int)e : -1);
+      if (mine) {
+        sp.list[sp.run[e] + __popc(peers & below)] = i;
+        sp.sigma[i / a.K] = kSigmaNeeded;
+      }
+      __syncwarp();
+      if (mine && (peers & below) == 0) sp.run[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  consumers_sync();
+  // Scale exponents of this CTA's bf16 tokens (as the token prep computes them).
+  if (bf16_tokens) {
+    for (int t = warp; t < T; t += kConsumerWarps) {
+      if (sp.sigma[t] != kSigmaNeeded) continue;
+      const uint4* row =
+          reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) + (size_t)t * a.I);
+      uint32_t m = 0;
+      for (int i = lane; i < a.I / 8; i += 32) {
+        const uint4 v = __ldg(row + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          m = max(m, (w[k] << 16) & 0x7fffffffu);
+          m = max(m, w[k] & 0x7fff0000u);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(kFullMask, m, o));
+      const int ex = (int)(m >> 23);
+      int sg = 0;
+      if (m != 0 && ex < 255) sg = min(126, 135 - ex);
+      __syncwarp();
+      if (lane == 0) sp.sigma[t] = sg;
+    }
+  }
+  consumers_sync();
+}
 
 // One pass of one consumer warp over its RWS rows of a staged tile, for NTA
 // tokens: lane = group g of the warp's column; each (row, token) gets one
@@ -240,27 +478,40 @@ __device__ __forceinline__ void stream_pass_any(const StreamArgs& a,
 // position `base` of an expert's segment [base, seg_end).
 // Also the factor that undoes each token's power-of-two scaling (1 for fp32
 // tokens).
-template <typename Elem, int NT>
-__device__ __forceinline__ void load_pass(const StreamArgs& a, GroupToken<Elem> (&xt)[NT],
-                                          int (&pair)[NT], float (&unscale)[NT], int base,
-                                          int seg_end, int g) {
+template <typename Elem, int NT, bool kSelf>
+__device__ __forceinline__ void load_pass(const StreamArgs& a, const SelfPlan& sp,
+                                          GroupToken<Elem> (&xt)[NT], int (&pair)[NT],
+                                          float (&unscale)[NT], int base, int seg_end, int g) {
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    pair[j] = a.plan.pair_list[base + min(j, seg_end - base - 1)];
+    const int pos = base + min(j, seg_end - base - 1);
+    pair[j] = kSelf ? sp.list[pos] : a.plan.pair_list[pos];
     const int t = pair[j] / a.K;
-    if (g < a.G) xt[j].load(static_cast<const Elem*>(a.x) + (size_t)t * a.I, g);
-    unscale[j] = a.sigma != nullptr ? __uint_as_float((uint32_t)(127 - a.sigma[t]) << 23) : 1.f;
+    if constexpr (kSelf && sizeof(Elem) == 2) {
+      // bf16 tokens scaled on load by this CTA's own power of two.
+      const int sg = sp.sigma[t];
+      if (g < a.G)
+        xt[j].load_scaled(static_cast<const __nv_bfloat16*>(a.x) + (size_t)t * a.I, g,
+                          __uint_as_float((uint32_t)(sg + 127) << 23));
+      unscale[j] = __uint_as_float((uint32_t)(127 - sg) << 23);
+    } else {
+      if (g < a.G) xt[j].load(static_cast<const Elem*>(a.x) + (size_t)t * a.I, g);
+      unscale[j] =
+          a.sigma != nullptr ? __uint_as_float((uint32_t)(127 - a.sigma[t]) << 23) : 1.f;
+    }
   }
 }
 
-template <typename Elem, int RWS, int NT>
+template <typename Elem, int RWS, int NT, bool kSelf>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 gemv_stream_kernel(const StreamArgs a) {
   static_assert(NT == 1 || NT == 2, "one or two tokens per pass");
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  unsigned char* stage_base = smem + 2 * kMaxStages * sizeof(uint64_t);
+  unsigned char* route_area = smem + 2 * kMaxStages * sizeof(uint64_t);
+  unsigned char* stage_base = route_area + (kSelf ? a.route_bytes : 0u);
+  const SelfPlan rp = self_plan(route_area, a.E, a.P, a.T);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
@@ -271,16 +522,27 @@ gemv_stream_kernel(const StreamArgs a) {
     }
     fence_mbar_init();
   }
-  __syncthreads();
-  pdl_wait();                  // the routing lists and prepared tokens are ready
+  // Self-routed: this is the call's first kernel, so it reads the ids and
+  // tokens only after whatever ran before it on the stream has finished.
+  // Otherwise: the bucketer's lists and the prepared tokens are ready.
+  pdl_wait();
+  if constexpr (kSelf) {
+    self_route_plan(a, rp);                // ends with a block barrier
+    if (warp != kConsumerWarps) self_route_lists(a, rp, sizeof(Elem) == 2);
+  } else {
+    __syncthreads();
+  }
 
   // Each CTA takes one contiguous range of units, so consecutive units are
   // consecutive row tiles of the same expert (and of consecutive memory).
   // The bucketer balances the ranges by cost (an expert's units cost more
   // the more tokens it has); without its table the ranges are equal.
-  const int num_units = a.plan.meta[kMetaNumActive] * a.row_tiles;
+  const int num_units = (kSelf ? rp.misc[0] : a.plan.meta[kMetaNumActive]) * a.row_tiles;
   int ubeg, uend;
-  if (a.plan.unit_begin != nullptr) {
+  if (kSelf) {
+    ubeg = min(rp.misc[1], num_units);
+    uend = min(rp.misc[2], num_units);
+  } else if (a.plan.unit_begin != nullptr) {
     ubeg = min(a.plan.unit_begin[blockIdx.x], num_units);
     uend = min(a.plan.unit_begin[blockIdx.x + 1], num_units);
   } else {
@@ -303,7 +565,7 @@ gemv_stream_kernel(const StreamArgs a) {
     for (int unit = ubeg; unit < uend; ++unit, ++issued) {
       const int st = issued % a.stages;
       const uint32_t round = (uint32_t)(issued / a.stages);
-      if (u != cached_u) { e = a.plan.active[u]; cached_u = u; }
+      if (u != cached_u) { e = kSelf ? rp.active[u] : a.plan.active[u]; cached_u = u; }
       const int o0 = tile * a.rows_per_tile;
       const int rows = min(a.rows_per_tile, O - o0);
       const size_t row0 = (size_t)e * O + o0;
@@ -374,9 +636,9 @@ gemv_stream_kernel(const StreamArgs a) {
     if (working && rbase < rows) {
       if (e != cached_e) {                    // new expert: its first pass
         cached_e = e;
-        seg_beg = a.plan.offsets[e];
-        seg_end = a.plan.offsets[e + 1];
-        load_pass(a, x0, pair0, unscale0, seg_beg, seg_end, g);
+        seg_beg = kSelf ? rp.off[e] : a.plan.offsets[e];
+        seg_end = kSelf ? rp.off[e + 1] : a.plan.offsets[e + 1];
+        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, unscale0, seg_beg, seg_end, g);
       }
       // This lane's group in row rbase of the tile: packed bytes and scale.
       const uint32_t sp_lane =
@@ -400,7 +662,7 @@ gemv_stream_kernel(const StreamArgs a) {
         if (base >= seg_end) break;
         // More tokens: the cache now holds a later pass, so reload the first
         // one at the next tile.
-        load_pass(a, x0, pair0, unscale0, base, seg_end, g);
+        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, unscale0, base, seg_end, g);
         cached_e = -1;
       }
     }
@@ -489,12 +751,12 @@ int num_sms() {
 
 int64_t stream_grid(int64_t bound_units) { return std::min<int64_t>(num_sms(), bound_units); }
 
-template <typename Elem, int RWS>
+template <typename Elem, int RWS, bool kSelf>
 cudaError_t launch_stream(StreamArgs a, size_t smem, int64_t bound_units, cudaStream_t stream) {
   // Two tokens per pass for f16 operands; fp32 operands take twice the
   // registers, so one.
   constexpr int NT = sizeof(Elem) == 2 ? 2 : 1;
-  auto kern = gemv_stream_kernel<Elem, RWS, NT>;
+  auto kern = gemv_stream_kernel<Elem, RWS, NT, kSelf>;
   static std::mutex mu;
   static size_t opted[64] = {};
   int dev = 0;
@@ -570,6 +832,16 @@ int64_t stream_row_tiles(const StreamShape& sh, int64_t O) {
 #define MXFP4EL_GEMV_FIXED_COST 0
 #endif
 
+bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
+  // Test knob: MXFP4EL_ROUTE=bucketer keeps the separate bucketer launch.
+  if (const char* env = std::getenv("MXFP4EL_ROUTE"))
+    if (std::strcmp(env, "bucketer") == 0) return false;
+  const StreamShape sh = stream_shape(I / 32);
+  const int64_t P = T * K;
+  return sh.rws > 0 && P > 0 && O > 0 && P <= kSelfMaxPairs && E <= kSelfMaxExperts &&
+         T <= kSelfMaxTokens;
+}
+
 UnitSplit gemv_unit_split(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
   UnitSplit sp{0, 0, 0};
   const StreamShape sh = stream_shape(I / 32);
@@ -606,9 +878,10 @@ cudaError_t launch_prep_tokens(const void* x, __half* x16, int* sigma, int64_t T
 }
 
 cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const int* sigma,
-                        const uint8_t* packed, const uint8_t* scales, const RoutePlan& plan,
-                        float* part, unsigned long long* status, int64_t T, int64_t E,
-                        int64_t I, int64_t O, int64_t K, cudaStream_t stream) {
+                        const void* sel, int index_dtype, const uint8_t* packed,
+                        const uint8_t* scales, const RoutePlan& plan, float* part,
+                        unsigned long long* status, int64_t T, int64_t E, int64_t I, int64_t O,
+                        int64_t K, cudaStream_t stream) {
   const int64_t G = I / 32;
   const StreamShape sh = stream_shape(G);
   if (sh.rws == 0) {
@@ -618,9 +891,17 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
     return launch_direct(static_cast<const float*>(x), packed, scales, plan, part, T, E, I,
                          O, K, stream);
   }
+  const bool self = gemv_self_route(T, E, I, O, K);
   StreamArgs a;
-  a.x = token_dtype == kTokenBF16 ? static_cast<const void*>(x16) : x;
-  a.sigma = token_dtype == kTokenBF16 ? sigma : nullptr;
+  a.x = token_dtype == kTokenBF16 && !self ? static_cast<const void*>(x16) : x;
+  a.sigma = token_dtype == kTokenBF16 && !self ? sigma : nullptr;
+  a.sel = sel;
+  a.sel_i64 = index_dtype == kIndexI64 ? 1 : 0;
+  a.T = (int)T;
+  a.E = (int)E;
+  a.P = (int)(T * K);
+  a.fixed_cost = MXFP4EL_GEMV_FIXED_COST;
+  a.route_bytes = self ? self_route_bytes(a.E, a.P, a.T) : 0u;
   a.packed = packed;
   a.scales = scales;
   a.scales_end = scales + (size_t)E * O * G;
@@ -639,20 +920,26 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
   if (gemv_unit_split(T, E, I, O, K).ctas == 0) a.plan.unit_begin = nullptr;
   a.packed_stage_bytes = (uint32_t)((size_t)a.rows_per_tile * G * 16);
   a.stage_bytes = (uint32_t)((stage_bytes_for(a.rows_per_tile, G) + 127) / 128 * 128);
-  a.stages = (int)std::min<size_t>(kMaxStages, kSmemBudget / a.stage_bytes);
-  const size_t smem = 2 * kMaxStages * sizeof(uint64_t) + (size_t)a.stages * a.stage_bytes;
+  a.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - a.route_bytes) / a.stage_bytes);
+  if (a.stages < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem =
+      2 * kMaxStages * sizeof(uint64_t) + a.route_bytes + (size_t)a.stages * a.stage_bytes;
   const int64_t bound_units = std::min<int64_t>(E, T * K) * a.row_tiles;
   if (bound_units > 0x7fffffff) return cudaErrorInvalidConfiguration;
-#define MXFP4EL_STREAM_CASES(ELEM)                                        \
-  switch (sh.rws) {                                                        \
-    case 8: return launch_stream<ELEM, 8>(a, smem, bound_units, stream);   \
-    case 4: return launch_stream<ELEM, 4>(a, smem, bound_units, stream);   \
-    case 2: return launch_stream<ELEM, 2>(a, smem, bound_units, stream);   \
-    default: return launch_stream<ELEM, 1>(a, smem, bound_units, stream);  \
+#define MXFP4EL_STREAM_CASES_SELF(ELEM, SELF)                                    \
+  switch (sh.rws) {                                                               \
+    case 8: return launch_stream<ELEM, 8, SELF>(a, smem, bound_units, stream);    \
+    case 4: return launch_stream<ELEM, 4, SELF>(a, smem, bound_units, stream);    \
+    case 2: return launch_stream<ELEM, 2, SELF>(a, smem, bound_units, stream);    \
+    default: return launch_stream<ELEM, 1, SELF>(a, smem, bound_units, stream);   \
   }
+#define MXFP4EL_STREAM_CASES(ELEM)                                     \
+  if (self) { MXFP4EL_STREAM_CASES_SELF(ELEM, true) }                   \
+  MXFP4EL_STREAM_CASES_SELF(ELEM, false)
   if (token_dtype == kTokenBF16) { MXFP4EL_STREAM_CASES(__half) }
   MXFP4EL_STREAM_CASES(float)
 #undef MXFP4EL_STREAM_CASES
+#undef MXFP4EL_STREAM_CASES_SELF
 }
 
 }  // namespace mxfp4el

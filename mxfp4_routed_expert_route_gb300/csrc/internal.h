@@ -112,9 +112,15 @@ int gemv_partial_columns(int64_t I);
 cudaError_t launch_prep_tokens(const void* x, __half* x16, int* sigma, int64_t T,
                                int64_t I, cudaStream_t stream);
 
+// True when the staged GEMV routes for itself: few enough pairs that each
+// CTA derives the routing lists and token scales it needs from the ids, and
+// neither the bucketer nor the token prep runs.
+bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K);
+
 cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16,
-                        const int* sigma, const uint8_t* packed,
-                        const uint8_t* scales, const RoutePlan& plan, float* part,
+                        const int* sigma, const void* sel, int index_dtype,
+                        const uint8_t* packed, const uint8_t* scales,
+                        const RoutePlan& plan, float* part,
                         unsigned long long* status, int64_t T, int64_t E,
                         int64_t I, int64_t O, int64_t K, cudaStream_t stream);
 

@@ -72,8 +72,12 @@ def test_workspace_size(lib):
     assert ws(1 << 40, 4, 64, 8, 2, 0) == bad       # too large
     n = ws(8, 128, 2880, 5760, 4, 1)
     assert n >= 8 * 4 * 5760 * 4 and n % 256 == 0
-    # bf16 tokens also keep a power-of-two scaled f16 copy of the tokens
-    assert n >= ws(8, 128, 2880, 5760, 4, 0) + 8 * 2880 * 2
+    # decode-size batches route and scale the tokens inside the GEMV: no
+    # f16 copy of the tokens, so bf16 and fp32 tokens need the same scratch
+    assert n == ws(8, 128, 2880, 5760, 4, 0)
+    # larger GEMV batches keep a power-of-two scaled f16 copy of the tokens
+    m = ws(400, 128, 2880, 5760, 4, 1)
+    assert m >= ws(400, 128, 2880, 5760, 4, 0) + 400 * 2880 * 2
 
 
 def test_argument_checks_return_before_gpu_work(lib):

@@ -304,3 +304,23 @@ def test_many_pairs_gemv_path_with_invalid_ids():
     rows = np.union1d(rows, [17, 2399])
     want, absm, bad = oracle_rows(wl, rows=rows, sel=sel)
     assert_parity(out[torch.from_numpy(rows).cuda()], want, absm, wl.dtype, "9600 pairs")
+
+
+@pytest.mark.parametrize("dtype,idx", [(torch.bfloat16, torch.int32), (torch.float32, torch.int64)])
+def test_self_routed_gemv_matches_bucketer_bitwise(monkeypatch, dtype, idx):
+    # Small batches on the GEMV route inside the GEMV's own CTAs; the
+    # bucketer path computes the same lists, split and token scales, so the
+    # two give the same bits. Some ids are out of range.
+    wl = workloads.make(24, 40, 5, 320, 150, dtype=dtype, seed=43)
+    sel = wl.sel.clone().to(idx)
+    sel[3, 1] = 40
+    sel[20, 4] = -2
+    device_errors()
+    a = run_gpu(wl, sel=sel)
+    assert device_errors() == 2
+    monkeypatch.setenv("MXFP4EL_ROUTE", "bucketer")
+    b = run_gpu(wl, sel=sel)
+    assert device_errors() == 2
+    assert torch.equal(a, b)
+    want, absm, _ = oracle_rows(wl, sel=sel)
+    assert_parity(a, want, absm, dtype, "self-routed")
