@@ -19,9 +19,12 @@
 //   * tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), accumulator in TMEM.
 //
 // Warp roles in a CTA of 24 warps (one CTA per SM, persistent over units
-// (expert, token block, 128-row tile)):
+// (expert, token block, 128-row tile), which CTAs take from a global counter
+// as they go, so the cost differences between units even out):
 //   warp 0      producer of scales and packed weights (lane 0; a deep ring
-//               of 4 KB stages covers HBM latency) and TMEM allocation
+//               of 4 KB stages covers HBM latency) and TMEM allocation; it
+//               takes each next unit from the counter and hands its index to
+//               the other roles through a small shared-memory ring
 //   warp 1      MMA issuer (the whole warp waits, one elected lane issues)
 //   warp 2      per-expert lists in shared memory at start
 //   warp 3      producer of token tiles (lane 0)
@@ -59,7 +62,11 @@ constexpr uint32_t kDCol = 0;               // two accumulators of kNMax columns
 constexpr uint32_t kACol = 2 * kNMax;       // kRing A buffers of 32 columns
 static_assert(kACol + kRing * 32 <= kTmemCols, "TMEM budget");
 constexpr int kMaxExpertsTc = 1024;         // per-expert lists kept in shared memory
+constexpr int kUnitRing = 4;                // unit indices handed from producer A
 constexpr int kDequantWarp0 = 4, kDequantWarps = 16, kTeamWarps = 4, kEpiWarp0 = 20;
+// Readers of the unit ring, one arrival each: producer B, the MMA warp, the
+// dequantizer warps and the epilogue warps.
+constexpr int kUnitReaders = 2 + kDequantWarps + (kTcThreads / 32 - kEpiWarp0);
 static_assert(kDequantWarps == kRing * kTeamWarps, "one team per A buffer");
 constexpr int kNumLoads = 5;                // token-box heights
 __host__ __device__ constexpr int load_rows(int l) {
@@ -92,6 +99,8 @@ struct __align__(8) TcShared {
   uint64_t d_full[2], d_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t drain;
+  uint64_t u_full[kUnitRing], u_empty[kUnitRing];
+  int unit_ring[kUnitRing];      // unit indices in the order this CTA takes them; -1 ends
   uint32_t tmem_base;
   int scale_off[2];              // per scale buffer: offset of the tile's first byte, or -1
   int num_units;
@@ -310,6 +319,19 @@ __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* 
   return true;
 }
 
+// The next unit index from the ring. kWarp: called by a whole warp, whose
+// lane 0 arrives once all lanes have read it; else by one thread. Returns
+// false if the wait gave up; *idx < 0 means no more units.
+template <bool kWarp>
+__device__ __forceinline__ bool pop_unit(TcShared& sh, RingPos& pu, int lane, int* idx) {
+  if (!mbar_wait(&sh.u_full[pu.idx], pu.phase)) return false;
+  *idx = sh.unit_ring[pu.idx];
+  if (kWarp) __syncwarp();
+  if (lane == 0) mbar_arrive(&sh.u_empty[pu.idx]);
+  pu.next(kUnitRing);
+  return true;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -340,6 +362,10 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       mbar_init(&sh.s_empty[b], kDequantWarps);
     }
     mbar_init(&sh.drain, 1);
+    for (int r = 0; r < kUnitRing; ++r) {
+      mbar_init(&sh.u_full[r], 1);
+      mbar_init(&sh.u_empty[r], kUnitReaders);
+    }
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -393,8 +419,17 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();     // weights: read once
       int it = 0, issued = 0;
-      RingPos pa;
-      for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
+      RingPos pa, pu;
+      int* counter = &a.plan.meta[kMetaUnitCounter];
+      int next = atomicAdd(counter, 1);                  // one unit ahead
+      for (;; ++it) {
+        const int idx = next < num_units ? next : -1;
+        if (!mbar_wait(&sh.u_empty[pu.idx], pu.phase ^ 1u)) { ok = false; break; }
+        sh.unit_ring[pu.idx] = idx;
+        mbar_arrive(&sh.u_full[pu.idx]);                 // releases the index
+        pu.next(kUnitRing);
+        if (idx < 0) break;
+        next = atomicAdd(counter, 1);
         const Unit w = unit_at(a, sh, idx);
         if (w.ntok <= 0) { --it; continue; }
         // The tile's scale bytes, by one bulk copy of the aligned span that
@@ -443,9 +478,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     // ------------------------------------------------------ producer B: tokens
     if (lane == 0) {
       const uint64_t pol = l2_evict_last_policy();      // tokens: reread per tile
-      int issued = 0;
-      RingPos pr;
-      for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x) {
+      int issued = 0, idx;
+      RingPos pr, pu;
+      while (ok) {
+        if (!pop_unit<false>(sh, pu, 0, &idx)) { ok = false; break; }
+        if (idx < 0) break;
         const Unit w = unit_at(a, sh, idx);
         if (w.ntok <= 0) continue;
         const uint32_t tx = (uint32_t)load_rows(w.load) * 128u;
@@ -473,9 +510,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     // ---------------------------------------------------------- MMA issuer
     // The whole warp runs the loop and waits; one elected lane (always the
     // same one, so its commits track its own MMAs) issues.
-    int it = 0;
-    RingPos pr;
-    for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
+    int it = 0, idx;
+    RingPos pr, pu;
+    for (; ok; ++it) {
+      if (!pop_unit<true>(sh, pu, lane, &idx)) { ok = false; break; }
+      if (idx < 0) break;
       const Unit w = unit_at(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int db = it & 1;
@@ -518,8 +557,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     const int m = 32 * q + lane;                     // weight row in the tile
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     TeamPos tp{team, team, 0u, 0u};                  // chunk `team` is the team's first
-    int it = 0, base = 0;
-    for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
+    int it = 0, base = 0, idx;
+    RingPos pu;
+    for (; ok; ++it) {
+      if (!pop_unit<true>(sh, pu, lane, &idx)) { ok = false; break; }
+      if (idx < 0) break;
       const Unit w = unit_at(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int sb = it & 1;
@@ -548,8 +590,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     const int q = warp & 3;
     const int m = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    int it = 0;
-    for (int idx = blockIdx.x; idx < num_units && ok; idx += gridDim.x, ++it) {
+    int it = 0, idx;
+    RingPos pu;
+    for (; ok; ++it) {
+      if (!pop_unit<true>(sh, pu, lane, &idx)) { ok = false; break; }
+      if (idx < 0) break;
       const Unit w = unit_at(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int db = it & 1;
@@ -591,6 +636,8 @@ gather_tokens_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restr
                      RoutePlan plan, int I, int K) {
   pdl_launch_dependents();
   pdl_wait();                    // the bucketer's lists are ready
+  // The tensor-core kernel after this one takes its units from this counter.
+  if (blockIdx.x == 0 && threadIdx.x == 0) plan.meta[kMetaUnitCounter] = 0;
   const int npairs = plan.meta[kMetaNumPairs];
   const int vec_per_row = I / 8;
   const int warps = blockDim.x / 32;

@@ -26,6 +26,7 @@ constexpr int kStatusWords = 4;
 // Slots of RoutePlan::meta.
 constexpr int kMetaNumActive = 0;   // experts with at least one valid pair
 constexpr int kMetaNumPairs = 1;    // valid pairs
+constexpr int kMetaUnitCounter = 2; // next unit of the tensor-core kernel (reset by the gather)
 constexpr int kMetaWords = 64;
 
 // Routing lists written by the bucketer, all in device memory.
