@@ -411,7 +411,16 @@ __device__ void self_route_lists(const StreamArgs& a, const SelfPlan& sp, bool b
 // group partial per lane, summed across the warp and stored as the column's
 // partial result. kScalesStaged: the tile's scale bytes are in shared memory
 // (else they are read from global memory).
-template <typename Elem, int RWS, int NTA, bool kScalesStaged>
+// The group partial times 2^(s - 127), exactly (one rounding, at the end):
+// first by f2 = 2^(s - c) in {1/2, 1, 2}, then by 2^(c - 127) with c = s
+// clamped to [1, 254], so no step leaves float32's normal range early.
+__device__ __forceinline__ float apply_scale(float v, uint32_t s) {
+  const uint32_t c = min(max(s, 1u), 254u);
+  return (v * __uint_as_float((s + 127u - c) << 23)) * __uint_as_float(c << 23);
+}
+
+// kFull: all RWS rows of the warp lie inside the tile (no per-row test).
+template <typename Elem, int RWS, int NTA, bool kScalesStaged, bool kFull>
 __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToken<Elem> (&xt)[NTA],
                                             const int (&pair)[NTA], const float (&unscale)[NTA],
                                             uint32_t sp_lane,
@@ -425,17 +434,20 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
   if (g_ok) {
+    uint32_t pa = sp_lane, sa = ss_lane;
+    const uint8_t* ga = gs_lane;
 #pragma unroll
     for (int r = 0; r < RWS; ++r) {
-      if (rbase + r < rows) {
+      if (kFull || rbase + r < rows) {
         uint32_t w[16];
-        decode_group(lds128(sp_lane + (uint32_t)r * prow), w);
-        const uint32_t sb = kScalesStaged ? lds_u8(ss_lane + (uint32_t)(r * G))
-                                          : (uint32_t)__ldg(gs_lane + (size_t)r * G);
-        const float2 f = e8m0_split(sb);
+        decode_group(lds128(pa), w);
+        const uint32_t sb = kScalesStaged ? lds_u8(sa) : (uint32_t)__ldg(ga);
 #pragma unroll
-        for (int j = 0; j < NTA; ++j) acc[r * NTA + j] = xt[j].dot(w) * f.x * f.y;
+        for (int j = 0; j < NTA; ++j) acc[r * NTA + j] = apply_scale(xt[j].dot(w), sb);
       }
+      pa += prow;
+      sa += (uint32_t)G;
+      ga += G;
     }
   }
   const float total = warp_reduce_scatter<V>(acc, lane);
@@ -443,7 +455,7 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
     const int idx = (lane >> (5 - L)) & (V - 1);
     if (idx < RWS * NTA) {
       const int r = idx / NTA, j = idx - (idx / NTA) * NTA;
-      if (rbase + r < rows) {
+      if (kFull || rbase + r < rows) {
         int pj = pair[0];
         float us = unscale[0];
 #pragma unroll
@@ -466,12 +478,15 @@ __device__ __forceinline__ void stream_pass_any(const StreamArgs& a,
                                                 uint32_t ss_lane, const uint8_t* gs_lane,
                                                 bool staged, int o0, int rows, int rbase, int c,
                                                 bool g_ok, int lane) {
-  if (staged)
-    stream_pass<Elem, RWS, NTA, true>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane, o0, rows,
-                                      rbase, c, g_ok, lane);
+  if (staged && rbase + RWS <= rows)
+    stream_pass<Elem, RWS, NTA, true, true>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane, o0,
+                                            rows, rbase, c, g_ok, lane);
+  else if (staged)
+    stream_pass<Elem, RWS, NTA, true, false>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane, o0,
+                                             rows, rbase, c, g_ok, lane);
   else
-    stream_pass<Elem, RWS, NTA, false>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane, o0,
-                                       rows, rbase, c, g_ok, lane);
+    stream_pass<Elem, RWS, NTA, false, false>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane,
+                                              o0, rows, rbase, c, g_ok, lane);
 }
 
 // Token operands (this lane's group) and pair ids of the pass starting at
