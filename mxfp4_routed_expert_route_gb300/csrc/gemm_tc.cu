@@ -33,8 +33,11 @@
 //               waits and stores interleave; in a team thread m (one weight
 //               row) decodes both groups of the chunk into 32 TMEM columns
 //   warps 20-23 epilogue: TMEM -> registers -> float32 partial results
-// Four A buffers and two accumulators in TMEM let dequantize, MMA and the
-// epilogue of consecutive chunks and units overlap. Every wait is bounded;
+// Four A buffers and two accumulators in TMEM, and a ring of four to six
+// token stages in shared memory (a stage is refilled only after its chunk's
+// MMAs finish, so its TMA latency needs several chunks of cover), let the
+// loads, dequantize, MMA and epilogue of consecutive chunks and units
+// overlap. Every wait is bounded;
 // a role whose wait gives up records it, stops, and the CTA still waits
 // (bounded) for its own copies and MMAs before freeing TMEM.
 #include <cuda.h>
@@ -53,7 +56,8 @@ constexpr int kBM = 128;                    // weight rows per tile
 constexpr int kBK = 64;                     // K elements per stage
 constexpr int kNMax = 192;                  // tokens per block
 constexpr int kStagesAMax = 16;            // packed-weight ring (from HBM)
-constexpr int kRing = 4;                   // token stages = TMEM A buffers
+constexpr int kRing = 4;                   // TMEM A buffers (one per dequantizer team)
+constexpr int kStagesBMax = 6;             // token stages, as shared memory allows
 constexpr uint32_t kStageB = kNMax * 128;   // token tile, 128 B per row
 constexpr uint32_t kStageA = kBM * 32;      // packed bytes, 32 B per row
 static_assert(kStageB % 1024 == 0 && kStageA % 1024 == 0, "stages keep 1024-byte alignment");
@@ -92,10 +96,10 @@ struct TcMaps {
 
 struct __align__(8) TcShared {
   uint64_t full_a[kStagesAMax], empty_a[kStagesAMax];
-  // Chunk ring r = chunk % kRing: token stage r and TMEM A buffer r.
-  uint64_t full_b[kRing];        // tokens landed (TMA)
+  // Chunk c uses token stage c % SB and TMEM A buffer c % kRing.
+  uint64_t full_b[kStagesBMax];  // tokens landed (TMA)
+  uint64_t done[kStagesBMax];    // the chunk's MMAs finished: its stage and A buffer free
   uint64_t a_full[kRing];        // A buffer written (dequantizers)
-  uint64_t done[kRing];          // the chunk's MMAs finished: stage and buffer free
   uint64_t d_full[2], d_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t drain;
@@ -280,7 +284,7 @@ struct TeamPos {
 // exchanged when bit 2 of m is set, so eight consecutive rows read eight
 // different bank groups. scale(g) returns the row's scale byte of group g.
 // Returns false if a wait gave up.
-template <typename ScaleFn>
+template <int SB, typename ScaleFn>
 __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* ring_a,
                                              int stages_a, uint32_t tmem, uint32_t lane_base,
                                              int team, int m, int lane, int base, int nk,
@@ -305,8 +309,12 @@ __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* 
     uint32_t v0[16], v1[16];
     dequant_group_bf16(pk0, s0, v0);
     dequant_group_bf16(pk1, s1, v1);
-    // The buffer is free once the MMAs of this team's previous chunk finished.
-    if (!mbar_wait(&sh.done[team], tp.buf_phase ^ 1u)) return false;
+    // The buffer is free once the MMAs of this team's previous chunk finished
+    // (chunk next - kRing, whose token stage is (next - kRing) % SB).
+    if (tp.next >= kRing) {
+      const int pc = tp.next - kRing;
+      if (!mbar_wait(&sh.done[pc % SB], (uint32_t)(pc / SB) & 1u)) return false;
+    }
     tc_fence_after_sync();
     tmem_st16(a_col, v0);
     tmem_st16(a_col + 16, v1);
@@ -332,13 +340,15 @@ __device__ __forceinline__ bool pop_unit(TcShared& sh, RingPos& pu, int lane, in
   return true;
 }
 
+template <int SB>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
+  static_assert(SB >= kRing && SB <= kStagesBMax, "token ring depth");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // Token stages need 1024-byte alignment (128-byte swizzle atoms).
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* ring_b = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  unsigned char* ring_a = ring_b + (size_t)kRing * kStageB;
+  unsigned char* ring_a = ring_b + (size_t)SB * kStageB;
   unsigned char* scale_buf = ring_a + (size_t)a.stages_a * kStageA;
   TcShared& sh = *reinterpret_cast<TcShared*>(scale_buf + 2 * a.scale_cap);
 
@@ -350,11 +360,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       mbar_init(&sh.full_a[s], 1);
       mbar_init(&sh.empty_a[s], kTeamWarps);
     }
-    for (int r = 0; r < kRing; ++r) {
+    for (int r = 0; r < SB; ++r) {
       mbar_init(&sh.full_b[r], 1);
-      mbar_init(&sh.a_full[r], kTeamWarps);
       mbar_init(&sh.done[r], 1);
     }
+    for (int r = 0; r < kRing; ++r) mbar_init(&sh.a_full[r], kTeamWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.d_full[b], 1);
       mbar_init(&sh.d_empty[b], 4);
@@ -494,14 +504,14 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
           mbar_arrive_expect_tx(&sh.full_b[pr.idx], tx);
           tma_load_2d(ring_b + (size_t)pr.idx * kStageB, &maps.b[w.load], kc * kBK, w.tok0,
                       &sh.full_b[pr.idx], pol);
-          pr.next(kRing);
+          pr.next(SB);
         }
       }
       if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
-      for (int k = 0; k < min(issued, kRing); ++k) {
+      for (int k = 0; k < min(issued, SB); ++k) {
         int idx = pr.idx - 1 - k;
         uint32_t ph = pr.phase;
-        if (idx < 0) { idx += kRing; ph ^= 1u; }
+        if (idx < 0) { idx += SB; ph ^= 1u; }
         if (!mbar_wait(&sh.full_b[idx], ph)) break;
       }
     }
@@ -511,7 +521,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     // The whole warp runs the loop and waits; one elected lane (always the
     // same one, so its commits track its own MMAs) issues.
     int it = 0, idx;
-    RingPos pr, pu;
+    RingPos pr, pb, pu;               // A buffer, token stage, unit ring
     for (; ok; ++it) {
       if (!pop_unit<true>(sh, pu, lane, &idx)) { ok = false; break; }
       if (idx < 0) break;
@@ -523,23 +533,24 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const uint32_t idesc = mma_idesc(kBM, w.nmma);
       const uint32_t d_tmem = tmem + kDCol + (uint32_t)db * kNMax;
       for (int kc = 0; kc < nk; ++kc) {
-        if (!mbar_wait(&sh.full_b[pr.idx], pr.phase) ||
+        if (!mbar_wait(&sh.full_b[pb.idx], pb.phase) ||
             !mbar_wait(&sh.a_full[pr.idx], pr.phase)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t b_addr = smem_addr(ring_b + (size_t)pr.idx * kStageB);
+        const uint32_t b_addr = smem_addr(ring_b + (size_t)pb.idx * kStageB);
         const uint32_t a_tmem = tmem + kACol + (uint32_t)pr.idx * 32;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             tc_mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
                       (kc > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&sh.done[pr.idx]);     // token stage and A buffer free once these finish
+          tc_commit(&sh.done[pb.idx]);     // token stage and A buffer free once these finish
         }
         __syncwarp();
         pr.next(kRing);
+        pb.next(SB);
       }
       if (!ok) break;
       if (elect_one()) tc_commit(&sh.d_full[db]);   // accumulator complete
@@ -572,12 +583,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       if (soff >= 0) {
         const unsigned char* srow =
             scale_buf + (size_t)sb * a.scale_cap + soff + (size_t)min(m, w.rows - 1) * G;
-        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk, tp,
-                          [&](int g) { return (uint32_t)srow[g]; });
+        ok = dequant_tile<SB>(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk,
+                              tp, [&](int g) { return (uint32_t)srow[g]; });
       } else {
         const uint8_t* grow = a.scales + ((size_t)w.e * O + w.m0 + min(m, w.rows - 1)) * G;
-        ok = dequant_tile(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk, tp,
-                          [&](int g) { return (uint32_t)__ldg(grow + g); });
+        ok = dequant_tile<SB>(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk,
+                              tp, [&](int g) { return (uint32_t)__ldg(grow + g); });
       }
       base += nk;
       if (!ok) break;
@@ -676,12 +687,31 @@ int num_sms_tc() {
   return cached[dev];
 }
 
-size_t tc_shared_bytes(int stages_a, uint32_t scale_cap) {
-  return 1024 + (size_t)kRing * kStageB + (size_t)stages_a * kStageA + 2 * (size_t)scale_cap +
+size_t tc_shared_bytes(int stages_a, int stages_b, uint32_t scale_cap) {
+  return 1024 + (size_t)stages_b * kStageB + (size_t)stages_a * kStageA + 2 * (size_t)scale_cap +
          sizeof(TcShared);
 }
 
 constexpr size_t kSmemLimit = 227 * 1024;
+
+template <int SB>
+cudaError_t launch_tc(const TcMaps& maps, const TcArgs& args, size_t smem, cudaStream_t stream) {
+  static std::mutex mu;
+  static size_t opted[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && opted[dev] < smem) {
+      cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel<SB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      opted[dev] = smem;
+    }
+  }
+  return launch_after_previous(gemm_tc_kernel<SB>, dim3((unsigned)num_sms_tc()), dim3(kTcThreads),
+                               smem, stream, maps, args);
+}
 
 }  // namespace
 
@@ -699,7 +729,7 @@ bool gemm_tc_supported(int64_t E, int64_t I, int64_t O) {
   if (G % 2 != 0) return false;                    // K chunks of 64
   if (E > kMaxExpertsTc || E * O > 0x7fffffff) return false;
   const uint32_t scale_cap = (uint32_t)((kBM * G + 31) / 16 * 16);
-  return tc_shared_bytes(4, scale_cap) <= kSmemLimit;
+  return tc_shared_bytes(kRing, kRing, scale_cap) <= kSmemLimit;
 }
 
 size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I) {
@@ -749,27 +779,21 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
   args.K = (int)K;
   args.mtiles = (int)((O + kBM - 1) / kBM);
   args.scale_cap = (uint32_t)((kBM * G + 31) / 16 * 16);
-  // As deep a packed-weight ring (HBM latency) as shared memory allows, a
-  // multiple of kRing so that each dequantizer team keeps to its own stages.
+  // As many token stages as fit next to 8 packed-weight stages (their
+  // refill latency is what the MMAs wait on), then as deep a packed-weight
+  // ring as shared memory allows, a multiple of kRing so that each
+  // dequantizer team keeps to its own stages.
+  int sb = kRing;
+  while (sb < kStagesBMax && tc_shared_bytes(2 * kRing, sb + 1, args.scale_cap) <= kSmemLimit) ++sb;
   int sa = kStagesAMax;
-  while (sa > kRing && tc_shared_bytes(sa, args.scale_cap) > kSmemLimit) sa -= kRing;
+  while (sa > kRing && tc_shared_bytes(sa, sb, args.scale_cap) > kSmemLimit) sa -= kRing;
   args.stages_a = sa;
-  const size_t smem = tc_shared_bytes(sa, args.scale_cap);
-  static std::mutex mu;
-  static size_t opted[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < 64 && opted[dev] < smem) {
-      cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (err != cudaSuccess) return err;
-      opted[dev] = smem;
-    }
+  const size_t smem = tc_shared_bytes(sa, sb, args.scale_cap);
+  switch (sb) {
+    case 6: return launch_tc<6>(maps, args, smem, stream);
+    case 5: return launch_tc<5>(maps, args, smem, stream);
+    default: return launch_tc<4>(maps, args, smem, stream);
   }
-  return launch_after_previous(gemm_tc_kernel, dim3((unsigned)num_sms_tc()), dim3(kTcThreads),
-                               smem, stream, maps, args);
 }
 
 }  // namespace mxfp4el
