@@ -248,6 +248,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Asks the TMA engine to bring `bytes` (a multiple of 16) at the 16-byte
+// aligned `src` into L2, without waiting.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // One contiguous global -> shared copy on the TMA engine; completion is
 // signalled on `bar` as `bytes` transaction bytes. Both addresses must be
 // 16-byte aligned and `bytes` a multiple of 16.

@@ -203,8 +203,10 @@ constexpr int kSelfMaxPairs = 1024;
 constexpr int kSelfMaxExperts = 2048;
 constexpr int kSelfMaxTokens = 1024;
 constexpr int kSigmaNeeded = -1000;            // token used by this CTA, scale pending
+constexpr int kSelfPrefetchTokens = 64;        // token rows prefetched into L2 at start
 
 struct SelfPlan {
+  int* ids;      // [P]     the expert ids, as loaded (-1 for ids outside [0, E))
   int* off;      // [E + 1] segment offsets
   int* run;      // [E]     next free position while placing pairs
   int* active;   // [E]     ascending active experts
@@ -215,14 +217,16 @@ struct SelfPlan {
 };
 
 __host__ __device__ inline uint32_t self_route_bytes(int E, int P, int T) {
-  return (uint32_t)(((size_t)(E + 1) + 2 * (size_t)E + (size_t)P + (size_t)T + 8 + 33) * 4 + 127) /
+  return (uint32_t)(((size_t)(E + 1) + 2 * (size_t)E + 2 * (size_t)P + (size_t)T + 8 + 33) * 4 +
+                    127) /
          128 * 128;
 }
 
 __device__ __forceinline__ SelfPlan self_plan(unsigned char* area, int E, int P, int T) {
   SelfPlan sp;
   int* w = reinterpret_cast<int*>(area);
-  sp.off = w;
+  sp.ids = w;
+  sp.off = sp.ids + P;
   sp.run = sp.off + (E + 1);
   sp.active = sp.run + E;
   sp.list = sp.active + E;
@@ -304,11 +308,13 @@ __device__ void self_route_plan(const StreamArgs& a, const SelfPlan& sp) {
   for (int e = tid; e < E; e += nthr) sp.off[e] = 0;
   for (int t = tid; t < T; t += nthr) sp.sigma[t] = 0;
   __syncthreads();
-  // Counts (order does not matter here).
+  // Counts (order does not matter here); the ids stay in shared memory.
   int bad = 0;
   for (int i = tid; i < P; i += nthr) {
     const long long e = load_id(a, i);
-    if (e >= 0 && e < E) atomicAdd(&sp.off[e], 1);
+    const bool valid = e >= 0 && e < E;
+    sp.ids[i] = valid ? (int)e : -1;
+    if (valid) atomicAdd(&sp.off[e], 1);
     else ++bad;
   }
 #pragma unroll
@@ -365,9 +371,9 @@ __device__ void self_route_lists(const StreamArgs& a, const SelfPlan& sp, bool b
     const unsigned below = (1u << lane) - 1u;
     for (int base = 0; base < P; base += 32) {
       const int i = base + lane;
-      const long long e = i < P ? load_id(a, i) : -1;
+      const int e = i < P ? sp.ids[i] : -1;
       const bool mine = e >= e_lo && e <= e_hi;
-      const unsigned peers = __match_any_sync(kFullMask, mine ? (int)e : -1);
+      const unsigned peers = __match_any_sync(kFullMask, mine ? e : -1);
       if (mine) {
         sp.list[sp.run[e] + __popc(peers & below)] = i;
         sp.sigma[i / a.K] = kSigmaNeeded;
@@ -542,6 +548,13 @@ gemv_stream_kernel(const StreamArgs a) {
   // Otherwise: the bucketer's lists and the prepared tokens are ready.
   pdl_wait();
   if constexpr (kSelf) {
+    // Few tokens: start bringing their rows into L2 now; the CTA reads them
+    // (scale, then operands) only after its routing plan is ready.
+    if (warp == kConsumerWarps && a.T <= kSelfPrefetchTokens)
+      for (int t = lane; t < a.T; t += 32)
+        prefetch_l2(static_cast<const unsigned char*>(a.x) +
+                        (size_t)t * a.I * (sizeof(Elem) == 2 ? 2 : 4),
+                    (uint32_t)a.I * (sizeof(Elem) == 2 ? 2u : 4u));
     self_route_plan(a, rp);                // ends with a block barrier
     if (warp != kConsumerWarps) self_route_lists(a, rp, sizeof(Elem) == 2);
   } else {
@@ -635,6 +648,14 @@ gemv_stream_kernel(const StreamArgs a) {
 #pragma unroll
   for (int j = 0; j < NT; ++j) { pair0[j] = 0; unscale0[j] = 1.f; }
 
+  // Self-routed: the first unit's expert is known from the plan, so its
+  // tokens load while the first stage is still on its way.
+  if (kSelf && working && ubeg < uend) {
+    cached_e = rp.active[ubeg / a.row_tiles];
+    seg_beg = rp.off[cached_e];
+    seg_end = rp.off[cached_e + 1];
+    load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, unscale0, seg_beg, seg_end, g);
+  }
   int it = 0;
   for (int unit = ubeg; unit < uend; ++unit, ++it) {
     const int st = it % a.stages;
