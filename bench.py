@@ -128,6 +128,25 @@ def ncu_traffic(kernel, workload):
     return d.get("dram_bytes_per_launch")
 
 
+# ---------------------------------------------------------- across ranks ----
+def max_over_ranks(seconds, device, world):
+    """The slowest rank's time: every rank passes its own and gets the max
+    (all-reduce MAX on `device`, which is the GPU for NCCL and the CPU for
+    gloo)."""
+    import torch
+    t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step, steps, world, t_max_s):
+    """Units all ranks processed per second: every rank runs the same
+    replica (weak scaling), timed by the slowest rank."""
+    return world * units_per_rank_step * steps / t_max_s
+
+
 # --------------------------------------------------------------- clocks ----
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -343,11 +362,7 @@ def run_ours(args, rank, world):
     lib.mxfp4el_set_stage_events(_native.STAGE_LINEAR, None, None)
     lin_ms = [a.elapsed_time(b) for a, b in lin]
 
-    total_s = sum(step_ms) / 1e3
-    t_local = torch.tensor([total_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
-    t_max = float(t_local.item())
+    t_max = max_over_ranks(sum(step_ms) / 1e3, dev, world)
 
     # End to end through the public API: pinned host inputs in, result out.
     x_h = wl.x.pin_memory()
@@ -375,10 +390,7 @@ def run_ours(args, rank, world):
         e2e_step()
         e2e_ev[i][1].record(stream)
     barrier()
-    e2e_s = sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3
-    e2e_t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_max = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3, dev, world)
     h2d = sum(t.numel() * t.element_size() for t in (x_h, sel_h, p_h, ys_h))
     d2h = out_h.numel() * out_h.element_size()
 
@@ -393,8 +405,8 @@ def run_ours(args, rank, world):
     t_roof = max(bytes_step / (peaks["hbm_gbs"] * 1e9),
                  flops_step / (peaks["bf16_tflops"] * 1e12))
     hbm_bound = workload_is_hbm_bound(wl, U, peaks)
-    gbps = world * bytes_step * K / t_max / 1e9
-    tflops = world * flops_step * K / t_max / 1e12
+    gbps = whole_job_rate(bytes_step, K, world, t_max) / 1e9
+    tflops = whole_job_rate(flops_step, K, world, t_max) / 1e12
     value, unit = (gbps, "GB/s") if hbm_bound else (tflops, "TFLOP/s")
     ms_step = t_max / K * 1e3
     lin_mean_s = sum(lin_ms) / len(lin_ms) / 1e3
@@ -420,7 +432,7 @@ def run_ours(args, rank, world):
                     "peak_source": f"hbm_gbs of {peaks_src}",
                     "bytes_per_launch": lin_bytes, "launch_us": lin_mean_s * 1e6}
     roofline["traffic"] = ncu_traffic(kernel, wl.name)
-    e2e_v = world * (bytes_step if hbm_bound else flops_step) * K / float(e2e_t.item())
+    e2e_v = whole_job_rate(bytes_step if hbm_bound else flops_step, K, world, e2e_max)
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True,
@@ -441,7 +453,7 @@ def run_ours(args, rank, world):
         "roofline": roofline,
         "e2e": {"value": e2e_v / (1e9 if hbm_bound else 1e12), "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": float(e2e_t.item()) / K * 1e3},
+                "ms_per_step": e2e_max / K * 1e3},
         "gpu_launches": int(launches),
         "clocks": clocks,
         "wall_s": wall,
