@@ -32,7 +32,8 @@
 //               and takes chunks t, t+4, t+8, ..., so the teams' decode,
 //               waits and stores interleave; in a team thread m (one weight
 //               row) decodes both groups of the chunk into 32 TMEM columns
-//   warps 20-23 epilogue: TMEM -> registers -> float32 partial results
+//   warps 20-23 epilogue: TMEM -> registers -> shared memory (transposed) ->
+//               float32 partial results, four consecutive rows per store
 // Four A buffers and two accumulators in TMEM, and a ring of four to six
 // token stages in shared memory (a stage is refilled only after its chunk's
 // MMAs finish, so its TMA latency needs several chunks of cover), let the
@@ -65,7 +66,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 0;               // two accumulators of kNMax columns
 constexpr uint32_t kACol = 2 * kNMax;       // kRing A buffers of 32 columns
 static_assert(kACol + kRing * 32 <= kTmemCols, "TMEM budget");
-constexpr int kMaxExpertsTc = 1024;         // per-expert lists kept in shared memory
+constexpr int kMaxExpertsTc = 512;          // per-expert lists kept in shared memory
+constexpr uint32_t kEpiStage = 16 * 32 * 4; // epilogue staging per warp: 16 columns x 32 rows
 constexpr int kUnitRing = 4;                // unit indices handed from producer A
 constexpr int kDequantWarp0 = 4, kDequantWarps = 16, kTeamWarps = 4, kEpiWarp0 = 20;
 // Readers of the unit ring, one arrival each: producer B, the MMA warp, the
@@ -94,7 +96,7 @@ struct TcMaps {
   CUtensorMap b[kNumLoads];      // grouped tokens bf16 [P, I], box {64, rows}, 128B swizzle
 };
 
-struct __align__(8) TcShared {
+struct __align__(16) TcShared {
   uint64_t full_a[kStagesAMax], empty_a[kStagesAMax];
   // Chunk c uses token stage c % SB and TMEM A buffer c % kRing.
   uint64_t full_b[kStagesBMax];  // tokens landed (TMA)
@@ -351,6 +353,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   unsigned char* ring_a = ring_b + (size_t)SB * kStageB;
   unsigned char* scale_buf = ring_a + (size_t)a.stages_a * kStageA;
   TcShared& sh = *reinterpret_cast<TcShared*>(scale_buf + 2 * a.scale_cap);
+  float* epi_stage = reinterpret_cast<float*>(&sh + 1);   // 16-byte aligned (TcShared is)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
@@ -599,6 +602,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    float* stage = epi_stage + (size_t)(warp - kEpiWarp0) * (kEpiStage / 4);
     const int m = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     int it = 0, idx;
@@ -613,6 +617,13 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       tc_fence_after_sync();
       const bool row_ok = m < w.rows;
       float* out_col = a.part + w.m0 + m;
+      // Four consecutive rows per store: this warp's 32 rows x 16 columns go
+      // through shared memory (column-major), then lane (c, j) of each round
+      // stores rows 4j..4j+3 of column c. Needs whole 4-row groups inside
+      // the tile and 16-byte aligned part rows.
+      const bool vec = (O & 3) == 0 && 32 * q + 32 <= w.rows;
+      const int jr = lane & 7;                       // 4-row group of the lane
+      float* part_rows = a.part + w.m0 + 32 * q + 4 * jr;
       for (int c0 = 0; c0 < w.nmma; c0 += 16) {
         // Pair ids of these 16 columns: one load per lane, then broadcast.
         const int my_pair = (lane < 16 && c0 + lane < w.ntok)
@@ -620,10 +631,25 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         uint32_t v[16];
         tmem_ld16(tmem + lane_base + kDCol + (uint32_t)db * kNMax + (uint32_t)c0, v);
         tmem_wait_ld();
+        if (vec) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int pair = __shfl_sync(kFullMask, my_pair, i);
-          if (row_ok && c0 + i < w.ntok) out_col[(size_t)pair * O] = __uint_as_float(v[i]);
+          for (int i = 0; i < 16; ++i) stage[i * 32 + lane] = __uint_as_float(v[i]);
+          __syncwarp();
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int c = 4 * r + (lane >> 3);
+            const int pair = __shfl_sync(kFullMask, my_pair, c);
+            if (c0 + c < w.ntok)
+              *reinterpret_cast<float4*>(part_rows + (size_t)pair * O) =
+                  *reinterpret_cast<const float4*>(stage + c * 32 + 4 * jr);
+          }
+          __syncwarp();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int pair = __shfl_sync(kFullMask, my_pair, i);
+            if (row_ok && c0 + i < w.ntok) out_col[(size_t)pair * O] = __uint_as_float(v[i]);
+          }
         }
       }
       tc_fence_before_sync();
@@ -689,7 +715,7 @@ int num_sms_tc() {
 
 size_t tc_shared_bytes(int stages_a, int stages_b, uint32_t scale_cap) {
   return 1024 + (size_t)stages_b * kStageB + (size_t)stages_a * kStageA + 2 * (size_t)scale_cap +
-         sizeof(TcShared);
+         sizeof(TcShared) + (kTcThreads / 32 - kEpiWarp0) * (size_t)kEpiStage;
 }
 
 constexpr size_t kSmemLimit = 227 * 1024;
