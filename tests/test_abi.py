@@ -117,3 +117,16 @@ def test_product_path_has_no_oracle_reference():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "liboracle" not in text, f
+
+
+def test_linear_path_choice(lib):
+    # Tensor cores for bf16 tokens once experts average 16 tokens (and the
+    # shapes fit the kernel), the GEMV otherwise; no GPU needed to ask.
+    from mxfp4_routed_expert_route_gb300 import _native as n
+    path = lib.mxfp4el_linear_path
+    assert path(8, 128, 2880, 5760, 4, n.DTYPE_BF16) == n.PATH_GEMV        # decode
+    assert path(4096, 128, 2880, 5760, 4, n.DTYPE_BF16) == n.PATH_GEMM     # prefill
+    assert path(4096, 128, 2880, 5760, 4, n.DTYPE_F32) == n.PATH_GEMV      # fp32 tokens
+    assert path(4096, 128, 2848, 5760, 4, n.DTYPE_BF16) == n.PATH_GEMV     # G odd
+    assert path(640, 512, 64, 48, 16, n.DTYPE_BF16) == n.PATH_GEMM
+    assert path(640, 600, 64, 48, 16, n.DTYPE_BF16) == n.PATH_GEMV         # > 512 experts

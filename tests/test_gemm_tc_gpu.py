@@ -85,3 +85,20 @@ def test_gemm_and_gemv_agree(monkeypatch):
     want, absm, _ = oracle_rows(wl)
     assert_parity(a, want, absm, wl.dtype, "gemm")
     assert_parity(b, want, absm, wl.dtype, "gemv")
+
+
+def test_more_experts_than_the_tensor_core_lists_take_the_gemv(monkeypatch):
+    # The tensor-core kernel keeps per-expert lists for up to 512 experts in
+    # shared memory; beyond that a call runs on the GEMV, even when experts
+    # average many tokens, and still matches the oracle.
+    from mxfp4_routed_expert_route_gb300 import _native
+    monkeypatch.delenv("MXFP4EL_PATH", raising=False)
+    T, E, K, I, O = 640, 600, 16, 64, 48
+    lib = _native.load()
+    assert lib.mxfp4el_linear_path(T, E, I, O, K, _native.DTYPE_BF16) == _native.PATH_GEMV
+    assert lib.mxfp4el_linear_path(T, 512, I, O, K, _native.DTYPE_BF16) == _native.PATH_GEMM
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, seed=44)
+    out = run_gpu(wl)
+    rows = np.arange(0, T, 37)
+    want, absm, _ = oracle_rows(wl, rows=rows)
+    assert_parity(out[torch.from_numpy(rows).cuda()], want, absm, wl.dtype, "E=600")
