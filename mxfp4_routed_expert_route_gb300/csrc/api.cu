@@ -120,7 +120,7 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
     const bool prep = !gemm && !self && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
     const bool prep_in_route = prep && prep_fits_route(T, I);
     TokenPrep tp = {prep_in_route ? x : nullptr, ws.x16, ws.sigma, I};
-    const UnitSplit split = gemm ? UnitSplit{0, 0, 0} : gemv_unit_split(T, E, I, O, K);
+    const UnitSplit split = gemm ? UnitSplit{0, 0, 0, 1000} : gemv_unit_split(T, E, I, O, K);
     mark(MXFP4EL_STAGE_ROUTE, true, stream);
     err = cudaSuccess;
     if (!self)

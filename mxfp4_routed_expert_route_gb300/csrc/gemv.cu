@@ -54,6 +54,13 @@ constexpr int kDirectWarps = kDirectThreads / 32;
 constexpr size_t kMaxStageBytes = 64 * 1024;
 constexpr size_t kSmemBudget = 220 * 1024;
 constexpr int kMaxStages = 8;
+// Dynamic shared memory: the stage barriers, the scale-factor table, then
+// (self-routed mode) the routing area and the stages.
+constexpr uint32_t kScaleLutOffset = 2 * kMaxStages * sizeof(uint64_t);
+constexpr int kScaleLutEntries = 512;
+constexpr uint32_t kScaleLutBytes = kScaleLutEntries * sizeof(float2);
+constexpr uint32_t kStreamHeadBytes = kScaleLutOffset + kScaleLutBytes;
+static_assert(kStreamHeadBytes % 128 == 0, "the routing area and stages stay 128-byte aligned");
 
 template <int V> struct Log2 { static constexpr int value = 1 + Log2<V / 2>::value; };
 template <> struct Log2<1> { static constexpr int value = 0; };
@@ -176,6 +183,11 @@ struct StreamArgs {
   int T, E, P;                   // P = T * K
   int fixed_cost;                // split cost of a unit beyond its tokens
   uint32_t route_bytes;          // bytes of the routing area in shared memory
+  // Dynamic tail: the contiguous per-CTA ranges cover static_permille/1000
+  // of the cost; the units after them form a pool that CTAs claim one at a
+  // time from *pool once their own range is done.
+  int static_permille;
+  int* pool;                     // claim counter (workspace), reset by CTA 0
 };
 
 // Written by the producer into each stage before its copies are issued.
@@ -202,6 +214,8 @@ template <> struct Pow2Ceil<1> { static constexpr int value = 1; };
 constexpr int kSelfMaxPairs = 1024;
 constexpr int kSelfMaxExperts = 2048;
 constexpr int kSelfMaxTokens = 1024;
+static_assert(kSelfMaxExperts < 4096 && kSelfMaxPairs < (1 << 18),
+              "the plan scans pairs and active experts packed in one int");
 constexpr int kSigmaNeeded = -1000;            // token used by this CTA, scale pending
 constexpr int kSelfPrefetchTokens = 64;        // token rows prefetched into L2 at start
 
@@ -212,7 +226,8 @@ struct SelfPlan {
   int* active;   // [E]     ascending active experts
   int* list;     // [P]     pair ids of this CTA's experts, at their global positions
   int* sigma;    // [T]     token scale exponents (bf16 tokens)
-  int* misc;     // [8]     0: active experts, 1: first unit, 2: end unit, 3: pairs
+  int* misc;     // [8]     0: active experts, 1: first unit, 2: end unit, 3: pairs,
+                 //         4: first unit of the shared pool
   int* wbuf;     // [33]    scan scratch
 };
 
@@ -330,9 +345,12 @@ __device__ void self_route_plan(const StreamArgs& a, const SelfPlan& sp) {
     my_pairs += sp.off[e];
     my_active += sp.off[e] > 0 ? 1 : 0;
   }
-  int total_pairs, total_active;
-  int off = block_scan(my_pairs, sp.wbuf, &total_pairs);
-  int act = block_scan(my_active, sp.wbuf, &total_active);
+  // One scan of both sums: pairs (at most kSelfMaxPairs) from bit 12 up,
+  // active experts (at most kSelfMaxExperts < 4096) below.
+  int total;
+  const int packed = block_scan((my_pairs << 12) | my_active, sp.wbuf, &total);
+  int off = packed >> 12, act = packed & 0xfff;
+  const int total_pairs = total >> 12, total_active = total & 0xfff;
   for (int e = e0; e < e1; ++e) {
     const int c = sp.off[e];
     sp.off[e] = off;
@@ -345,34 +363,51 @@ __device__ void self_route_plan(const StreamArgs& a, const SelfPlan& sp) {
     sp.misc[3] = total_pairs;
   }
   __syncthreads();
-  // This CTA's unit range.
-  if (tid == 0) {
-    sp.misc[1] = split_begin(sp, total_active, total_pairs, a.row_tiles, a.fixed_cost,
-                             blockIdx.x, gridDim.x);
-    sp.misc[2] = split_begin(sp, total_active, total_pairs, a.row_tiles, a.fixed_cost,
-                             blockIdx.x + 1, gridDim.x);
+  // This CTA's static range and the start of the shared pool, one boundary
+  // per warp: boundary b of n sits at b * static_permille / (1000 n) of the
+  // cost.
+  if (lane == 0 && tid < 96) {
+    const int w = tid >> 5;
+    const int64_t b = w == 0 ? blockIdx.x : w == 1 ? blockIdx.x + 1 : gridDim.x;
+    sp.misc[w == 2 ? 4 : 1 + w] =
+        split_begin(sp, total_active, total_pairs, a.row_tiles, a.fixed_cost,
+                    b * a.static_permille, (int64_t)gridDim.x * 1000);
   }
   __syncthreads();
 }
 
 // The rest, by the consumer warps while the producer starts its copies:
-// the pair ids of this CTA's experts and the scales of their tokens.
+// the pair ids of the experts this CTA may meet (its own range and the
+// shared pool) and the scales of their tokens.
 __device__ void self_route_lists(const StreamArgs& a, const SelfPlan& sp, bool bf16_tokens) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int P = a.P, T = a.T;
-  const int ubeg = sp.misc[1], uend = sp.misc[2];
-  if (ubeg >= uend) return;
-  // Pair ids of this CTA's experts (active slots ubeg/rt .. (uend-1)/rt,
-  // i.e. expert ids e_lo .. e_hi), placed in (token, slot) order by one warp.
-  const int e_lo = sp.active[ubeg / a.row_tiles], e_hi = sp.active[(uend - 1) / a.row_tiles];
+  const int num_units = sp.misc[0] * a.row_tiles;
+  const int ubeg = min(sp.misc[1], num_units), uend = min(sp.misc[2], num_units);
+  const int pool_begin = min(sp.misc[4], num_units);
+  if (ubeg >= uend && pool_begin >= num_units) return;
+  // Expert ids e_lo .. e_hi (active slots ubeg/rt .. (uend-1)/rt) and, for
+  // the pool, p_lo .. the last active expert (p_lo >= e_hi: the static
+  // ranges lie before the pool); an empty range is 0 .. -1.
+  int e_lo = 0, e_hi = -1, p_lo = 0, p_hi = -1;
+  if (ubeg < uend) {
+    e_lo = sp.active[ubeg / a.row_tiles];
+    e_hi = sp.active[(uend - 1) / a.row_tiles];
+  }
+  if (pool_begin < num_units) {
+    p_lo = sp.active[pool_begin / a.row_tiles];
+    p_hi = sp.active[sp.misc[0] - 1];
+  }
+  // Their pair ids, placed in (token, slot) order by one warp.
   if (warp == 0) {
     for (int e = e_lo + lane; e <= e_hi; e += 32) sp.run[e] = sp.off[e];
+    for (int e = max(p_lo, e_hi + 1) + lane; e <= p_hi; e += 32) sp.run[e] = sp.off[e];
     __syncwarp();
     const unsigned below = (1u << lane) - 1u;
     for (int base = 0; base < P; base += 32) {
       const int i = base + lane;
       const int e = i < P ? sp.ids[i] : -1;
-      const bool mine = e >= e_lo && e <= e_hi;
+      const bool mine = (e >= e_lo && e <= e_hi) || (e >= p_lo && e <= p_hi);
       const unsigned peers = __match_any_sync(kFullMask, mine ? e : -1);
       if (mine) {
         sp.list[sp.run[e] + __popc(peers & below)] = i;
@@ -417,18 +452,54 @@ __device__ void self_route_lists(const StreamArgs& a, const SelfPlan& sp, bool b
 // group partial per lane, summed across the warp and stored as the column's
 // partial result. kScalesStaged: the tile's scale bytes are in shared memory
 // (else they are read from global memory).
-// The group partial times 2^(s - 127), exactly (one rounding, at the end):
-// first by f2 = 2^(s - c) in {1/2, 1, 2}, then by 2^(c - 127) with c = s
-// clamped to [1, 254], so no step leaves float32's normal range early.
-__device__ __forceinline__ float apply_scale(float v, uint32_t s) {
-  const uint32_t c = min(max(s, 1u), 254u);
-  return (v * __uint_as_float((s + 127u - c) << 23)) * __uint_as_float(c << 23);
+// The group partial v times 2^(s - 127 - sigma_t), exactly: the weight
+// scale and the token's own power of two (bf16 tokens are pre-scaled by
+// 2^sigma_t into f16; sigma_t = 0 for fp32 tokens) in one factor, so that no
+// intermediate leaves float32's range when the result does not. The factor
+// is a pair (f1, f2), applied as (v * f1) * f2, from a table in shared memory
+// indexed by s + 126 - sigma_t (sigma_t is in [-119, 126], so 0..500);
+// entry i stands for 2^e with e = i - 253:
+//   -149 <= e <= 127: (2^e, 1)          one multiply by a float32 (2^e is
+//                                       subnormal below -126): one rounding;
+//   e > 127:          (2^127, 2^(e-127)) v * 2^127 is exact or overflows
+//                                       only when v * 2^e does;
+//   -165 <= e < -149: (2^-100, 2^(e+100)) for f16-token partials, which are
+//                                       0 or at least 2^-24 in magnitude, so
+//                                       v * 2^-100 is exact;
+//   e < -165:         (0, 1)            |v| < 2^16 there, so v * 2^e rounds
+//                                       to zero.
+// fp32 tokens only reach -127 <= e <= 128.
+__device__ __forceinline__ const float2* scale_lut() {
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
+  return reinterpret_cast<const float2*>(dyn_smem + kScaleLutOffset);
+}
+__device__ __forceinline__ float pow2f(int e) {          // exact 2^e, -149 <= e <= 127
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23)
+                   : __uint_as_float(1u << (e + 149));
+}
+__device__ __forceinline__ void fill_scale_lut(float2* lut) {
+  for (int i = threadIdx.x; i < kScaleLutEntries; i += blockDim.x) {
+    const int e = i - 253;
+    float2 f;
+    if (e > 254) f = make_float2(pow2f(127), __uint_as_float(0x7f800000u));   // never indexed
+    else if (e > 127) f = make_float2(pow2f(127), pow2f(e - 127));
+    else if (e >= -149) f = make_float2(pow2f(e), 1.f);
+    else if (e >= -165) f = make_float2(pow2f(-100), pow2f(e + 100));
+    else f = make_float2(0.f, 1.f);
+    lut[i] = f;
+  }
+}
+// Table offset of a token's factors.
+__device__ __forceinline__ int scale_offset(int sigma) { return 126 - sigma; }
+__device__ __forceinline__ float apply_scale(float v, uint32_t s, const float2* lut_t) {
+  const float2 f = lut_t[s];
+  return (v * f.x) * f.y;
 }
 
 // kFull: all RWS rows of the warp lie inside the tile (no per-row test).
 template <typename Elem, int RWS, int NTA, bool kScalesStaged, bool kFull>
 __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToken<Elem> (&xt)[NTA],
-                                            const int (&pair)[NTA], const float (&unscale)[NTA],
+                                            const int (&pair)[NTA], const int (&soff)[NTA],
                                             uint32_t sp_lane,
                                             uint32_t ss_lane, const uint8_t* gs_lane, int o0,
                                             int rows, int rbase, int c, bool g_ok, int lane) {
@@ -436,6 +507,7 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
   constexpr int L = Log2<V>::value;
   const int G = a.G, O = a.O;
   const uint32_t prow = (uint32_t)G * 16u;      // bytes per packed row
+  const float2* lut = scale_lut();
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
@@ -449,7 +521,7 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
         decode_group(lds128(pa), w);
         const uint32_t sb = kScalesStaged ? lds_u8(sa) : (uint32_t)__ldg(ga);
 #pragma unroll
-        for (int j = 0; j < NTA; ++j) acc[r * NTA + j] = apply_scale(xt[j].dot(w), sb);
+        for (int j = 0; j < NTA; ++j) acc[r * NTA + j] = apply_scale(xt[j].dot(w), sb, lut + soff[j]);
       }
       pa += prow;
       sa += (uint32_t)G;
@@ -463,13 +535,9 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
       const int r = idx / NTA, j = idx - (idx / NTA) * NTA;
       if (kFull || rbase + r < rows) {
         int pj = pair[0];
-        float us = unscale[0];
 #pragma unroll
-        for (int q = 1; q < NTA; ++q) {
-          pj = (j == q) ? pair[q] : pj;
-          us = (j == q) ? unscale[q] : us;
-        }
-        a.part[((size_t)pj * a.ncol + c) * O + o0 + rbase + r] = total * us;
+        for (int q = 1; q < NTA; ++q) pj = (j == q) ? pair[q] : pj;
+        a.part[((size_t)pj * a.ncol + c) * O + o0 + rbase + r] = total;
       }
     }
   }
@@ -480,29 +548,29 @@ template <typename Elem, int RWS, int NTA>
 __device__ __forceinline__ void stream_pass_any(const StreamArgs& a,
                                                 const GroupToken<Elem> (&xt)[NTA],
                                                 const int (&pair)[NTA],
-                                                const float (&unscale)[NTA], uint32_t sp_lane,
+                                                const int (&soff)[NTA], uint32_t sp_lane,
                                                 uint32_t ss_lane, const uint8_t* gs_lane,
                                                 bool staged, int o0, int rows, int rbase, int c,
                                                 bool g_ok, int lane) {
   if (staged && rbase + RWS <= rows)
-    stream_pass<Elem, RWS, NTA, true, true>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane, o0,
+    stream_pass<Elem, RWS, NTA, true, true>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane, o0,
                                             rows, rbase, c, g_ok, lane);
   else if (staged)
-    stream_pass<Elem, RWS, NTA, true, false>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane, o0,
+    stream_pass<Elem, RWS, NTA, true, false>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane, o0,
                                              rows, rbase, c, g_ok, lane);
   else
-    stream_pass<Elem, RWS, NTA, false, false>(a, xt, pair, unscale, sp_lane, ss_lane, gs_lane,
+    stream_pass<Elem, RWS, NTA, false, false>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane,
                                               o0, rows, rbase, c, g_ok, lane);
 }
 
 // Token operands (this lane's group) and pair ids of the pass starting at
-// position `base` of an expert's segment [base, seg_end).
-// Also the factor that undoes each token's power-of-two scaling (1 for fp32
+// position `base` of an expert's segment [base, seg_end), and each token's
+// offset into the scale-factor table (from its power of two; 0 for fp32
 // tokens).
 template <typename Elem, int NT, bool kSelf>
 __device__ __forceinline__ void load_pass(const StreamArgs& a, const SelfPlan& sp,
                                           GroupToken<Elem> (&xt)[NT], int (&pair)[NT],
-                                          float (&unscale)[NT], int base, int seg_end, int g) {
+                                          int (&soff)[NT], int base, int seg_end, int g) {
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     const int pos = base + min(j, seg_end - base - 1);
@@ -514,11 +582,10 @@ __device__ __forceinline__ void load_pass(const StreamArgs& a, const SelfPlan& s
       if (g < a.G)
         xt[j].load_scaled(static_cast<const __nv_bfloat16*>(a.x) + (size_t)t * a.I, g,
                           __uint_as_float((uint32_t)(sg + 127) << 23));
-      unscale[j] = __uint_as_float((uint32_t)(127 - sg) << 23);
+      soff[j] = scale_offset(sg);
     } else {
       if (g < a.G) xt[j].load(static_cast<const Elem*>(a.x) + (size_t)t * a.I, g);
-      unscale[j] =
-          a.sigma != nullptr ? __uint_as_float((uint32_t)(127 - a.sigma[t]) << 23) : 1.f;
+      soff[j] = scale_offset(a.sigma != nullptr ? a.sigma[t] : 0);
     }
   }
 }
@@ -530,12 +597,13 @@ gemv_stream_kernel(const StreamArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  unsigned char* route_area = smem + 2 * kMaxStages * sizeof(uint64_t);
+  unsigned char* route_area = smem + kStreamHeadBytes;
   unsigned char* stage_base = route_area + (kSelf ? a.route_bytes : 0u);
   const SelfPlan rp = self_plan(route_area, a.E, a.P, a.T);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
+  fill_scale_lut(reinterpret_cast<float2*>(smem + kScaleLutOffset));   // read after a barrier
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -547,6 +615,12 @@ gemv_stream_kernel(const StreamArgs a) {
   // tokens only after whatever ran before it on the stream has finished.
   // Otherwise: the bucketer's lists and the prepared tokens are ready.
   pdl_wait();
+  // The pool counter starts at zero for this launch. A CTA that claims
+  // before this reset gets a stale value: one past the pool ends its claims,
+  // one inside the pool repeats a unit (the same values written twice). CTA
+  // 0 claims only after its reset, so it keeps claiming until every pool
+  // unit has been taken.
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.pool != nullptr) atomicExch(a.pool, 0);
   if constexpr (kSelf) {
     // Few tokens: start bringing their rows into L2 now; the CTA reads them
     // (scale, then operands) only after its routing plan is ready.
@@ -566,13 +640,15 @@ gemv_stream_kernel(const StreamArgs a) {
   // The bucketer balances the ranges by cost (an expert's units cost more
   // the more tokens it has); without its table the ranges are equal.
   const int num_units = (kSelf ? rp.misc[0] : a.plan.meta[kMetaNumActive]) * a.row_tiles;
-  int ubeg, uend;
+  int ubeg, uend, pool_begin = num_units;
   if (kSelf) {
     ubeg = min(rp.misc[1], num_units);
     uend = min(rp.misc[2], num_units);
+    pool_begin = min(rp.misc[4], num_units);
   } else if (a.plan.unit_begin != nullptr) {
     ubeg = min(a.plan.unit_begin[blockIdx.x], num_units);
     uend = min(a.plan.unit_begin[blockIdx.x + 1], num_units);
+    pool_begin = min(a.plan.unit_begin[gridDim.x], num_units);
   } else {
     const int per_cta = num_units / (int)gridDim.x;
     const int extra = num_units - per_cta * (int)gridDim.x;
@@ -587,12 +663,25 @@ gemv_stream_kernel(const StreamArgs a) {
     const uint64_t policy = l2_evict_first_policy();
     int issued = 0;
     bool ok = true;
-    int u = ubeg / max(a.row_tiles, 1);
-    int tile = ubeg - u * a.row_tiles;
     int e = -1, cached_u = -1;
-    for (int unit = ubeg; unit < uend; ++unit, ++issued) {
+    // Units of the CTA's own range, then units claimed from the pool, then
+    // an end marker: a stage whose header names no expert.
+    int unit = ubeg;
+    for (;; ++issued) {
+      if (unit >= uend) {
+        const int claim = pool_begin < num_units ? atomicAdd(a.pool, 1) : -1;
+        unit = claim >= 0 && claim < num_units - pool_begin ? pool_begin + claim : -1;
+      }
       const int st = issued % a.stages;
       const uint32_t round = (uint32_t)(issued / a.stages);
+      if (unit < 0) {
+        if (!mbar_wait(&empty[st], (round & 1u) ^ 1u)) { ok = false; break; }
+        reinterpret_cast<StageHeader*>(stage_base + (size_t)st * a.stage_bytes)->e = -1;
+        mbar_arrive(&full[st]);
+        ++issued;
+        break;
+      }
+      const int u = unit / a.row_tiles, tile = unit - u * a.row_tiles;
       if (u != cached_u) { e = kSelf ? rp.active[u] : a.plan.active[u]; cached_u = u; }
       const int o0 = tile * a.rows_per_tile;
       const int rows = min(a.rows_per_tile, O - o0);
@@ -619,7 +708,7 @@ gemv_stream_kernel(const StreamArgs a) {
       if (sbytes)
         bulk_copy_g2s(dst + sizeof(StageHeader) + a.packed_stage_bytes,
                       reinterpret_cast<const void*>(c_lo), sbytes, &full[st], policy);
-      if (++tile == a.row_tiles) { tile = 0; ++u; }
+      ++unit;                       // past uend (pool units lie after every range): claim
     }
     if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
     // Do not leave copies in flight: wait (bounded) for the last round of
@@ -644,9 +733,9 @@ gemv_stream_kernel(const StreamArgs a) {
   // Token operands of the expert's first pass, kept across its tiles.
   GroupToken<Elem> x0[NT];
   int pair0[NT];
-  float unscale0[NT];
+  int soff0[NT];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) { pair0[j] = 0; unscale0[j] = 1.f; }
+  for (int j = 0; j < NT; ++j) { pair0[j] = 0; soff0[j] = scale_offset(0); }
 
   // Self-routed: the first unit's expert is known from the plan, so its
   // tokens load while the first stage is still on its way.
@@ -654,10 +743,10 @@ gemv_stream_kernel(const StreamArgs a) {
     cached_e = rp.active[ubeg / a.row_tiles];
     seg_beg = rp.off[cached_e];
     seg_end = rp.off[cached_e + 1];
-    load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, unscale0, seg_beg, seg_end, g);
+    load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, g);
   }
-  int it = 0;
-  for (int unit = ubeg; unit < uend; ++unit, ++it) {
+  // Stages in the producer's order until its end marker.
+  for (int it = 0;; ++it) {
     const int st = it % a.stages;
     const uint32_t round = (uint32_t)(it / a.stages);
     if (!mbar_wait(&full[st], round & 1u)) {
@@ -666,7 +755,9 @@ gemv_stream_kernel(const StreamArgs a) {
     }
     const unsigned char* hp = stage_base + (size_t)st * a.stage_bytes;
     const StageHeader* h = reinterpret_cast<const StageHeader*>(hp);
-    const int e = h->e, o0 = h->o0, rows = h->rows, scale_off = h->scale_off;
+    const int e = h->e;
+    if (e < 0) break;
+    const int o0 = h->o0, rows = h->rows, scale_off = h->scale_off;
     const unsigned char* sp = hp + sizeof(StageHeader);
 
     if (working && rbase < rows) {
@@ -674,7 +765,7 @@ gemv_stream_kernel(const StreamArgs a) {
         cached_e = e;
         seg_beg = kSelf ? rp.off[e] : a.plan.offsets[e];
         seg_end = kSelf ? rp.off[e + 1] : a.plan.offsets[e + 1];
-        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, unscale0, seg_beg, seg_end, g);
+        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, g);
       }
       // This lane's group in row rbase of the tile: packed bytes and scale.
       const uint32_t sp_lane =
@@ -685,20 +776,20 @@ gemv_stream_kernel(const StreamArgs a) {
       const bool staged = scale_off >= 0, g_ok = g < G;
       for (int base = seg_beg;;) {
         if (seg_end - base >= NT) {
-          stream_pass_any<Elem, RWS, NT>(a, x0, pair0, unscale0, sp_lane, ss_lane, gs_lane,
+          stream_pass_any<Elem, RWS, NT>(a, x0, pair0, soff0, sp_lane, ss_lane, gs_lane,
                                          staged, o0, rows, rbase, c, g_ok, lane);
         } else {                              // one token left (NT == 2)
           stream_pass_any<Elem, RWS, 1>(
               a, reinterpret_cast<const GroupToken<Elem>(&)[1]>(x0[0]),
               reinterpret_cast<const int(&)[1]>(pair0[0]),
-              reinterpret_cast<const float(&)[1]>(unscale0[0]), sp_lane, ss_lane, gs_lane,
+              reinterpret_cast<const int(&)[1]>(soff0[0]), sp_lane, ss_lane, gs_lane,
               staged, o0, rows, rbase, c, g_ok, lane);
         }
         base += NT;
         if (base >= seg_end) break;
         // More tokens: the cache now holds a later pass, so reload the first
         // one at the next tile.
-        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, unscale0, base, seg_end, g);
+        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, base, seg_end, g);
         cached_e = -1;
       }
     }
@@ -862,10 +953,18 @@ int64_t stream_row_tiles(const StreamShape& sh, int64_t O) {
 }  // namespace
 
 // Cost of a unit beyond its tokens, in token passes. Measured on GB300: a
-// unit's time grows in proportion to its expert's tokens (the decode and the
-// bulk copy hide behind the token passes), so the split weighs tokens alone.
+// unit's time grows with its expert's tokens; with the pool below, weighing
+// tokens alone balances best.
 #ifndef MXFP4EL_GEMV_FIXED_COST
 #define MXFP4EL_GEMV_FIXED_COST 0
+#endif
+// Share of the cost, in thousandths, that the per-CTA ranges cover; the
+// remaining units are claimed dynamically, so CTAs that stream faster or
+// drew cheaper units than the cost model says take more of them. Measured
+// on GB300: 900 takes the wide decode batch from 349 to 325 us and leaves
+// the 8-token batch unchanged; 850 and 800 are slower on both.
+#ifndef MXFP4EL_GEMV_STATIC_PERMILLE
+#define MXFP4EL_GEMV_STATIC_PERMILLE 900
 #endif
 
 bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
@@ -874,27 +973,33 @@ bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
     if (std::strcmp(env, "bucketer") == 0) return false;
   const StreamShape sh = stream_shape(I / 32);
   const int64_t P = T * K;
-  return sh.rws > 0 && P > 0 && O > 0 && P <= kSelfMaxPairs && E <= kSelfMaxExperts &&
-         T <= kSelfMaxTokens;
+  if (sh.rws == 0 || P <= 0 || O <= 0 || P > kSelfMaxPairs || E > kSelfMaxExperts ||
+      T > kSelfMaxTokens)
+    return false;
+  // The in-kernel split multiplies costs by the row tiles, 1000 and the
+  // grid in int64.
+  const int64_t max_cost = std::min<int64_t>(E, P) * MXFP4EL_GEMV_FIXED_COST + P;
+  return stream_row_tiles(sh, O) * max_cost <= ((int64_t)1 << 40);
 }
 
 UnitSplit gemv_unit_split(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
-  UnitSplit sp{0, 0, 0};
+  UnitSplit sp{0, 0, 0, 1000};
   const StreamShape sh = stream_shape(I / 32);
   if (sh.rws == 0 || T * K == 0 || O == 0) return sp;
   const int64_t rt = stream_row_tiles(sh, O);
   const int64_t bound_units = std::min<int64_t>(E, T * K) * rt;
   const int64_t ctas = stream_grid(bound_units);
   const int64_t fixed = MXFP4EL_GEMV_FIXED_COST;
-  // The bucketer sums costs in int32 and multiplies them by rt * ctas in
-  // int64; beyond that the kernel keeps its even split.
+  // The bucketer sums costs in int32 and multiplies them by rt, ctas and
+  // 1000 in int64; beyond that the kernel keeps its even split.
   const int64_t max_cost = std::min<int64_t>(E, T * K) * fixed + T * K;
   if (ctas <= 0 || ctas > kMaxSplitCtas || bound_units > 0x7fffffff ||
-      max_cost >= ((int64_t)1 << 31) || rt * max_cost > ((int64_t)1 << 50))
+      max_cost >= ((int64_t)1 << 31) || rt * max_cost > ((int64_t)1 << 40))
     return sp;
   sp.ctas = (int)ctas;
   sp.row_tiles = (int)rt;
   sp.fixed_cost = (int)fixed;
+  sp.static_permille = MXFP4EL_GEMV_STATIC_PERMILLE;
   return sp;
 }
 
@@ -937,6 +1042,8 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
   a.E = (int)E;
   a.P = (int)(T * K);
   a.fixed_cost = MXFP4EL_GEMV_FIXED_COST;
+  a.static_permille = MXFP4EL_GEMV_STATIC_PERMILLE;
+  a.pool = plan.meta + kMetaPoolCounter;
   a.route_bytes = self ? self_route_bytes(a.E, a.P, a.T) : 0u;
   a.packed = packed;
   a.scales = scales;
@@ -956,10 +1063,10 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
   if (gemv_unit_split(T, E, I, O, K).ctas == 0) a.plan.unit_begin = nullptr;
   a.packed_stage_bytes = (uint32_t)((size_t)a.rows_per_tile * G * 16);
   a.stage_bytes = (uint32_t)((stage_bytes_for(a.rows_per_tile, G) + 127) / 128 * 128);
-  a.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - a.route_bytes) / a.stage_bytes);
+  a.stages = (int)std::min<size_t>(
+      kMaxStages, (kSmemBudget - kStreamHeadBytes - a.route_bytes) / a.stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem =
-      2 * kMaxStages * sizeof(uint64_t) + a.route_bytes + (size_t)a.stages * a.stage_bytes;
+  const size_t smem = kStreamHeadBytes + a.route_bytes + (size_t)a.stages * a.stage_bytes;
   const int64_t bound_units = std::min<int64_t>(E, T * K) * a.row_tiles;
   if (bound_units > 0x7fffffff) return cudaErrorInvalidConfiguration;
 #define MXFP4EL_STREAM_CASES_SELF(ELEM, SELF)                                    \

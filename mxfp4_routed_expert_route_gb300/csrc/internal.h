@@ -27,6 +27,7 @@ constexpr int kStatusWords = 4;
 constexpr int kMetaNumActive = 0;   // experts with at least one valid pair
 constexpr int kMetaNumPairs = 1;    // valid pairs
 constexpr int kMetaUnitCounter = 2; // next unit of the tensor-core kernel (reset by the gather)
+constexpr int kMetaPoolCounter = 3; // next pool unit of the staged GEMV (reset by the GEMV)
 constexpr int kMetaWords = 64;
 
 // Routing lists written by the bucketer, all in device memory.
@@ -43,14 +44,16 @@ struct RoutePlan {
 // Cost-balanced split of the staged GEMV's units (active expert, row tile)
 // over its CTAs, computed by the bucketer: unit (u, tile) costs
 // fixed_cost + (tokens of expert u), CTA b starts at the first unit whose
-// cost prefix reaches b/ctas of the total. With equal unit counts per CTA,
-// the CTAs that drew experts with several tokens finished last and the
-// others idled. ctas == 0: no split.
+// cost prefix reaches b * static_permille / (1000 ctas) of the total; entry
+// ctas is the first unit of the pool that the CTAs share after their own
+// ranges. With equal unit counts per CTA, the CTAs that drew experts with
+// several tokens finished last and the others idled. ctas == 0: no split.
 constexpr int kMaxSplitCtas = 1024;
 struct UnitSplit {
   int ctas;
   int row_tiles;
   int fixed_cost;
+  int static_permille;
 };
 
 // Workspace layout for one call.

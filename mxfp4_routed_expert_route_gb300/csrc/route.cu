@@ -80,21 +80,26 @@ __device__ void write_unit_split(const RoutePlan& plan, const UnitSplit& split, 
     for (int b = threadIdx.x; b <= split.ctas; b += blockDim.x) plan.unit_begin[b] = 0;
     return;
   }
+  // Boundary b of n (b = n: the pool's start) sits at cost b*S*C/N with
+  // S = static_permille and N = 1000 n.
+  const int64_t S = split.static_permille, N = 1000 * n;
   int slot = act0;
   for (int e = e0; e < e1; ++e) {
     const int c = plan.counts[e];
     if (c == 0) continue;
     const int64_t cu = split.fixed_cost + c;
     const int64_t lo = rt * cost, hi = rt * (cost + cu);   // [lo, hi) in cost units
-    // Boundaries b with b*C/n in [lo, hi).
-    for (int64_t b = (lo * n + C - 1) / C; b < n && b * C < hi * n; ++b) {
-      const int64_t tile = (b * C - lo * n + n * cu - 1) / (n * cu);
+    // Boundaries b with b*S*C/N in [lo, hi).
+    for (int64_t b = (lo * N + S * C - 1) / (S * C); b <= n && b * S * C < hi * N; ++b) {
+      const int64_t tile = (b * S * C - lo * N + N * cu - 1) / (N * cu);
       plan.unit_begin[b] = (int)(slot * rt + tile);
     }
     cost += (int)cu;
     ++slot;
   }
-  if (threadIdx.x == 0) plan.unit_begin[split.ctas] = (int)((int64_t)total_active * rt);
+  // With S = 1000 boundary n is the end of the last expert's units.
+  if (threadIdx.x == 0 && S >= 1000)
+    plan.unit_begin[split.ctas] = (int)((int64_t)total_active * rt);
 }
 
 template <typename Idx>

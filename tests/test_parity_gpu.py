@@ -174,6 +174,58 @@ def test_scale_byte_zero_and_255_fp32():
     assert got[0] == 2.0 ** -128 and got[1] == 2.0 ** 127
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_every_scale_byte_exact(dtype):
+    # Output row r uses scale byte r for its one group of codes 1.0, and the
+    # token is all ones: the row is 32 * 2^(r - 127) = 2^(r - 122), exact in
+    # float32 (bf16 holds every power of two in range too) and +inf past the
+    # largest finite value.
+    O = 256
+    packed = np.full((1, O, 1, 16), 0x22, dtype=np.uint8)
+    scales = np.arange(O, dtype=np.uint8).reshape(1, O, 1)
+    x = torch.ones((1, 32), dtype=dtype)
+    out = mxfp4_expert_linear(x.cuda(), torch.from_numpy(packed).cuda(),
+                              torch.from_numpy(scales).cuda(),
+                              torch.zeros((1, 1), dtype=torch.int32).cuda(),
+                              torch.ones((1, 1)).cuda(), torch.zeros((1, O), dtype=dtype).cuda())
+    got = out.float().cpu().double().numpy()[0]
+    want, _, _ = oracle.expert_linear(x.double().numpy(), packed, scales,
+                                      np.zeros((1, 1), dtype=np.int64), np.ones((1, 1)),
+                                      np.zeros((1, O)))
+    want = want[0]
+    fmax = float(torch.finfo(dtype).max)
+    finite = np.abs(want) <= fmax
+    assert np.array_equal(got[finite], want[finite])
+    assert np.all(np.isinf(got[~finite]) & (got[~finite] > 0))
+    assert finite[:250].all() and not finite[250:].any()
+
+
+def test_extreme_token_magnitudes_bf16():
+    # bf16 tokens of magnitude 2^m (m from -120 to 100) against every scale
+    # byte: the GEMV pre-scales each token by its own power of two into f16,
+    # so weight scale and token scale meet in one factor 2^(s-127-sigma)
+    # that spans 2^-253 .. 2^247. Elements whose terms stay within float32
+    # range match the oracle to the bf16 tolerance; those past it are not
+    # finite (inf, or NaN where terms of both signs overflow).
+    rng = np.random.default_rng(21)
+    T, E, K, I, O = 8, 3, 2, 64, 96
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, scale_lo=0, scale_hi=255, seed=21)
+    mags = torch.tensor([-120, -100, -30, 0, 30, 60, 90, 100], dtype=torch.float32)
+    wl.x = (wl.x.float() * torch.exp2(mags)[:, None]).to(torch.bfloat16)
+    wl.y_shared = torch.zeros((T, O), dtype=torch.bfloat16)
+    out = run_gpu(wl).float().cpu().double().numpy()
+    want, absm, _ = oracle_rows(wl)
+    fmax = float(torch.finfo(torch.float32).max)
+    inside = (absm >= 2.0 ** -100) & (absm <= fmax / 4)
+    assert inside.sum() > T * O // 4
+    err = np.abs(out[inside] - want[inside])
+    assert np.all(err <= TOL[torch.bfloat16] * absm[inside])
+    over = np.abs(want) >= 2 * fmax
+    assert over.any()
+    assert not np.isfinite(out[over]).any()
+    assert not np.isnan(out[absm <= fmax / 4]).any()
+
+
 def test_integer_inputs_exact_bf16():
     rng = np.random.default_rng(13)
     T, E, K, I, O = 16, 3, 1, 256, 64
