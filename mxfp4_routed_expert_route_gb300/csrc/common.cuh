@@ -248,6 +248,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// As mbar_wait, but each test may suspend the thread in hardware until the
+// phase completes (or about 20 us pass) instead of spinning on issue slots
+// that other warps of the SM need.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(20000u)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_suspend(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // Asks the TMA engine to bring `bytes` (a multiple of 16) at the 16-byte
 // aligned `src` into L2, without waiting.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {

@@ -511,22 +511,25 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  if (g_ok) {
-    uint32_t pa = sp_lane, sa = ss_lane;
-    const uint8_t* ga = gs_lane;
+  // Every lane runs the rows (lanes past the last group read group G-1,
+  // see the caller) and keeps zero where it has no group: no divergence.
+  uint32_t pa = sp_lane, sa = ss_lane;
+  const uint8_t* ga = gs_lane;
 #pragma unroll
-    for (int r = 0; r < RWS; ++r) {
-      if (kFull || rbase + r < rows) {
-        uint32_t w[16];
-        decode_group(lds128(pa), w);
-        const uint32_t sb = kScalesStaged ? lds_u8(sa) : (uint32_t)__ldg(ga);
+  for (int r = 0; r < RWS; ++r) {
+    if (kFull || rbase + r < rows) {
+      uint32_t w[16];
+      decode_group(lds128(pa), w);
+      const uint32_t sb = kScalesStaged ? lds_u8(sa) : (uint32_t)__ldg(ga);
 #pragma unroll
-        for (int j = 0; j < NTA; ++j) acc[r * NTA + j] = apply_scale(xt[j].dot(w), sb, lut + soff[j]);
+      for (int j = 0; j < NTA; ++j) {
+        const float v = apply_scale(xt[j].dot(w), sb, lut + soff[j]);
+        acc[r * NTA + j] = g_ok ? v : 0.f;
       }
-      pa += prow;
-      sa += (uint32_t)G;
-      ga += G;
     }
+    pa += prow;
+    sa += (uint32_t)G;
+    if (!kScalesStaged) ga += G;
   }
   const float total = warp_reduce_scatter<V>(acc, lane);
   if ((lane & ((1 << (5 - L)) - 1)) == 0) {
@@ -667,13 +670,13 @@ gemv_stream_kernel(const StreamArgs a) {
     // Units of the CTA's own range, then units claimed from the pool, then
     // an end marker: a stage whose header names no expert.
     int unit = ubeg;
+    int st = 0;
+    uint32_t round = 0;
     for (;; ++issued) {
       if (unit >= uend) {
         const int claim = pool_begin < num_units ? atomicAdd(a.pool, 1) : -1;
         unit = claim >= 0 && claim < num_units - pool_begin ? pool_begin + claim : -1;
       }
-      const int st = issued % a.stages;
-      const uint32_t round = (uint32_t)(issued / a.stages);
       if (unit < 0) {
         if (!mbar_wait(&empty[st], (round & 1u) ^ 1u)) { ok = false; break; }
         reinterpret_cast<StageHeader*>(stage_base + (size_t)st * a.stage_bytes)->e = -1;
@@ -709,6 +712,10 @@ gemv_stream_kernel(const StreamArgs a) {
         bulk_copy_g2s(dst + sizeof(StageHeader) + a.packed_stage_bytes,
                       reinterpret_cast<const void*>(c_lo), sbytes, &full[st], policy);
       ++unit;                       // past uend (pool units lie after every range): claim
+      if (++st == a.stages) {
+        st = 0;
+        ++round;
+      }
     }
     if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
     // Do not leave copies in flight: wait (bounded) for the last round of
@@ -728,6 +735,7 @@ gemv_stream_kernel(const StreamArgs a) {
   const bool working = warp < a.ncol * a.nsub;
   const int c = warp % a.ncol, sub = warp / a.ncol;
   const int g = c * 32 + lane;
+  const int gc = min(g, a.G - 1);     // lanes past the last group shadow group G-1
   const int rbase = sub * RWS;
   int cached_e = -1, seg_beg = 0, seg_end = 0;
   // Token operands of the expert's first pass, kept across its tiles.
@@ -743,13 +751,13 @@ gemv_stream_kernel(const StreamArgs a) {
     cached_e = rp.active[ubeg / a.row_tiles];
     seg_beg = rp.off[cached_e];
     seg_end = rp.off[cached_e + 1];
-    load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, g);
+    load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, gc);
   }
   // Stages in the producer's order until its end marker.
-  for (int it = 0;; ++it) {
-    const int st = it % a.stages;
-    const uint32_t round = (uint32_t)(it / a.stages);
-    if (!mbar_wait(&full[st], round & 1u)) {
+  int st = 0;
+  uint32_t phase = 0;
+  for (;;) {
+    if (!mbar_wait_suspend(&full[st], phase)) {
       if (lane == 0) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
       return;
     }
@@ -765,15 +773,16 @@ gemv_stream_kernel(const StreamArgs a) {
         cached_e = e;
         seg_beg = kSelf ? rp.off[e] : a.plan.offsets[e];
         seg_end = kSelf ? rp.off[e + 1] : a.plan.offsets[e + 1];
-        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, g);
+        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, gc);
       }
       // This lane's group in row rbase of the tile: packed bytes and scale.
       const uint32_t sp_lane =
-          smem_addr(sp) + ((uint32_t)rbase * (uint32_t)G + (uint32_t)g) * 16u;
+          smem_addr(sp) + ((uint32_t)rbase * (uint32_t)G + (uint32_t)gc) * 16u;
       const uint32_t ss_lane =
-          smem_addr(sp) + a.packed_stage_bytes + (uint32_t)(scale_off + rbase * G + g);
-      const uint8_t* gs_lane = a.scales + ((size_t)e * O + o0 + rbase) * G + g;
+          smem_addr(sp) + a.packed_stage_bytes + (uint32_t)(scale_off + rbase * G + gc);
       const bool staged = scale_off >= 0, g_ok = g < G;
+      const uint8_t* gs_lane =
+          staged ? nullptr : a.scales + ((size_t)e * O + o0 + rbase) * G + gc;
       for (int base = seg_beg;;) {
         if (seg_end - base >= NT) {
           stream_pass_any<Elem, RWS, NT>(a, x0, pair0, soff0, sp_lane, ss_lane, gs_lane,
@@ -789,12 +798,16 @@ gemv_stream_kernel(const StreamArgs a) {
         if (base >= seg_end) break;
         // More tokens: the cache now holds a later pass, so reload the first
         // one at the next tile.
-        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, base, seg_end, g);
+        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, base, seg_end, gc);
         cached_e = -1;
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
+    if (++st == a.stages) {
+      st = 0;
+      phase ^= 1u;
+    }
   }
 }
 
