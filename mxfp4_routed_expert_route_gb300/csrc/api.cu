@@ -146,9 +146,11 @@ int run(const void* x, const uint8_t* packed, const uint8_t* scales,
     if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
   }
   mark(MXFP4EL_STAGE_COMBINE, true, stream);
+  // With K > 0 and E > 0 a linear kernel of the library ran just before
+  // (the launchers skip only an empty grid, E == 0).
   err = launch_combine(ys, sel, index_dtype, p, ws.part,
                        linear_partial_columns(T, E, I, O, K, token_dtype), out, token_dtype, T,
-                       E, O, K, stream);
+                       E, O, K, K > 0 && E > 0, stream);
   mark(MXFP4EL_STAGE_COMBINE, false, stream);
   return err == cudaSuccess ? MXFP4EL_OK : MXFP4EL_ERR_CUDA;
 }

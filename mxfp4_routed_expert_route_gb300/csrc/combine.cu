@@ -74,69 +74,124 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&x)[4]) {
 constexpr int kVecLanes = 32;   // one warp per segment of 4 * 32 outputs
 constexpr int kSlotBatch = 4;   // slots whose loads are issued together
 
-// Adds slots [k0, k0 + n) of pair row t*K (n <= kSlotBatch) to acc in slot
-// order. All ids, weights and partial-result vectors of the batch are loaded
-// before the first add, so their loads are in flight together.
-template <typename Idx>
-__device__ __forceinline__ void add_slots(const Idx* __restrict__ sel, const float* __restrict__ p,
-                                          const float* __restrict__ part, int ncol, int64_t O,
-                                          int64_t E, int64_t pk0, int n, int64_t o,
-                                          float (&acc)[4]) {
+// Ids and weights of slots [k0, k0 + n) of pair row t*K (n <= kSlotBatch).
+struct SlotBatch {
   bool valid[kSlotBatch];
   float w[kSlotBatch];
+};
+template <typename Idx>
+__device__ __forceinline__ SlotBatch load_slots(const Idx* __restrict__ sel,
+                                                const float* __restrict__ p, int64_t E,
+                                                int64_t pk0, int n) {
+  SlotBatch b;
 #pragma unroll
   for (int j = 0; j < kSlotBatch; ++j) {
     const long long e = j < n ? (long long)sel[pk0 + j] : -1;
-    valid[j] = e >= 0 && e < E;
-    w[j] = j < n ? p[pk0 + j] : 0.f;
+    b.valid[j] = e >= 0 && e < E;
+    b.w[j] = j < n ? p[pk0 + j] : 0.f;
   }
+  return b;
+}
+
+// Adds those slots' partial results to acc in slot order, each slot's
+// columns summed in column order first. kCols (the GEMV's partials, ncol > 1):
+// the loads go out four columns of the batch (16 vectors) at a time, so a row
+// of ncol columns costs ceil(ncol/4) round trips to L2 instead of ncol. One
+// column (the tensor-core GEMM's partials, HBM-bound at prefill sizes): one
+// vector per slot, few registers, many warps per SM.
+constexpr int kColBatch = 4;
+template <bool kCols>
+__device__ __forceinline__ void add_slots(const SlotBatch& b, const float* __restrict__ part,
+                                          int ncol, int64_t O, int64_t pk0, int64_t o,
+                                          float (&acc)[4]) {
   const int64_t row = (int64_t)ncol * O;          // floats per pair
   const float* base = part + pk0 * row + o;
   float4 s[kSlotBatch];
+  if constexpr (!kCols) {
 #pragma unroll
-  for (int j = 0; j < kSlotBatch; ++j)
-    s[j] = valid[j] ? __ldcs(reinterpret_cast<const float4*>(base + j * row))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = 1; c < ncol; ++c) {
+    for (int j = 0; j < kSlotBatch; ++j)
+      s[j] = b.valid[j] ? __ldcs(reinterpret_cast<const float4*>(base + j * row))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    for (int c0 = 0; c0 < ncol; c0 += kColBatch) {
+      float4 u[kColBatch][kSlotBatch];
 #pragma unroll
-    for (int j = 0; j < kSlotBatch; ++j) {
-      if (valid[j]) {
-        const float4 u = __ldcs(reinterpret_cast<const float4*>(base + j * row + (int64_t)c * O));
-        s[j].x += u.x; s[j].y += u.y; s[j].z += u.z; s[j].w += u.w;
+      for (int cc = 0; cc < kColBatch; ++cc) {
+#pragma unroll
+        for (int j = 0; j < kSlotBatch; ++j) {
+          u[cc][j] = b.valid[j] && c0 + cc < ncol
+                         ? __ldcs(reinterpret_cast<const float4*>(base + j * row +
+                                                                  (int64_t)(c0 + cc) * O))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < kColBatch; ++cc) {
+        if (c0 + cc >= ncol) break;
+#pragma unroll
+        for (int j = 0; j < kSlotBatch; ++j) {
+          if (c0 + cc == 0) {
+            s[j] = u[cc][j];
+          } else {
+            s[j].x += u[cc][j].x; s[j].y += u[cc][j].y;
+            s[j].z += u[cc][j].z; s[j].w += u[cc][j].w;
+          }
+        }
       }
     }
   }
 #pragma unroll
   for (int j = 0; j < kSlotBatch; ++j) {
-    if (valid[j]) {
-      acc[0] = fmaf(w[j], s[j].x, acc[0]);
-      acc[1] = fmaf(w[j], s[j].y, acc[1]);
-      acc[2] = fmaf(w[j], s[j].z, acc[2]);
-      acc[3] = fmaf(w[j], s[j].w, acc[3]);
+    if (b.valid[j]) {
+      acc[0] = fmaf(b.w[j], s[j].x, acc[0]);
+      acc[1] = fmaf(b.w[j], s[j].y, acc[1]);
+      acc[2] = fmaf(b.w[j], s[j].z, acc[2]);
+      acc[3] = fmaf(b.w[j], s[j].w, acc[3]);
     }
   }
 }
 
-template <typename Tok, typename Idx>
+template <typename Tok, typename Idx, bool kCols>
 __global__ void __launch_bounds__(256)
 combine_vec_kernel(const Tok* __restrict__ ys, const Idx* __restrict__ sel,
                    const float* __restrict__ p, const float* __restrict__ part, int ncol,
-                   Tok* __restrict__ out, int64_t T, int64_t O, int K, int64_t E) {
-  pdl_wait();                  // the linear kernel's partial results are complete
+                   Tok* __restrict__ out, int64_t T, int64_t O, int K, int64_t E,
+                   int prefetch) {
   const int64_t nv = O / 4;                         // 4-wide vectors per token row
   const int64_t segs = (nv + kVecLanes - 1) / kVecLanes;
   const int64_t tasks = T * segs;
   const int warps = blockDim.x / 32, lane = threadIdx.x & 31;
-  for (int64_t task = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); task < tasks;
-       task += (int64_t)gridDim.x * warps) {
+  const int64_t first = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5);
+  float acc0[4] = {0.f, 0.f, 0.f, 0.f};
+  SlotBatch b0 = {};
+  const bool early = prefetch != 0 && first < tasks;
+  if (early) {
+    const int64_t t = first / segs;
+    const int64_t v = (first - t * segs) * kVecLanes + lane;
+    if (v < nv) {
+      load4(ys + t * O + 4 * v, acc0);
+      b0 = load_slots(sel, p, E, t * K, min(kSlotBatch, K));
+    }
+  }
+  pdl_wait();                  // the linear kernel's partial results are complete
+  for (int64_t task = first; task < tasks; task += (int64_t)gridDim.x * warps) {
     const int64_t t = task / segs;
     const int64_t v = (task - t * segs) * kVecLanes + lane;
     if (v >= nv) continue;
     const int64_t o = 4 * v;
+    const bool pre = early && task == first;
     float acc[4];
-    load4(ys + t * O + o, acc);
-    for (int k0 = 0; k0 < K; k0 += kSlotBatch)
-      add_slots(sel, p, part, ncol, O, E, t * K + k0, min(kSlotBatch, K - k0), o, acc);
+    if (pre) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = acc0[i];
+    } else {
+      load4(ys + t * O + o, acc);
+    }
+    for (int k0 = 0; k0 < K; k0 += kSlotBatch) {
+      const int n = min(kSlotBatch, K - k0);
+      const SlotBatch b = pre && k0 == 0 ? b0 : load_slots(sel, p, E, t * K + k0, n);
+      add_slots<kCols>(b, part, ncol, O, t * K + k0, o, acc);
+    }
     store4(out + t * O + o, acc);
   }
 }
@@ -144,7 +199,7 @@ combine_vec_kernel(const Tok* __restrict__ ys, const Idx* __restrict__ sel,
 template <typename Tok, typename Idx>
 cudaError_t launch_typed(const Tok* ys, const Idx* sel, const float* p,
                          const float* part, int ncol, Tok* out, int64_t T, int64_t E,
-                         int64_t O, int64_t K, cudaStream_t stream) {
+                         int64_t O, int64_t K, bool prefetch, cudaStream_t stream) {
   const int64_t n = T * O;
   if (n == 0) return cudaSuccess;
   const uintptr_t tok_align = 4 * sizeof(Tok);
@@ -153,8 +208,16 @@ cudaError_t launch_typed(const Tok* ys, const Idx* sel, const float* p,
       reinterpret_cast<uintptr_t>(part) % 16 == 0) {
     const int64_t tasks = T * ((O / 4 + kVecLanes - 1) / kVecLanes);
     const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, 152 * 8);
-    return launch_after_previous(combine_vec_kernel<Tok, Idx>, dim3((unsigned)blocks), dim3(256),
-                                 0, stream, ys, sel, p, part, ncol, out, T, O, (int)K, E);
+    // The early loads only shorten the path when each warp has one task
+    // (small batches); with many tasks per warp the combine is bandwidth-bound.
+    prefetch = prefetch && tasks <= blocks * 8;
+    if (ncol > 1)
+      return launch_after_previous(combine_vec_kernel<Tok, Idx, true>, dim3((unsigned)blocks),
+                                   dim3(256), 0, stream, ys, sel, p, part, ncol, out, T, O,
+                                   (int)K, E, prefetch ? 1 : 0);
+    return launch_after_previous(combine_vec_kernel<Tok, Idx, false>, dim3((unsigned)blocks),
+                                 dim3(256), 0, stream, ys, sel, p, part, ncol, out, T, O, (int)K,
+                                 E, prefetch ? 1 : 0);
   }
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 16);
   return launch_after_previous(combine_kernel<Tok, Idx>, dim3((unsigned)blocks), dim3(256), 0,
@@ -164,13 +227,13 @@ cudaError_t launch_typed(const Tok* ys, const Idx* sel, const float* p,
 template <typename Tok>
 cudaError_t launch_by_index(const Tok* ys, const void* sel, int index_dtype,
                             const float* p, const float* part, int ncol, Tok* out,
-                            int64_t T, int64_t E, int64_t O, int64_t K,
+                            int64_t T, int64_t E, int64_t O, int64_t K, bool prefetch,
                             cudaStream_t stream) {
   if (index_dtype == kIndexI64)
     return launch_typed(ys, static_cast<const int64_t*>(sel), p, part, ncol, out, T,
-                        E, O, K, stream);
+                        E, O, K, prefetch, stream);
   return launch_typed(ys, static_cast<const int32_t*>(sel), p, part, ncol, out, T, E,
-                      O, K, stream);
+                      O, K, prefetch, stream);
 }
 
 }  // namespace
@@ -178,13 +241,15 @@ cudaError_t launch_by_index(const Tok* ys, const void* sel, int index_dtype,
 cudaError_t launch_combine(const void* y_shared, const void* sel,
                            int index_dtype, const float* p, const float* part,
                            int ncol, void* out, int token_dtype, int64_t T,
-                           int64_t E, int64_t O, int64_t K, cudaStream_t stream) {
+                           int64_t E, int64_t O, int64_t K, bool after_linear,
+                           cudaStream_t stream) {
   if (token_dtype == kTokenBF16)
     return launch_by_index(static_cast<const __nv_bfloat16*>(y_shared), sel,
                            index_dtype, p, part, ncol,
-                           static_cast<__nv_bfloat16*>(out), T, E, O, K, stream);
+                           static_cast<__nv_bfloat16*>(out), T, E, O, K, after_linear, stream);
   return launch_by_index(static_cast<const float*>(y_shared), sel, index_dtype,
-                         p, part, ncol, static_cast<float*>(out), T, E, O, K, stream);
+                         p, part, ncol, static_cast<float*>(out), T, E, O, K, after_linear,
+                         stream);
 }
 
 }  // namespace mxfp4el

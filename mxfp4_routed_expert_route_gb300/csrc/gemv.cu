@@ -605,7 +605,6 @@ gemv_stream_kernel(const StreamArgs a) {
   const SelfPlan rp = self_plan(route_area, a.E, a.P, a.T);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_launch_dependents();
   fill_scale_lut(reinterpret_cast<float2*>(smem + kScaleLutOffset));   // read after a barrier
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -618,6 +617,9 @@ gemv_stream_kernel(const StreamArgs a) {
   // tokens only after whatever ran before it on the stream has finished.
   // Otherwise: the bucketer's lists and the prepared tokens are ready.
   pdl_wait();
+  // Only now may the combine start: it reads the call's other inputs before
+  // waiting for this kernel, so everything before this kernel must be done.
+  pdl_launch_dependents();
   // The pool counter starts at zero for this launch. A CTA that claims
   // before this reset gets a stale value: one past the pool ends its claims,
   // one inside the pool repeats a unit (the same values written twice). CTA

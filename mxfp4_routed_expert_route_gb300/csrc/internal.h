@@ -142,10 +142,15 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
 enum class LinearPath { kGemv, kGemm };
 LinearPath choose_path(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype);
 
+// after_linear: the previous kernel on `stream` is the library's linear
+// kernel (which releases its dependents only after everything before it has
+// finished); the combine then reads y_shared, the ids and the weights before
+// waiting for the partial results.
 cudaError_t launch_combine(const void* y_shared, const void* sel,
                            int index_dtype, const float* p, const float* part,
                            int ncol, void* out, int token_dtype, int64_t T,
-                           int64_t E, int64_t O, int64_t K, cudaStream_t stream);
+                           int64_t E, int64_t O, int64_t K, bool after_linear,
+                           cudaStream_t stream);
 
 // Device address of the status words on the current device.
 unsigned long long* device_status_words();
