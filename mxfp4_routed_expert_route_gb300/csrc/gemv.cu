@@ -714,6 +714,12 @@ gemv_stream_kernel(const StreamArgs a) {
         bulk_copy_g2s(dst + sizeof(StageHeader) + a.packed_stage_bytes,
                       reinterpret_cast<const void*>(c_lo), sbytes, &full[st], policy);
       ++unit;                       // past uend (pool units lie after every range): claim
+      // Slow start: the first stage goes out alone and lands before the
+      // rest of the ring is requested. With every CTA's whole ring
+      // requested at once the first stages landed only after most of those
+      // bytes (6 us after the request); the consumers, the bottleneck here,
+      // now start about 1 us sooner (decode, measured).
+      if (issued == 0 && !mbar_wait(&full[0], 0u)) { ok = false; break; }
       if (++st == a.stages) {
         st = 0;
         ++round;
