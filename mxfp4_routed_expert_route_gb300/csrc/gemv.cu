@@ -116,6 +116,10 @@ template <> struct GroupToken<float> {      // fp32 tokens, used as they are
     TokenIO<float>::load32(row + (size_t)g * 32, v);
   }
   __device__ __forceinline__ float dot(const uint32_t (&w)[16]) const { return dot_group_f32(w, v); }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+  }
 };
 
 template <> struct GroupToken<__half> {     // bf16 tokens, pre-scaled to f16
@@ -144,6 +148,10 @@ template <> struct GroupToken<__half> {     // bf16 tokens, pre-scaled to f16
     }
   }
   __device__ __forceinline__ float dot(const uint32_t (&w)[16]) const { return dot_group_f16(w, v); }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0u;
+  }
 };
 
 // ---------------------------------------------------------- token prep -----
@@ -502,7 +510,7 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
                                             const int (&pair)[NTA], const int (&soff)[NTA],
                                             uint32_t sp_lane,
                                             uint32_t ss_lane, const uint8_t* gs_lane, int o0,
-                                            int rows, int rbase, int c, bool g_ok, int lane) {
+                                            int rows, int rbase, int c, int lane) {
   constexpr int V = Pow2Ceil<RWS * NTA>::value;
   constexpr int L = Log2<V>::value;
   const int G = a.G, O = a.O;
@@ -511,8 +519,9 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  // Every lane runs the rows (lanes past the last group read group G-1,
-  // see the caller) and keeps zero where it has no group: no divergence.
+  // Every lane runs the rows: lanes past the last group read group G-1's
+  // weights against zeroed token values (see load_pass), so their partials
+  // are zero without a branch or a select.
   uint32_t pa = sp_lane, sa = ss_lane;
   const uint8_t* ga = gs_lane;
 #pragma unroll
@@ -522,10 +531,7 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
       decode_group(lds128(pa), w);
       const uint32_t sb = kScalesStaged ? lds_u8(sa) : (uint32_t)__ldg(ga);
 #pragma unroll
-      for (int j = 0; j < NTA; ++j) {
-        const float v = apply_scale(xt[j].dot(w), sb, lut + soff[j]);
-        acc[r * NTA + j] = g_ok ? v : 0.f;
-      }
+      for (int j = 0; j < NTA; ++j) acc[r * NTA + j] = apply_scale(xt[j].dot(w), sb, lut + soff[j]);
     }
     pa += prow;
     sa += (uint32_t)G;
@@ -554,22 +560,22 @@ __device__ __forceinline__ void stream_pass_any(const StreamArgs& a,
                                                 const int (&soff)[NTA], uint32_t sp_lane,
                                                 uint32_t ss_lane, const uint8_t* gs_lane,
                                                 bool staged, int o0, int rows, int rbase, int c,
-                                                bool g_ok, int lane) {
+                                                int lane) {
   if (staged && rbase + RWS <= rows)
     stream_pass<Elem, RWS, NTA, true, true>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane, o0,
-                                            rows, rbase, c, g_ok, lane);
+                                            rows, rbase, c, lane);
   else if (staged)
     stream_pass<Elem, RWS, NTA, true, false>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane, o0,
-                                             rows, rbase, c, g_ok, lane);
+                                             rows, rbase, c, lane);
   else
     stream_pass<Elem, RWS, NTA, false, false>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane,
-                                              o0, rows, rbase, c, g_ok, lane);
+                                              o0, rows, rbase, c, lane);
 }
 
 // Token operands (this lane's group) and pair ids of the pass starting at
 // position `base` of an expert's segment [base, seg_end), and each token's
 // offset into the scale-factor table (from its power of two; 0 for fp32
-// tokens).
+// tokens). Lanes past the last group (g >= G) get zeros.
 template <typename Elem, int NT, bool kSelf>
 __device__ __forceinline__ void load_pass(const StreamArgs& a, const SelfPlan& sp,
                                           GroupToken<Elem> (&xt)[NT], int (&pair)[NT],
@@ -585,9 +591,12 @@ __device__ __forceinline__ void load_pass(const StreamArgs& a, const SelfPlan& s
       if (g < a.G)
         xt[j].load_scaled(static_cast<const __nv_bfloat16*>(a.x) + (size_t)t * a.I, g,
                           __uint_as_float((uint32_t)(sg + 127) << 23));
+      else
+        xt[j].zero();
       soff[j] = scale_offset(sg);
     } else {
       if (g < a.G) xt[j].load(static_cast<const Elem*>(a.x) + (size_t)t * a.I, g);
+      else xt[j].zero();
       soff[j] = scale_offset(a.sigma != nullptr ? a.sigma[t] : 0);
     }
   }
@@ -759,7 +768,7 @@ gemv_stream_kernel(const StreamArgs a) {
     cached_e = rp.active[ubeg / a.row_tiles];
     seg_beg = rp.off[cached_e];
     seg_end = rp.off[cached_e + 1];
-    load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, gc);
+    load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, g);
   }
   // Stages in the producer's order until its end marker.
   int st = 0;
@@ -781,32 +790,32 @@ gemv_stream_kernel(const StreamArgs a) {
         cached_e = e;
         seg_beg = kSelf ? rp.off[e] : a.plan.offsets[e];
         seg_end = kSelf ? rp.off[e + 1] : a.plan.offsets[e + 1];
-        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, gc);
+        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, g);
       }
       // This lane's group in row rbase of the tile: packed bytes and scale.
       const uint32_t sp_lane =
           smem_addr(sp) + ((uint32_t)rbase * (uint32_t)G + (uint32_t)gc) * 16u;
       const uint32_t ss_lane =
           smem_addr(sp) + a.packed_stage_bytes + (uint32_t)(scale_off + rbase * G + gc);
-      const bool staged = scale_off >= 0, g_ok = g < G;
+      const bool staged = scale_off >= 0;
       const uint8_t* gs_lane =
           staged ? nullptr : a.scales + ((size_t)e * O + o0 + rbase) * G + gc;
       for (int base = seg_beg;;) {
         if (seg_end - base >= NT) {
           stream_pass_any<Elem, RWS, NT>(a, x0, pair0, soff0, sp_lane, ss_lane, gs_lane,
-                                         staged, o0, rows, rbase, c, g_ok, lane);
+                                         staged, o0, rows, rbase, c, lane);
         } else {                              // one token left (NT == 2)
           stream_pass_any<Elem, RWS, 1>(
               a, reinterpret_cast<const GroupToken<Elem>(&)[1]>(x0[0]),
               reinterpret_cast<const int(&)[1]>(pair0[0]),
               reinterpret_cast<const int(&)[1]>(soff0[0]), sp_lane, ss_lane, gs_lane,
-              staged, o0, rows, rbase, c, g_ok, lane);
+              staged, o0, rows, rbase, c, lane);
         }
         base += NT;
         if (base >= seg_end) break;
         // More tokens: the cache now holds a later pass, so reload the first
         // one at the next tile.
-        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, base, seg_end, gc);
+        load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, base, seg_end, g);
         cached_e = -1;
       }
     }
