@@ -236,11 +236,10 @@ struct SelfPlan {
   int* sigma;    // [T]     token scale exponents (bf16 tokens)
   int* misc;     // [8]     0: active experts, 1: first unit, 2: end unit, 3: pairs,
                  //         4: first unit of the shared pool
-  int* wbuf;     // [33]    scan scratch
 };
 
 __host__ __device__ inline uint32_t self_route_bytes(int E, int P, int T) {
-  return (uint32_t)(((size_t)(E + 1) + 2 * (size_t)E + 2 * (size_t)P + (size_t)T + 8 + 33) * 4 +
+  return (uint32_t)(((size_t)(E + 1) + 2 * (size_t)E + 2 * (size_t)P + (size_t)T + 8) * 4 +
                     127) /
          128 * 128;
 }
@@ -255,7 +254,6 @@ __device__ __forceinline__ SelfPlan self_plan(unsigned char* area, int E, int P,
   sp.list = sp.active + E;
   sp.sigma = sp.list + P;
   sp.misc = sp.sigma + T;
-  sp.wbuf = sp.misc + 8;
   return sp;
 }
 
@@ -264,53 +262,27 @@ __device__ __forceinline__ long long load_id(const StreamArgs& a, int i) {
                    : (long long)static_cast<const int*>(a.sel)[i];
 }
 
-// Exclusive prefix sum over the block (any multiple of 32 threads up to
-// 1024); *total gets the block total.
-__device__ __forceinline__ int block_scan(int v, int* wbuf, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int n = __shfl_up_sync(kFullMask, incl, off);
-    if (lane >= off) incl += n;
-  }
-  if (lane == 31) wbuf[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = lane < nw ? wbuf[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int n = __shfl_up_sync(kFullMask, wi, off);
-      if (lane >= off) wi += n;
-    }
-    if (lane < nw) wbuf[lane] = wi - w;
-    if (lane == 31) wbuf[32] = wi;
-  }
-  __syncthreads();
-  const int r = wbuf[warp] + incl - v;
-  *total = wbuf[32];
-  __syncthreads();
-  return r;
-}
-
 // First unit of CTA b of n under the cost-balanced split (unit (u, tile)
 // costs fixed + tokens of active expert u); the same integer formula as the
-// bucketer's table.
-__device__ __forceinline__ int split_begin(const SelfPlan& sp, int na, int pairs, int64_t rt,
-                                           int fixed, int64_t b, int64_t n) {
+// bucketer's table. Called by a whole warp: each lane tests one active
+// expert of a 32-wide chunk (the cost prefix rises with u, so the experts
+// that qualify form a prefix of the chunk) instead of one thread's binary
+// search over dependent shared-memory loads.
+__device__ __forceinline__ int split_begin_warp(const SelfPlan& sp, int na, int pairs, int64_t rt,
+                                                int fixed, int64_t b, int64_t n, int lane) {
   if (b >= n) return (int)(na * rt);
   const int64_t C = rt * ((int64_t)fixed * na + pairs);   // cost of all units
   if (C == 0) return 0;
   auto cost_before = [&](int u) { return (int64_t)fixed * u + sp.off[sp.active[u]]; };
-  // Largest u with rt * cost_before(u) * n <= b * C.
-  int lo = 0, hi = na - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (rt * cost_before(mid) * n <= b * C) lo = mid;
-    else hi = mid - 1;
+  // Largest u with rt * cost_before(u) * n <= b * C (u = 0 always qualifies).
+  int u = 0;
+  for (int base = 0; base < na; base += 32) {
+    const int v = base + lane;
+    const bool ok = v < na && rt * cost_before(v) * n <= b * C;
+    const unsigned m = __ballot_sync(kFullMask, ok);
+    if (m != 0u) u = base + 31 - __clz(m);
+    if (m != kFullMask) break;
   }
-  const int u = lo;
   const int64_t e = sp.active[u];
   const int64_t cu = fixed + (sp.off[e + 1] - sp.off[e]);
   const int64_t lo_cost = rt * cost_before(u);
@@ -326,15 +298,26 @@ __device__ __forceinline__ void consumers_sync() {
 // The CTA's routing plan, by the whole block: counts, offsets, the active
 // list and this CTA's unit range (what the producer needs).
 __device__ void self_route_plan(const StreamArgs& a, const SelfPlan& sp) {
-  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, P = a.P, T = a.T;
+  // The ids first: their loads are in flight while the counters are zeroed.
+  constexpr int kIdsPerThread = (kSelfMaxPairs + kStreamThreads - 1) / kStreamThreads;
+  long long id[kIdsPerThread];
+#pragma unroll
+  for (int j = 0; j < kIdsPerThread; ++j) {
+    const int i = tid + j * nthr;
+    id[j] = i < P ? load_id(a, i) : -1;
+  }
   for (int e = tid; e < E; e += nthr) sp.off[e] = 0;
   for (int t = tid; t < T; t += nthr) sp.sigma[t] = 0;
   __syncthreads();
   // Counts (order does not matter here); the ids stay in shared memory.
   int bad = 0;
-  for (int i = tid; i < P; i += nthr) {
-    const long long e = load_id(a, i);
+#pragma unroll
+  for (int j = 0; j < kIdsPerThread; ++j) {
+    const int i = tid + j * nthr;
+    if (i >= P) continue;
+    const long long e = id[j];
     const bool valid = e >= 0 && e < E;
     sp.ids[i] = valid ? (int)e : -1;
     if (valid) atomicAdd(&sp.off[e], 1);
@@ -345,41 +328,44 @@ __device__ void self_route_plan(const StreamArgs& a, const SelfPlan& sp) {
   if (lane == 0 && bad > 0 && blockIdx.x == 0)     // every CTA sees them; one counts
     atomicAdd(&a.status[kStatusBadPairs], (unsigned long long)bad);
   __syncthreads();
-  // Offsets and the ascending active list.
-  const int per = (E + nthr - 1) / nthr;
-  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-  int my_pairs = 0, my_active = 0;
-  for (int e = e0; e < e1; ++e) {
-    my_pairs += sp.off[e];
-    my_active += sp.off[e] > 0 ? 1 : 0;
-  }
-  // One scan of both sums: pairs (at most kSelfMaxPairs) from bit 12 up,
-  // active experts (at most kSelfMaxExperts < 4096) below.
-  int total;
-  const int packed = block_scan((my_pairs << 12) | my_active, sp.wbuf, &total);
-  int off = packed >> 12, act = packed & 0xfff;
-  const int total_pairs = total >> 12, total_active = total & 0xfff;
-  for (int e = e0; e < e1; ++e) {
-    const int c = sp.off[e];
-    sp.off[e] = off;
-    if (c > 0) sp.active[act++] = e;
-    off += c;
-  }
-  if (tid == 0) {
-    sp.off[E] = total_pairs;
-    sp.misc[0] = total_active;
-    sp.misc[3] = total_pairs;
+  // Offsets and the ascending active list, by warp 0 alone (lane l owns
+  // experts [l*per, (l+1)*per)): one warp scan of pairs (from bit 12 up, at
+  // most kSelfMaxPairs) and active experts (below, at most kSelfMaxExperts
+  // < 4096) packed in one int.
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int mine = 0;
+    for (int e = e0; e < e1; ++e) mine += (sp.off[e] << 12) | (sp.off[e] > 0 ? 1 : 0);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int total = __shfl_sync(kFullMask, incl, 31);
+    int off = (incl - mine) >> 12, act = (incl - mine) & 0xfff;
+    for (int e = e0; e < e1; ++e) {
+      const int c = sp.off[e];
+      sp.off[e] = off;
+      if (c > 0) sp.active[act++] = e;
+      off += c;
+    }
+    if (lane == 0) {
+      sp.off[E] = total >> 12;
+      sp.misc[0] = total & 0xfff;
+      sp.misc[3] = total >> 12;
+    }
   }
   __syncthreads();
   // This CTA's static range and the start of the shared pool, one boundary
   // per warp: boundary b of n sits at b * static_permille / (1000 n) of the
   // cost.
-  if (lane == 0 && tid < 96) {
-    const int w = tid >> 5;
-    const int64_t b = w == 0 ? blockIdx.x : w == 1 ? blockIdx.x + 1 : gridDim.x;
-    sp.misc[w == 2 ? 4 : 1 + w] =
-        split_begin(sp, total_active, total_pairs, a.row_tiles, a.fixed_cost,
-                    b * a.static_permille, (int64_t)gridDim.x * 1000);
+  if (warp < 3) {
+    const int64_t b = warp == 0 ? blockIdx.x : warp == 1 ? blockIdx.x + 1 : gridDim.x;
+    const int v = split_begin_warp(sp, sp.misc[0], sp.misc[3], a.row_tiles, a.fixed_cost,
+                                   b * a.static_permille, (int64_t)gridDim.x * 1000, lane);
+    if (lane == 0) sp.misc[warp == 2 ? 4 : 1 + warp] = v;
   }
   __syncthreads();
 }
