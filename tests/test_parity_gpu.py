@@ -324,12 +324,16 @@ def test_no_kernel_wait_timed_out():
     assert wait_timeouts() == 0
 
 
-def test_combine_vector_and_scalar_paths_agree_bitwise():
-    # The combine has a 16-byte vector path (width a multiple of 4, aligned
+@pytest.mark.parametrize("T,E,K,I,O", [
+    (24, 6, 3, 256, 64),      # GEMV partials, several columns
+    (4096, 8, 4, 256, 512),   # tensor-core partials, many segments per warp
+])
+def test_combine_vector_and_scalar_paths_agree_bitwise(T, E, K, I, O):
+    # The combine has 16-byte vector paths (width a multiple of 4, aligned
     # buffers) and an elementwise path. A shared-output view that starts one
     # element into its storage is misaligned and takes the elementwise path;
-    # both evaluate the same expression in the same order.
-    wl = workloads.make(24, 6, 3, 256, 64, dtype=torch.bfloat16, seed=41)
+    # all evaluate the same expression in the same order.
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, seed=41)
     d = wl.device_tensors("cuda")
     a = mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"], d["y_shared"])
     store = torch.empty(wl.T * wl.O + 1, dtype=torch.bfloat16, device="cuda")
@@ -376,3 +380,26 @@ def test_self_routed_gemv_matches_bucketer_bitwise(monkeypatch, dtype, idx):
     assert torch.equal(a, b)
     want, absm, _ = oracle_rows(wl, sel=sel)
     assert_parity(a, want, absm, dtype, "self-routed")
+
+
+@pytest.mark.parametrize("name", ["decode", "wide_decode", "prefill"])
+def test_poisoned_workspace(name):
+    # A caller workspace full of 0xFF bytes: the GEMV's pool counter reads -1
+    # and every partial result NaN until written. The results must not
+    # depend on it: every unit is claimed and every partial written, on
+    # repeated calls.
+    from mxfp4_routed_expert_route_gb300 import workspace_size
+    wl = workloads.named(name)
+    d = wl.device_tensors("cuda")
+    n = workspace_size(wl.T, wl.E, wl.I, wl.O, wl.K, wl.dtype)
+    rows = np.array([0, wl.T // 3, wl.T - 1])
+    want, absm, _ = oracle_rows(wl, rows=rows)
+    r = torch.from_numpy(rows).cuda()
+    for _ in range(3):
+        ws = torch.full((max(n, 1),), 0xFF, dtype=torch.uint8, device="cuda")
+        out = mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"],
+                                  d["y_shared"], workspace=ws)
+        torch.cuda.synchronize()
+        assert wait_timeouts() == 0
+        assert torch.isfinite(out.float()).all()
+        assert_parity(out[r], want, absm, wl.dtype, f"{name}, poisoned workspace")
