@@ -283,6 +283,48 @@ def run_reference(args, rank):
 
 
 # ---------------------------------------------------------------- ours -----
+def measure_router(wl, d, dev, stream, flush, warmup, n, peaks):
+    """The router that feeds the linear (sigmoid top-K from logits, seeded
+    N(0,1) float32 logits, zero bias so that the routing is as balanced as
+    the workload's own picks): alone, and fused with the linear in one
+    library call; CUDA events on the stream, L2 flushed before each call,
+    medians."""
+    import torch
+    from mxfp4_routed_expert_route_gb300 import mxfp4_expert_linear_routed, router_topk
+    g = torch.Generator().manual_seed(1000 + wl.meta["seed"])
+    lg = torch.randn(wl.T, wl.E, generator=g).to(dev)
+    bias = torch.zeros(wl.E, device=dev)
+    out = torch.empty((wl.T, wl.O), dtype=wl.dtype, device=dev)
+
+    def routed():
+        mxfp4_expert_linear_routed(d["x"], d["packed"], d["scales"], lg, bias, wl.K,
+                                   d["y_shared"], out=out)
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        ev = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize(dev)
+        ts = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+        return ts[len(ts) // 2]
+
+    us = timed(lambda: router_topk(lg, bias, wl.K))
+    routed_us = timed(routed)
+    nbytes = wl.T * wl.E * 4 + wl.E * 4 + wl.T * wl.K * 8
+    gbps = nbytes / (us * 1e-6) / 1e9
+    return {"us": us, "bytes": nbytes, "gbps": gbps, "frac_of_hbm": gbps / peaks["hbm_gbs"],
+            "routed_call_us": routed_us,
+            "inputs": "seeded N(0,1) float32 logits, zero bias, scaling 1"}
+
+
 def run_ours(args, rank, world):
     import ctypes
 
@@ -394,9 +436,10 @@ def run_ours(args, rank, world):
     h2d = sum(t.numel() * t.element_size() for t in (x_h, sel_h, p_h, ys_h))
     d2h = out_h.numel() * out_h.element_size()
 
+    peaks, peaks_src = load_peaks()
+    router = measure_router(wl, d, dev, stream, flush, W, min(K, 200), peaks)
     if rank != 0:
         return
-    peaks, peaks_src = load_peaks()
     gemm = lib.mxfp4el_linear_path(wl.T, wl.E, wl.I, wl.O, wl.K,
                                    _native.DTYPE_BF16 if token_bytes(wl) == 2
                                    else _native.DTYPE_F32) == _native.PATH_GEMM
@@ -455,6 +498,7 @@ def run_ours(args, rank, world):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_max / K * 1e3},
         "gpu_launches": int(launches),
+        "router": router,
         "clocks": clocks,
         "wall_s": wall,
     }

@@ -105,6 +105,49 @@ int mxfp4_expert_linear(const void* latent_tokens,
                         void* stream);
 
 /*
+ * mxfp4_router_topk -- the sigmoid top-K router that feeds the routed expert
+ * linear ("MoE Expert Kernels: Grouped Prefill and Mixed-Quant Compact
+ * Experts", section 1, the sigmoid router; the Hy3 decode write-up, the
+ * router after its logits).
+ *
+ * router_logits (T, E) float32, row-major; router_bias (E) float32 or NULL
+ * (no bias). Per token: score = sigmoid(logit) in float32, choice = score +
+ * bias; selected_experts (T, K) int32 receives the K experts of highest
+ * choice, highest first, ties to the lower index; mixture_weights (T, K)
+ * float32 receives their raw scores (the bias steers the choice only),
+ * summed left to right, each divided by that sum plus 1e-20 and multiplied by
+ * `scaling`. An expert whose choice is NaN is never selected; a slot left
+ * without an expert gets id -1 (skipped by the linear) and weight 0.
+ * All pointers are device pointers owned by the caller; the outputs may not
+ * overlap the inputs or each other (MXFP4EL_ERR_ALIAS). Requires
+ * 0 <= K <= E and (2E + K) * 4 <= 49152 bytes (MXFP4EL_ERR_TOO_LARGE
+ * beyond). Stream-ordered on `stream`; returns MXFP4EL_OK or a negative code.
+ */
+int mxfp4_router_topk(const float* router_logits, const float* router_bias,
+                      int64_t T, int64_t E, int64_t K, float scaling,
+                      int32_t* selected_experts, float* mixture_weights,
+                      void* stream);
+
+/*
+ * mxfp4_expert_linear_routed -- the router above, then the routed expert
+ * linear on its selection, on one stream: selected_experts (T, K) int32 and
+ * mixture_weights (T, K) float32 are caller-owned outputs of the router and
+ * inputs of the linear (the linear's first kernel waits for the router).
+ * Every other argument, and the result in `out`, as mxfp4_expert_linear with
+ * index_dtype MXFP4EL_INDEX_I32. All arguments are checked before anything is
+ * enqueued.
+ */
+int mxfp4_expert_linear_routed(const void* latent_tokens,
+                               const uint8_t* packed_weights,
+                               const uint8_t* scale_bytes,
+                               const float* router_logits,
+                               const float* router_bias, float scaling,
+                               const void* shared_output, void* out,
+                               int32_t* selected_experts, float* mixture_weights,
+                               int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                               int token_dtype, void* stream);
+
+/*
  * Bytes of scratch one call of these sizes needs when the caller supplies it
  * (mxfp4_expert_linear_with_workspace). Returns 0 for a no-op call and
  * (size_t)-1 for sizes the library rejects.

@@ -21,7 +21,7 @@ import torch
 from . import _native
 
 __all__ = ["mxfp4_expert_linear", "workspace_size", "device_errors", "wait_timeouts",
-           "LibraryNotBuilt", "MXFP4Error"]
+           "LibraryNotBuilt", "MXFP4Error", "router_topk", "mxfp4_expert_linear_routed"]
 
 LibraryNotBuilt = _native.LibraryNotBuilt
 MXFP4Error = _native.MXFP4Error
@@ -106,6 +106,80 @@ def mxfp4_expert_linear(latent_tokens: torch.Tensor, packed_weights: torch.Tenso
             _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream))
     _native.check(rc, "mxfp4_expert_linear")
     return out
+
+
+def _router_args(router_logits, router_bias, K):
+    lg = router_logits
+    if not lg.is_cuda or lg.dtype != torch.float32 or lg.dim() != 2:
+        raise ValueError("router_logits must be a (T, E) float32 CUDA tensor")
+    T, E = lg.shape
+    if router_bias is not None:
+        if (router_bias.device != lg.device or router_bias.dtype != torch.float32
+                or tuple(router_bias.shape) != (E,)):
+            raise ValueError("router_bias must be an (E,) float32 tensor on the logits' device")
+        router_bias = router_bias.contiguous()
+    if not 0 <= K <= E:
+        raise ValueError("need 0 <= K <= E")
+    return lg.contiguous(), router_bias, T, E
+
+
+def router_topk(router_logits: torch.Tensor, router_bias: torch.Tensor | None, K: int,
+                scaling: float = 1.0) -> tuple[torch.Tensor, torch.Tensor]:
+    """(selected_experts (T, K) int32, mixture_weights (T, K) float32): the K
+    experts of highest sigmoid(logit) + bias per token, highest first, ties to
+    the lower index, weighted by their raw scores normalised to sum to
+    ``scaling`` (see mxfp4_router_topk in the C header)."""
+    lg, b, T, E = _router_args(router_logits, router_bias, K)
+    sel = torch.empty((T, K), dtype=torch.int32, device=lg.device)
+    p = torch.empty((T, K), dtype=torch.float32, device=lg.device)
+    stream = torch.cuda.current_stream(lg.device).cuda_stream
+    with torch.cuda.device(lg.device):
+        rc = _native.load().mxfp4_router_topk(_ptr(lg), _ptr(b), T, E, K, ctypes.c_float(scaling),
+                                              _ptr(sel), _ptr(p), ctypes.c_void_p(stream))
+    _native.check(rc, "mxfp4_router_topk")
+    return sel, p
+
+
+def mxfp4_expert_linear_routed(latent_tokens: torch.Tensor, packed_weights: torch.Tensor,
+                               scale_bytes: torch.Tensor, router_logits: torch.Tensor,
+                               router_bias: torch.Tensor | None, K: int,
+                               shared_output: torch.Tensor, scaling: float = 1.0,
+                               out: torch.Tensor | None = None
+                               ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(out, selected_experts, mixture_weights): the router, then the routed
+    expert linear on its selection, in one library call on the current
+    stream. Shapes as in :func:`mxfp4_expert_linear` and :func:`router_topk`."""
+    lg, b, T, E = _router_args(router_logits, router_bias, K)
+    x, w, s, ys = latent_tokens, packed_weights, scale_bytes, shared_output
+    if x.dtype not in _TOKEN_DTYPES or ys.dtype != x.dtype:
+        raise TypeError("tokens and shared_output must share a supported dtype")
+    if w.dim() != 4 or tuple(w.shape[:1]) != (E,) or x.dim() != 2 or x.shape[0] != T:
+        raise ValueError("expected x (T, I) and packed (E, O, I/32, 16) matching the logits")
+    if w.dtype != torch.uint8 or s.dtype != torch.uint8:
+        raise TypeError("packed_weights and scale_bytes must be uint8")
+    I = x.shape[1]
+    O = w.shape[1]
+    if tuple(w.shape) != (E, O, I // 32, 16) or tuple(s.shape) != (E, O, I // 32) \
+            or tuple(ys.shape) != (T, O):
+        raise ValueError("packed, scale or shared-output shape mismatch")
+    for t in (w, s, ys):
+        if t.device != lg.device or not x.is_cuda or x.device != lg.device:
+            raise ValueError("all tensors must be on the logits' CUDA device")
+    x, w, s, ys = (t.contiguous() for t in (x, w, s, ys))
+    if out is None:
+        out = torch.empty((T, O), dtype=x.dtype, device=x.device)
+    elif out.shape != (T, O) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous (T, O) tensor of the token dtype")
+    sel = torch.empty((T, K), dtype=torch.int32, device=x.device)
+    p = torch.empty((T, K), dtype=torch.float32, device=x.device)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    with torch.cuda.device(x.device):
+        rc = _native.load().mxfp4_expert_linear_routed(
+            _ptr(x), _ptr(w), _ptr(s), _ptr(lg), _ptr(b), ctypes.c_float(scaling), _ptr(ys),
+            _ptr(out), _ptr(sel), _ptr(p), T, E, I, O, K, _TOKEN_DTYPES[x.dtype],
+            ctypes.c_void_p(stream))
+    _native.check(rc, "mxfp4_expert_linear_routed")
+    return out, sel, p
 
 
 def device_errors(device=None) -> int:

@@ -56,6 +56,9 @@ SIGNATURES = {
     "mxfp4el_linear_path": (_INT, [_I64, _I64, _I64, _I64, _I64, _INT]),
     "mxfp4el_status_string": (ctypes.c_char_p, [_INT]),
     "mxfp4el_version": (_INT, []),
+    "mxfp4_router_topk": (_INT, [_P, _P, _I64, _I64, _I64, ctypes.c_float, _P, _P, _P]),
+    "mxfp4_expert_linear_routed": (_INT, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P,
+                                          _P, _I64, _I64, _I64, _I64, _I64, _INT, _P]),
 }
 
 _lock = threading.Lock()

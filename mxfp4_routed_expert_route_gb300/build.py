@@ -20,7 +20,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libmxfp4_expert_linear.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "route.cu", "gemv.cu", "gemm_tc.cu", "combine.cu", "static_scratch.cu"]
+SOURCES = ["api.cu", "route.cu", "gemv.cu", "gemm_tc.cu", "combine.cu", "static_scratch.cu",
+           "router.cu"]
 
 
 def nvcc() -> str:

@@ -285,6 +285,55 @@ extern "C" int mxfp4_expert_linear(const void* latent_tokens,
              index_dtype, ws, s);
 }
 
+extern "C" int mxfp4_router_topk(const float* router_logits, const float* router_bias,
+                                 int64_t T, int64_t E, int64_t K, float scaling,
+                                 int32_t* selected_experts, float* mixture_weights,
+                                 void* stream) {
+  if (T < 0 || E < 0 || K < 0 || K > E) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (T > kMaxDim || E > kMaxDim || (K > 0 && T > kMaxPairs / K)) return MXFP4EL_ERR_TOO_LARGE;
+  if (T == 0 || K == 0) return MXFP4EL_OK;
+  if (router_logits == nullptr || selected_experts == nullptr || mixture_weights == nullptr)
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (router_warps_per_block(E, K) <= 0) return MXFP4EL_ERR_TOO_LARGE;
+  const size_t nl = (size_t)T * E * sizeof(float), nb = (size_t)E * sizeof(float);
+  const size_t ns = (size_t)T * K * sizeof(int32_t), np = (size_t)T * K * sizeof(float);
+  if (overlaps(selected_experts, ns, router_logits, nl) ||
+      overlaps(selected_experts, ns, router_bias, nb) ||
+      overlaps(mixture_weights, np, router_logits, nl) ||
+      overlaps(mixture_weights, np, router_bias, nb) ||
+      overlaps(selected_experts, ns, mixture_weights, np))
+    return MXFP4EL_ERR_ALIAS;
+  return launch_router(router_logits, router_bias, T, E, K, scaling, selected_experts,
+                       mixture_weights, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MXFP4EL_OK
+             : MXFP4EL_ERR_CUDA;
+}
+
+extern "C" int mxfp4_expert_linear_routed(const void* latent_tokens,
+                                          const uint8_t* packed_weights,
+                                          const uint8_t* scale_bytes,
+                                          const float* router_logits,
+                                          const float* router_bias, float scaling,
+                                          const void* shared_output, void* out,
+                                          int32_t* selected_experts, float* mixture_weights,
+                                          int64_t T, int64_t E, int64_t I, int64_t O,
+                                          int64_t K, int token_dtype, void* stream) {
+  // Check the linear's arguments first: nothing is enqueued for a call that
+  // would fail half way.
+  int rc = validate(latent_tokens, packed_weights, scale_bytes, selected_experts,
+                    mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
+                    MXFP4EL_INDEX_I32);
+  if (rc != MXFP4EL_OK) return rc;
+  if (K > E) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (T == 0 || O == 0) return MXFP4EL_OK;
+  rc = mxfp4_router_topk(router_logits, router_bias, T, E, K, scaling, selected_experts,
+                         mixture_weights, stream);
+  if (rc != MXFP4EL_OK) return rc;
+  return mxfp4_expert_linear(latent_tokens, packed_weights, scale_bytes, selected_experts,
+                             mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
+                             MXFP4EL_INDEX_I32, stream);
+}
+
 extern "C" int mxfp4el_device_errors(void* stream, int64_t* bad_pairs) {
   if (bad_pairs == nullptr) return MXFP4EL_ERR_INVALID_ARGUMENT;
   return read_and_reset_status(static_cast<cudaStream_t>(stream), kStatusBadPairs,

@@ -152,6 +152,16 @@ cudaError_t launch_combine(const void* y_shared, const void* sel,
                            int64_t E, int64_t O, int64_t K, bool after_linear,
                            cudaStream_t stream);
 
+// Sigmoid top-K router (router.cu): one warp per token, the warp's raw,
+// choice and chosen scores in shared memory.
+constexpr int kRouterThreads = 256;
+constexpr int64_t kRouterSmemLimit = 48 * 1024;
+// Warps per block whose shared memory fits (0: 2E + K too large).
+int router_warps_per_block(int64_t E, int64_t K);
+cudaError_t launch_router(const float* logits, const float* bias, int64_t T, int64_t E,
+                          int64_t K, float scaling, int32_t* sel, float* p,
+                          cudaStream_t stream);
+
 // Device address of the status words on the current device.
 unsigned long long* device_status_words();
 

@@ -130,3 +130,21 @@ def test_linear_path_choice(lib):
     assert path(4096, 128, 2848, 5760, 4, n.DTYPE_BF16) == n.PATH_GEMV     # G odd
     assert path(640, 512, 64, 48, 16, n.DTYPE_BF16) == n.PATH_GEMM
     assert path(640, 600, 64, 48, 16, n.DTYPE_BF16) == n.PATH_GEMV         # > 512 experts
+
+
+def test_router_argument_checks(lib):
+    # Checked before anything is enqueued: no GPU needed. Codes: -1 invalid
+    # argument, -3 alias, -6 too large.
+    P = ctypes.c_void_p
+    f = ctypes.c_float(1.0)
+    # K > E
+    assert lib.mxfp4_router_topk(P(4096), None, 4, 3, 4, f, P(8192), P(16384), None) == -1
+    # missing outputs
+    assert lib.mxfp4_router_topk(P(4096), None, 4, 8, 2, f, None, P(16384), None) == -1
+    # the weights overlap the logits
+    assert lib.mxfp4_router_topk(P(4096), None, 4, 8, 2, f, P(1 << 20), P(4096 + 16), None) == -3
+    # E + K beyond the shared-memory limit
+    assert lib.mxfp4_router_topk(P(4096), None, 1, 20000, 4, f, P(1 << 30), P(1 << 31), None) == -6
+    # nothing to do
+    assert lib.mxfp4_router_topk(None, None, 0, 8, 2, f, None, None, None) == 0
+    assert lib.mxfp4_router_topk(None, None, 5, 8, 0, f, None, None, None) == 0
