@@ -325,6 +325,56 @@ def measure_router(wl, d, dev, stream, flush, warmup, n, peaks):
             "inputs": "seeded N(0,1) float32 logits, zero bias, scaling 1"}
 
 
+SWIGLU_FOR = {"decode": "swiglu_decode", "prefill": "swiglu_prefill"}
+
+
+def measure_swiglu(name, dev, stream, flush, warmup, n, peaks):
+    """The whole routed SwiGLU expert (gate/up linear, SwiGLU, down linear,
+    combine) at the layer shape of the named workload: one library call, CUDA
+    events on the stream, L2 flushed before each call, median. Its roofline
+    is the slower of the algorithmic bytes (selected experts' gate/up and
+    down bytes and scales, tokens, shared output, output, routing) at HBM
+    bandwidth and its FLOPs at the bf16 peak."""
+    import torch
+    from mxfp4_routed_expert_route_gb300 import (mxfp4_swiglu_expert, swiglu_workspace_size,
+                                                 workloads)
+    wl = workloads.named_swiglu(name)
+    d = wl.device_tensors(dev)
+    out = torch.empty((wl.T, wl.O), dtype=wl.dtype, device=dev)
+    ws = torch.empty(max(1, swiglu_workspace_size(wl.T, wl.E, wl.I, wl.F, wl.O, wl.K,
+                                                  wl.dtype)), dtype=torch.uint8, device=dev)
+
+    def call():
+        mxfp4_swiglu_expert(*[d[k] for k in wl.ARGS], out=out, workspace=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    ev = []
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize(dev)
+    ts = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+    us = ts[len(ts) // 2]
+    U = workloads.experts_touched(wl.sel, wl.E)
+    bx = token_bytes(wl)
+    per_expert = 2 * wl.F * (wl.I // 32) * 17 + wl.O * (wl.F // 32) * 17
+    nbytes = (U * per_expert + wl.T * wl.I * bx + 2 * wl.T * wl.O * bx + wl.T * wl.K * 8)
+    flops = 2 * wl.T * wl.K * (2 * wl.F * wl.I + wl.O * wl.F)
+    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    hbm = nbytes / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12)
+    return {"workload": name, "T": wl.T, "E": wl.E, "K": wl.K, "I": wl.I, "F": wl.F,
+            "O": wl.O, "experts_touched": U, "us": us, "bytes_alg": nbytes, "flops_alg": flops,
+            "gbps": nbytes / (us * 1e-6) / 1e9, "tflops": flops / (us * 1e-6) / 1e12,
+            "bound": "hbm" if hbm else "tensor", "t_roof_us": t_roof * 1e6,
+            "frac": t_roof / (us * 1e-6)}
+
+
 def run_ours(args, rank, world):
     import ctypes
 
@@ -438,6 +488,8 @@ def run_ours(args, rank, world):
 
     peaks, peaks_src = load_peaks()
     router = measure_router(wl, d, dev, stream, flush, W, min(K, 200), peaks)
+    swiglu = (measure_swiglu(SWIGLU_FOR[wl.name], dev, stream, flush, W, min(K, 100), peaks)
+              if wl.name in SWIGLU_FOR else None)
     if rank != 0:
         return
     gemm = lib.mxfp4el_linear_path(wl.T, wl.E, wl.I, wl.O, wl.K,
@@ -499,6 +551,7 @@ def run_ours(args, rank, world):
                 "ms_per_step": e2e_max / K * 1e3},
         "gpu_launches": int(launches),
         "router": router,
+        "swiglu_expert": swiglu,
         "clocks": clocks,
         "wall_s": wall,
     }

@@ -179,6 +179,66 @@ int mxfp4_expert_linear_with_workspace(const void* latent_tokens,
                                        void* stream);
 
 /*
+ * mxfp4_swiglu_expert -- the whole routed SwiGLU expert with MXFP4 weights
+ * ("MoE Expert Kernels: Grouped Prefill and Mixed-Quant Compact Experts",
+ * section 1, the expert shape: down(silu(gate(x)) * up(x)) per routed expert,
+ * accumulated with the routing weight in float32; the Hy3 decode write-up:
+ * gate and up stacked along their output rows, one gathered row per
+ * token-expert pair):
+ *
+ *   g = Wg_e x_t,  u = Wu_e x_t          (gate/up: rows 0..F-1 and F..2F-1)
+ *   h[f] = silu(g[f]) * u[f],  silu(v) = v / (1 + exp(-v))
+ *   out[t, :] = shared_output[t, :] + sum_{k < K} p[t, k] * Wd_e h,  e = sel[t, k]
+ *
+ * Every matrix decodes as in mxfp4_expert_linear. Layouts (dense, row-major):
+ *   latent_tokens   (T, I)                 token dtype
+ *   gate_up_packed  (E, 2F, I/32, 16)      uint8; rows 0..F-1 gate, F..2F-1 up
+ *   gate_up_scales  (E, 2F, I/32)          uint8
+ *   down_packed     (E, O, F/32, 16)       uint8
+ *   down_scales     (E, O, F/32)           uint8
+ *   selected_experts, mixture_weights, shared_output, out: as mxfp4_expert_linear.
+ * I and F are positive multiples of 32. g and u are float32 sums; h is
+ * computed in float32 and rounded once to the token dtype (the down
+ * projection's input); the K contributions are added in slot order in
+ * float32 and rounded once, so a call is deterministic.
+ *
+ * Ids outside [0, E): the pair contributes nothing and is counted once per
+ * call for mxfp4el_device_errors(). Scratch is library-owned exactly as for
+ * mxfp4_expert_linear (the same grow-only buffer per device and stream).
+ * All pointers are caller-owned device pointers; out may not overlap an
+ * input (MXFP4EL_ERR_ALIAS); latent_tokens, gate_up_packed and down_packed
+ * must be 16-byte aligned. Returns MXFP4EL_OK or a negative code, checked
+ * before anything is enqueued except MXFP4EL_ERR_CUDA.
+ */
+int mxfp4_swiglu_expert(const void* latent_tokens,
+                        const uint8_t* gate_up_packed, const uint8_t* gate_up_scales,
+                        const uint8_t* down_packed, const uint8_t* down_scales,
+                        const void* selected_experts, const float* mixture_weights,
+                        const void* shared_output, void* out,
+                        int64_t T, int64_t E, int64_t I, int64_t F, int64_t O, int64_t K,
+                        int token_dtype, int index_dtype, void* stream);
+
+/* Bytes of caller-owned scratch for mxfp4_swiglu_expert_with_workspace: 0 for
+ * a no-op call, (size_t)-1 for sizes the library rejects. */
+size_t mxfp4_swiglu_expert_workspace_size(int64_t T, int64_t E, int64_t I, int64_t F,
+                                          int64_t O, int64_t K, int token_dtype);
+
+/* mxfp4_swiglu_expert with caller-owned scratch, with the rules of
+ * mxfp4_expert_linear_with_workspace. */
+int mxfp4_swiglu_expert_with_workspace(const void* latent_tokens,
+                                       const uint8_t* gate_up_packed,
+                                       const uint8_t* gate_up_scales,
+                                       const uint8_t* down_packed,
+                                       const uint8_t* down_scales,
+                                       const void* selected_experts,
+                                       const float* mixture_weights,
+                                       const void* shared_output, void* out,
+                                       int64_t T, int64_t E, int64_t I, int64_t F,
+                                       int64_t O, int64_t K, int token_dtype,
+                                       int index_dtype, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
  * mxfp4_expert_linear_static_scratch -- the same operation for callers that
  * cannot allocate device memory (for example a serving process whose memory
  * budget is fixed at start-up, or a plugin of a host framework that owns

@@ -21,7 +21,8 @@ import torch
 from . import _native
 
 __all__ = ["mxfp4_expert_linear", "workspace_size", "device_errors", "wait_timeouts",
-           "LibraryNotBuilt", "MXFP4Error", "router_topk", "mxfp4_expert_linear_routed"]
+           "LibraryNotBuilt", "MXFP4Error", "router_topk", "mxfp4_expert_linear_routed",
+           "mxfp4_swiglu_expert", "swiglu_workspace_size"]
 
 LibraryNotBuilt = _native.LibraryNotBuilt
 MXFP4Error = _native.MXFP4Error
@@ -180,6 +181,78 @@ def mxfp4_expert_linear_routed(latent_tokens: torch.Tensor, packed_weights: torc
             ctypes.c_void_p(stream))
     _native.check(rc, "mxfp4_expert_linear_routed")
     return out, sel, p
+
+
+def swiglu_workspace_size(T: int, E: int, I: int, F: int, O: int, K: int,
+                          dtype: torch.dtype) -> int:
+    """Scratch bytes of one :func:`mxfp4_swiglu_expert` call of these sizes."""
+    n = _native.load().mxfp4_swiglu_expert_workspace_size(T, E, I, F, O, K,
+                                                          _TOKEN_DTYPES[dtype])
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("sizes rejected by the library")
+    return int(n)
+
+
+def mxfp4_swiglu_expert(latent_tokens: torch.Tensor, gate_up_packed: torch.Tensor,
+                        gate_up_scales: torch.Tensor, down_packed: torch.Tensor,
+                        down_scales: torch.Tensor, selected_experts: torch.Tensor,
+                        mixture_weights: torch.Tensor, shared_output: torch.Tensor,
+                        out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """The routed SwiGLU expert: out[t] = shared_output[t] + sum_k p[t,k] *
+    Wd_e (silu(Wg_e x_t) * (Wu_e x_t)), e = selected_experts[t, k].
+
+    Shapes: latent_tokens (T, I); gate_up_packed (E, 2F, I/32, 16) uint8 with
+    the gate rows first, gate_up_scales (E, 2F, I/32); down_packed
+    (E, O, F/32, 16), down_scales (E, O, F/32); routing and shared output as
+    in :func:`mxfp4_expert_linear`. All on one CUDA device."""
+    x, gw, gs, dw, ds = latent_tokens, gate_up_packed, gate_up_scales, down_packed, down_scales
+    sel, p, ys = selected_experts, mixture_weights, shared_output
+    if not x.is_cuda:
+        raise ValueError("latent_tokens must be a CUDA tensor")
+    dev = x.device
+    for name, t in (("gate_up_packed", gw), ("gate_up_scales", gs), ("down_packed", dw),
+                    ("down_scales", ds), ("selected_experts", sel),
+                    ("mixture_weights", p), ("shared_output", ys)):
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, tokens on {dev}")
+    if x.dtype not in _TOKEN_DTYPES or ys.dtype != x.dtype:
+        raise TypeError("tokens and shared_output must share a supported dtype")
+    if any(t.dtype != torch.uint8 for t in (gw, gs, dw, ds)):
+        raise TypeError("packed weights and scale bytes must be uint8")
+    if sel.dtype not in _INDEX_DTYPES or p.dtype != torch.float32:
+        raise TypeError("selected_experts must be int32/int64, mixture_weights float32")
+    if x.dim() != 2 or gw.dim() != 4 or dw.dim() != 4 or sel.dim() != 2:
+        raise ValueError("expected x (T,I), packed (E,2F,I/32,16), (E,O,F/32,16), sel (T,K)")
+    T, I = x.shape
+    E, F2, Gi, _ = gw.shape
+    F = F2 // 2
+    O, Gf = dw.shape[1], dw.shape[2]
+    K = sel.shape[1]
+    if (F2 % 2 or tuple(gw.shape) != (E, 2 * F, I // 32, 16) or I % 32
+            or tuple(gs.shape) != (E, 2 * F, I // 32)
+            or tuple(dw.shape) != (E, O, F // 32, 16) or F % 32 or Gf * 32 != F
+            or tuple(ds.shape) != (E, O, F // 32)):
+        raise ValueError("gate/up or down weight shapes do not match")
+    if tuple(sel.shape) != (T, K) or tuple(p.shape) != (T, K) or tuple(ys.shape) != (T, O):
+        raise ValueError("routing or shared-output shape mismatch")
+    x, gw, gs, dw, ds, sel, p, ys = (t.contiguous() for t in (x, gw, gs, dw, ds, sel, p, ys))
+    if out is None:
+        out = torch.empty((T, O), dtype=x.dtype, device=dev)
+    elif out.shape != (T, O) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous (T, O) tensor of the token dtype")
+    lib = _native.load()
+    ws_bytes = swiglu_workspace_size(T, E, I, F, O, K, x.dtype)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        rc = lib.mxfp4_swiglu_expert_with_workspace(
+            _ptr(x), _ptr(gw), _ptr(gs), _ptr(dw), _ptr(ds), _ptr(sel), _ptr(p), _ptr(ys),
+            _ptr(out), T, E, I, F, O, K, _TOKEN_DTYPES[x.dtype], _INDEX_DTYPES[sel.dtype],
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream))
+    _native.check(rc, "mxfp4_swiglu_expert")
+    return out
 
 
 def device_errors(device=None) -> int:

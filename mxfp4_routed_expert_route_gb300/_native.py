@@ -59,6 +59,12 @@ SIGNATURES = {
     "mxfp4_router_topk": (_INT, [_P, _P, _I64, _I64, _I64, ctypes.c_float, _P, _P, _P]),
     "mxfp4_expert_linear_routed": (_INT, [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P,
                                           _P, _I64, _I64, _I64, _I64, _I64, _INT, _P]),
+    "mxfp4_swiglu_expert": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64,
+                                   _I64, _I64, _I64, _INT, _INT, _P]),
+    "mxfp4_swiglu_expert_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I64, _INT]),
+    "mxfp4_swiglu_expert_with_workspace": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64,
+                                                  _I64, _I64, _I64, _I64, _I64, _INT, _INT,
+                                                  _P, _SZ, _P]),
 }
 
 _lock = threading.Lock()

@@ -1,5 +1,7 @@
 // api.cu -- the C ABI (include/mxfp4_expert_linear.h): argument checks,
-// workspace, and the launch sequence route -> GEMV -> combine on one stream.
+// workspace, and the launch sequences on one stream: route -> linear (GEMV or
+// GEMM) -> combine; router -> that; and for the SwiGLU expert gate/up linear
+// -> SwiGLU -> down linear -> combine.
 #include <algorithm>
 #include <atomic>
 #include <cstdlib>
@@ -83,7 +85,7 @@ void mark(int stage, bool begin, cudaStream_t stream) {
 }  // namespace
 
 LinearPath choose_path(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype) {
-  const bool tc_ok = token_dtype == MXFP4EL_DTYPE_BF16 && gemm_tc_supported(E, I, O);
+  const bool tc_ok = token_dtype == MXFP4EL_DTYPE_BF16 && E > 0 && gemm_tc_supported(E, I, O);
   // Test knob: MXFP4EL_PATH=gemv or gemm forces a kernel where it applies.
   if (const char* env = std::getenv("MXFP4EL_PATH")) {
     if (std::strcmp(env, "gemv") == 0) return LinearPath::kGemv;
@@ -106,51 +108,164 @@ int linear_partial_columns(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K
 
 namespace {
 
+// Route and linear for K > 0: the float32 partial results land in ws.part
+// (linear_partial_columns() columns per pair).
+cudaError_t run_linear(const void* x, const uint8_t* packed, const uint8_t* scales,
+                       const void* sel, int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                       int token_dtype, int index_dtype, const Workspace& ws,
+                       cudaStream_t stream) {
+  unsigned long long* status = device_status_words();
+  if (status == nullptr) return cudaErrorUnknown;
+  if (E == 0) {
+    // Every id is out of range: the bucketer counts them, nothing else runs.
+    mark(MXFP4EL_STAGE_ROUTE, true, stream);
+    const cudaError_t err = launch_route(sel, index_dtype, T, K, 0, ws.wc_global, ws.plan,
+                                         TokenPrep{nullptr, nullptr, nullptr, I},
+                                         UnitSplit{0, 0, 0, 1000}, stream);
+    mark(MXFP4EL_STAGE_ROUTE, false, stream);
+    return err;
+  }
+  const bool gemm = choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
+  // Small batches on the GEMV: each GEMV CTA routes for itself.
+  const bool self = !gemm && gemv_self_route(T, E, I, O, K);
+  const bool prep = !gemm && !self && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
+  const bool prep_in_route = prep && prep_fits_route(T, I);
+  TokenPrep tp = {prep_in_route ? x : nullptr, ws.x16, ws.sigma, I};
+  const UnitSplit split = gemm ? UnitSplit{0, 0, 0, 1000} : gemv_unit_split(T, E, I, O, K);
+  mark(MXFP4EL_STAGE_ROUTE, true, stream);
+  cudaError_t err = cudaSuccess;
+  if (!self)
+    err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, tp, split, stream);
+  if (err == cudaSuccess && prep && !prep_in_route)
+    err = launch_prep_tokens(x, ws.x16, ws.sigma, T, I, stream);
+  mark(MXFP4EL_STAGE_ROUTE, false, stream);
+  if (err != cudaSuccess) return err;
+  if (gemm) {
+    mark(MXFP4EL_STAGE_GATHER, true, stream);
+    err = launch_gather_tokens(x, ws.plan, ws.grouped, T, I, K, stream);
+    mark(MXFP4EL_STAGE_GATHER, false, stream);
+    if (err != cudaSuccess) return err;
+  }
+  mark(MXFP4EL_STAGE_LINEAR, true, stream);
+  if (gemm)
+    err = launch_gemm_tc(x, packed, scales, ws.plan, ws.grouped, ws.part, status, T, E, I, O, K,
+                         stream);
+  else
+    err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, sel, index_dtype, packed, scales,
+                      ws.plan, ws.part, status, T, E, I, O, K, stream);
+  mark(MXFP4EL_STAGE_LINEAR, false, stream);
+  return err;
+}
+
 int run(const void* x, const uint8_t* packed, const uint8_t* scales,
         const void* sel, const float* p, const void* ys, void* out, int64_t T,
         int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype,
         int index_dtype, const Workspace& ws, cudaStream_t stream) {
-  cudaError_t err;
-  if (K > 0) {
-    unsigned long long* status = device_status_words();
-    if (status == nullptr) return MXFP4EL_ERR_CUDA;
-    const bool gemm = choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
-    // Small batches on the GEMV: each GEMV CTA routes for itself.
-    const bool self = !gemm && gemv_self_route(T, E, I, O, K);
-    const bool prep = !gemm && !self && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
-    const bool prep_in_route = prep && prep_fits_route(T, I);
-    TokenPrep tp = {prep_in_route ? x : nullptr, ws.x16, ws.sigma, I};
-    const UnitSplit split = gemm ? UnitSplit{0, 0, 0, 1000} : gemv_unit_split(T, E, I, O, K);
-    mark(MXFP4EL_STAGE_ROUTE, true, stream);
-    err = cudaSuccess;
-    if (!self)
-      err = launch_route(sel, index_dtype, T, K, E, ws.wc_global, ws.plan, tp, split, stream);
-    if (err == cudaSuccess && prep && !prep_in_route)
-      err = launch_prep_tokens(x, ws.x16, ws.sigma, T, I, stream);
-    mark(MXFP4EL_STAGE_ROUTE, false, stream);
-    if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
-    if (gemm) {
-      mark(MXFP4EL_STAGE_GATHER, true, stream);
-      err = launch_gather_tokens(x, ws.plan, ws.grouped, T, I, K, stream);
-      mark(MXFP4EL_STAGE_GATHER, false, stream);
-      if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
-    }
-    mark(MXFP4EL_STAGE_LINEAR, true, stream);
-    if (gemm)
-      err = launch_gemm_tc(x, packed, scales, ws.plan, ws.grouped, ws.part, status, T, E, I, O,
-                           K, stream);
-    else
-      err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, sel, index_dtype, packed, scales,
-                        ws.plan, ws.part, status, T, E, I, O, K, stream);
-    mark(MXFP4EL_STAGE_LINEAR, false, stream);
-    if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
-  }
+  if (K > 0 && run_linear(x, packed, scales, sel, T, E, I, O, K, token_dtype, index_dtype, ws,
+                          stream) != cudaSuccess)
+    return MXFP4EL_ERR_CUDA;
   mark(MXFP4EL_STAGE_COMBINE, true, stream);
   // With K > 0 and E > 0 a linear kernel of the library ran just before
   // (the launchers skip only an empty grid, E == 0).
-  err = launch_combine(ys, sel, index_dtype, p, ws.part,
-                       linear_partial_columns(T, E, I, O, K, token_dtype), out, token_dtype, T,
-                       E, O, K, K > 0 && E > 0, stream);
+  const cudaError_t err =
+      launch_combine(ys, sel, index_dtype, p, ws.part,
+                     linear_partial_columns(T, E, I, O, K, token_dtype), out, token_dtype, T, E,
+                     O, K, K > 0 && E > 0, stream);
+  mark(MXFP4EL_STAGE_COMBINE, false, stream);
+  return err == cudaSuccess ? MXFP4EL_OK : MXFP4EL_ERR_CUDA;
+}
+
+// The SwiGLU expert: gate/up projection (2F stacked rows) -> SwiGLU -> down
+// projection with every pair as its own token -> combine.
+int validate_swiglu(const void* x, const uint8_t* gu_packed, const uint8_t* gu_scales,
+                    const uint8_t* dn_packed, const uint8_t* dn_scales, const void* sel,
+                    const float* p, const void* ys, void* out, int64_t T, int64_t E,
+                    int64_t I, int64_t F, int64_t O, int64_t K, int token_dtype,
+                    int index_dtype) {
+  if (token_dtype != MXFP4EL_DTYPE_F32 && token_dtype != MXFP4EL_DTYPE_BF16)
+    return MXFP4EL_ERR_UNSUPPORTED_DTYPE;
+  if (index_dtype != MXFP4EL_INDEX_I32 && index_dtype != MXFP4EL_INDEX_I64)
+    return MXFP4EL_ERR_UNSUPPORTED_DTYPE;
+  if (T < 0 || E < 0 || O < 0 || K < 0 || I <= 0 || I % 32 != 0 || F <= 0 || F % 32 != 0)
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (F > kMaxDim / 2 || !sizes_ok(T, E, I, 2 * F, K) || !sizes_ok(T * K, E, F, O, 1))
+    return MXFP4EL_ERR_TOO_LARGE;
+  if (T == 0 || O == 0) return MXFP4EL_OK;
+  if (ys == nullptr || out == nullptr) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (K > 0 && (x == nullptr || sel == nullptr || p == nullptr))
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (K > 0 && E > 0 &&
+      (gu_packed == nullptr || gu_scales == nullptr || dn_packed == nullptr ||
+       dn_scales == nullptr))
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(gu_packed) |
+       reinterpret_cast<uintptr_t>(dn_packed)) % 16)
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  const size_t tb = token_dtype == MXFP4EL_DTYPE_BF16 ? 2 : 4;
+  const size_t ib = index_dtype == MXFP4EL_INDEX_I64 ? 8 : 4;
+  const size_t Gi = (size_t)I / 32, Gf = (size_t)F / 32;
+  const size_t out_bytes = (size_t)T * O * tb;
+  const void* inputs[] = {x, gu_packed, gu_scales, dn_packed, dn_scales, sel, p, ys};
+  const size_t sizes[] = {(size_t)T * I * tb,        (size_t)E * 2 * F * Gi * 16,
+                          (size_t)E * 2 * F * Gi,    (size_t)E * O * Gf * 16,
+                          (size_t)E * O * Gf,        (size_t)T * K * ib,
+                          (size_t)T * K * 4,         (size_t)T * O * tb};
+  for (int i = 0; i < 8; ++i)
+    if (overlaps(out, out_bytes, inputs[i], sizes[i])) return MXFP4EL_ERR_ALIAS;
+  return MXFP4EL_OK;
+}
+
+struct SwigluWorkspace {
+  Workspace gate_up, down;   // the two projections' own workspaces
+  void* h = nullptr;         // (P, F) token dtype
+  int32_t* sel2 = nullptr;   // (P,) the down projection's expert per pair
+  size_t bytes = 0;
+};
+
+void carve_swiglu(void* base, int64_t T, int64_t E, int64_t I, int64_t F, int64_t O,
+                  int64_t K, int token_dtype, SwigluWorkspace* sw) {
+  const int64_t P = T * K;
+  const size_t tb = token_dtype == MXFP4EL_DTYPE_BF16 ? 2 : 4;
+  auto at = [&](size_t off) { return base ? static_cast<char*>(base) + off : nullptr; };
+  carve_workspace(base, T, E, I, 2 * F, K, token_dtype, &sw->gate_up);
+  size_t off = align_up(sw->gate_up.bytes);
+  carve_workspace(at(off), P, E, F, O, 1, token_dtype, &sw->down);
+  off = align_up(off + sw->down.bytes);
+  sw->h = at(off);
+  off = align_up(off + (size_t)P * F * tb);
+  sw->sel2 = reinterpret_cast<int32_t*>(at(off));
+  off = align_up(off + (size_t)P * sizeof(int32_t));
+  sw->bytes = off;
+}
+
+int run_swiglu(const void* x, const uint8_t* gu_packed, const uint8_t* gu_scales,
+               const uint8_t* dn_packed, const uint8_t* dn_scales, const void* sel,
+               const float* p, const void* ys, void* out, int64_t T, int64_t E, int64_t I,
+               int64_t F, int64_t O, int64_t K, int token_dtype, int index_dtype,
+               const SwigluWorkspace& sw, cudaStream_t stream) {
+  const int64_t P = T * K;
+  if (K > 0) {
+    // Invalid ids are counted here, once; the down projection sees expert 0
+    // with h = 0 in their place and the combine skips them.
+    if (run_linear(x, gu_packed, gu_scales, sel, T, E, I, 2 * F, K, token_dtype, index_dtype,
+                   sw.gate_up, stream) != cudaSuccess)
+      return MXFP4EL_ERR_CUDA;
+    if (E > 0) {
+      if (launch_swiglu(sw.gate_up.part,
+                        linear_partial_columns(T, E, I, 2 * F, K, token_dtype), sel,
+                        index_dtype, E, P, F, token_dtype, sw.h, sw.sel2,
+                        stream) != cudaSuccess)
+        return MXFP4EL_ERR_CUDA;
+      if (run_linear(sw.h, dn_packed, dn_scales, sw.sel2, P, E, F, O, 1, token_dtype,
+                     MXFP4EL_INDEX_I32, sw.down, stream) != cudaSuccess)
+        return MXFP4EL_ERR_CUDA;
+    }
+  }
+  mark(MXFP4EL_STAGE_COMBINE, true, stream);
+  const cudaError_t err =
+      launch_combine(ys, sel, index_dtype, p, sw.down.part,
+                     linear_partial_columns(P, E, F, O, 1, token_dtype), out, token_dtype, T, E,
+                     O, K, K > 0 && E > 0, stream);
   mark(MXFP4EL_STAGE_COMBINE, false, stream);
   return err == cudaSuccess ? MXFP4EL_OK : MXFP4EL_ERR_CUDA;
 }
@@ -164,6 +279,33 @@ std::mutex g_cache_mu;
 std::map<std::pair<int, cudaStream_t>, Cached>& cache() {
   static auto* m = new std::map<std::pair<int, cudaStream_t>, Cached>();
   return *m;
+}
+
+// The stream's cached workspace, grown (stream-ordered) to at least `bytes`.
+// Growing is refused while the stream is being captured.
+int cached_workspace(size_t bytes, cudaStream_t s, void** base) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MXFP4EL_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  Cached& c = cache()[{dev, s}];
+  if (c.bytes < bytes) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return MXFP4EL_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return MXFP4EL_ERR_WORKSPACE;
+    if (c.ptr) {
+      if (cudaFreeAsync(c.ptr, s) != cudaSuccess) return MXFP4EL_ERR_CUDA;
+      c.ptr = nullptr;
+      c.bytes = 0;
+    }
+    const size_t want = std::max(bytes, c.bytes + c.bytes / 4);
+    if (cudaMallocAsync(&c.ptr, want, s) != cudaSuccess) {
+      c.ptr = nullptr;
+      return MXFP4EL_ERR_CUDA;
+    }
+    c.bytes = want;
+  }
+  *base = c.ptr;
+  return MXFP4EL_OK;
 }
 
 }  // namespace
@@ -255,30 +397,9 @@ extern "C" int mxfp4_expert_linear(const void* latent_tokens,
   Workspace ws;
   carve_workspace(nullptr, T, E, I, O, K, token_dtype, &ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MXFP4EL_ERR_CUDA;
   void* base = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_cache_mu);
-    Cached& c = cache()[{dev, s}];
-    if (c.bytes < ws.bytes) {
-      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-      if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return MXFP4EL_ERR_CUDA;
-      if (cap != cudaStreamCaptureStatusNone) return MXFP4EL_ERR_WORKSPACE;
-      if (c.ptr) {
-        if (cudaFreeAsync(c.ptr, s) != cudaSuccess) return MXFP4EL_ERR_CUDA;
-        c.ptr = nullptr;
-        c.bytes = 0;
-      }
-      const size_t want = std::max(ws.bytes, c.bytes + c.bytes / 4);
-      if (cudaMallocAsync(&c.ptr, want, s) != cudaSuccess) {
-        c.ptr = nullptr;
-        return MXFP4EL_ERR_CUDA;
-      }
-      c.bytes = want;
-    }
-    base = c.ptr;
-  }
+  rc = cached_workspace(ws.bytes, s, &base);
+  if (rc != MXFP4EL_OK) return rc;
   carve_workspace(base, T, E, I, O, K, token_dtype, &ws);
   return run(latent_tokens, packed_weights, scale_bytes, selected_experts,
              mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
@@ -332,6 +453,64 @@ extern "C" int mxfp4_expert_linear_routed(const void* latent_tokens,
   return mxfp4_expert_linear(latent_tokens, packed_weights, scale_bytes, selected_experts,
                              mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
                              MXFP4EL_INDEX_I32, stream);
+}
+
+extern "C" size_t mxfp4_swiglu_expert_workspace_size(int64_t T, int64_t E, int64_t I,
+                                                     int64_t F, int64_t O, int64_t K,
+                                                     int token_dtype) {
+  if (token_dtype != MXFP4EL_DTYPE_F32 && token_dtype != MXFP4EL_DTYPE_BF16) return (size_t)-1;
+  if (T < 0 || E < 0 || O < 0 || K < 0 || I <= 0 || I % 32 != 0 || F <= 0 || F % 32 != 0)
+    return (size_t)-1;
+  if (F > kMaxDim / 2 || !sizes_ok(T, E, I, 2 * F, K) || !sizes_ok(T * K, E, F, O, 1))
+    return (size_t)-1;
+  if (T == 0 || O == 0) return 0;
+  SwigluWorkspace sw;
+  carve_swiglu(nullptr, T, E, I, F, O, K, token_dtype, &sw);
+  return sw.bytes;
+}
+
+extern "C" int mxfp4_swiglu_expert_with_workspace(
+    const void* latent_tokens, const uint8_t* gate_up_packed, const uint8_t* gate_up_scales,
+    const uint8_t* down_packed, const uint8_t* down_scales, const void* selected_experts,
+    const float* mixture_weights, const void* shared_output, void* out, int64_t T, int64_t E,
+    int64_t I, int64_t F, int64_t O, int64_t K, int token_dtype, int index_dtype,
+    void* workspace, size_t workspace_bytes, void* stream) {
+  const int rc = validate_swiglu(latent_tokens, gate_up_packed, gate_up_scales, down_packed,
+                                 down_scales, selected_experts, mixture_weights, shared_output,
+                                 out, T, E, I, F, O, K, token_dtype, index_dtype);
+  if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
+  SwigluWorkspace sw;
+  carve_swiglu(nullptr, T, E, I, F, O, K, token_dtype, &sw);
+  if (workspace == nullptr || workspace_bytes < sw.bytes ||
+      reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return MXFP4EL_ERR_WORKSPACE;
+  carve_swiglu(workspace, T, E, I, F, O, K, token_dtype, &sw);
+  return run_swiglu(latent_tokens, gate_up_packed, gate_up_scales, down_packed, down_scales,
+                    selected_experts, mixture_weights, shared_output, out, T, E, I, F, O, K,
+                    token_dtype, index_dtype, sw, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mxfp4_swiglu_expert(const void* latent_tokens, const uint8_t* gate_up_packed,
+                                   const uint8_t* gate_up_scales, const uint8_t* down_packed,
+                                   const uint8_t* down_scales, const void* selected_experts,
+                                   const float* mixture_weights, const void* shared_output,
+                                   void* out, int64_t T, int64_t E, int64_t I, int64_t F,
+                                   int64_t O, int64_t K, int token_dtype, int index_dtype,
+                                   void* stream) {
+  int rc = validate_swiglu(latent_tokens, gate_up_packed, gate_up_scales, down_packed,
+                           down_scales, selected_experts, mixture_weights, shared_output, out,
+                           T, E, I, F, O, K, token_dtype, index_dtype);
+  if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
+  SwigluWorkspace sw;
+  carve_swiglu(nullptr, T, E, I, F, O, K, token_dtype, &sw);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* base = nullptr;
+  rc = cached_workspace(sw.bytes, s, &base);
+  if (rc != MXFP4EL_OK) return rc;
+  carve_swiglu(base, T, E, I, F, O, K, token_dtype, &sw);
+  return run_swiglu(latent_tokens, gate_up_packed, gate_up_scales, down_packed, down_scales,
+                    selected_experts, mixture_weights, shared_output, out, T, E, I, F, O, K,
+                    token_dtype, index_dtype, sw, s);
 }
 
 extern "C" int mxfp4el_device_errors(void* stream, int64_t* bad_pairs) {

@@ -162,6 +162,15 @@ cudaError_t launch_router(const float* logits, const float* bias, int64_t T, int
                           int64_t K, float scaling, int32_t* sel, float* p,
                           cudaStream_t stream);
 
+// SwiGLU between the two projections of the SwiGLU expert (swiglu.cu): from
+// the gate/up projection's partial results `part` (P pairs x ncol columns x
+// 2F rows, gate rows first) h[pair, f] = silu(gate) * up in float32, rounded
+// to the token dtype, and sel2[pair] = the pair's expert, or 0 (with h = 0)
+// for an id outside [0, E).
+cudaError_t launch_swiglu(const float* part, int ncol, const void* sel, int index_dtype,
+                          int64_t E, int64_t P, int64_t F, int token_dtype, void* h,
+                          int32_t* sel2, cudaStream_t stream);
+
 // Device address of the status words on the current device.
 unsigned long long* device_status_words();
 

@@ -357,7 +357,7 @@ route_scatter_kernel(const Idx* __restrict__ sel, int64_t P, int E,
 }
 
 int multi_ctas(int64_t P, int64_t E, bool prep) {
-  if (prep || P < kMultiMinPairs || E > kMultiMaxExperts) return 0;
+  if (prep || P < kMultiMinPairs || E == 0 || E > kMultiMaxExperts) return 0;
   const int64_t n = (P + kMultiChunk - 1) / kMultiChunk;
   return n <= 0x7fffffff ? (int)n : 0;
 }

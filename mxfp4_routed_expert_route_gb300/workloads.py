@@ -150,3 +150,85 @@ def experts_touched(sel: torch.Tensor, E: int) -> int:
     s = sel.reshape(-1).to(torch.int64)
     s = s[(s >= 0) & (s < E)]
     return int(torch.unique(s).numel())
+
+
+# ------------------------------------------------------- the SwiGLU expert --
+@dataclass
+class SwigluWorkload:
+    """Inputs of the routed SwiGLU expert: the gate and up matrices stacked
+    along their rows (gate rows first), the down matrix, routing and the
+    shared output."""
+    name: str
+    T: int
+    E: int
+    K: int
+    I: int
+    F: int
+    O: int
+    dtype: torch.dtype
+    x: torch.Tensor               # (T, I)
+    gate_up_packed: torch.Tensor  # (E, 2F, I/32, 16) uint8
+    gate_up_scales: torch.Tensor  # (E, 2F, I/32) uint8
+    down_packed: torch.Tensor     # (E, O, F/32, 16) uint8
+    down_scales: torch.Tensor     # (E, O, F/32) uint8
+    sel: torch.Tensor             # (T, K) int32
+    p: torch.Tensor               # (T, K) float32
+    y_shared: torch.Tensor        # (T, O)
+    meta: dict = field(default_factory=dict)
+
+    ARGS = ("x", "gate_up_packed", "gate_up_scales", "down_packed", "down_scales", "sel",
+            "p", "y_shared")
+
+    def device_tensors(self, device) -> dict:
+        return {k: getattr(self, k).to(device) for k in self.ARGS}
+
+    def args(self) -> list:
+        return [getattr(self, k) for k in self.ARGS]
+
+
+# The SwiGLU expert at the layer shape of the named linear workloads: hidden
+# width I = 2880 and intermediate width F = 2880, so the stacked gate/up
+# matrix has the linear workloads' 5760 rows and the down matrix maps 2880
+# back to 2880.
+SWIGLU_CONFIGS = {
+    "swiglu_tiny_fp32": dict(T=4, E=4, K=2, I=64, F=64, O=32, dtype=torch.float32, seed=10),
+    "swiglu_decode": dict(T=8, E=128, K=4, I=2880, F=2880, O=2880, dtype=torch.bfloat16,
+                          seed=11),
+    "swiglu_prefill": dict(T=4096, E=128, K=4, I=2880, F=2880, O=2880,
+                           dtype=torch.bfloat16, seed=12),
+}
+
+
+def make_swiglu(T: int, E: int, K: int, I: int, F: int, O: int, dtype=torch.bfloat16,
+                scale_lo: int = 118, scale_hi: int = 124, picks: str = "uniform",
+                seed: int = 0, zipf_s: float = 1.2, name: str = "custom") -> SwigluWorkload:
+    """Draw one SwiGLU workload with the recipe of :func:`make` (uniform
+    bytes, uniform scale bytes in [scale_lo, scale_hi] for both matrices,
+    N(0, 1) tokens and shared output, softmax weights)."""
+    if I % 32 or F % 32:
+        raise ValueError("I and F must be multiples of 32")
+    rng = np.random.default_rng(seed)
+    gu = random_bytes(rng, E * 2 * F * (I // 32) * 16).reshape(E, 2 * F, I // 32, 16)
+    gus = rng.integers(scale_lo, scale_hi + 1, size=(E, 2 * F, I // 32)).astype(np.uint8)
+    dn = random_bytes(rng, E * O * (F // 32) * 16).reshape(E, O, F // 32, 16)
+    dns = rng.integers(scale_lo, scale_hi + 1, size=(E, O, F // 32)).astype(np.uint8)
+    x = _normal(rng, (T, I), dtype)
+    y_shared = _normal(rng, (T, O), dtype)
+    if picks == "uniform":
+        sel = uniform_picks(rng, T, E, K)
+    elif picks == "zipf":
+        sel = zipf_picks(rng, T, E, K, zipf_s)
+    else:
+        raise ValueError(picks)
+    p = softmax_weights(rng, T, K)
+    return SwigluWorkload(name=name, T=T, E=E, K=K, I=I, F=F, O=O, dtype=dtype, x=x,
+                          gate_up_packed=torch.from_numpy(gu),
+                          gate_up_scales=torch.from_numpy(gus),
+                          down_packed=torch.from_numpy(dn), down_scales=torch.from_numpy(dns),
+                          sel=torch.from_numpy(np.ascontiguousarray(sel, dtype=np.int32)),
+                          p=torch.from_numpy(p), y_shared=y_shared,
+                          meta=dict(seed=seed, picks=picks, scale_range=(scale_lo, scale_hi)))
+
+
+def named_swiglu(name: str) -> SwigluWorkload:
+    return make_swiglu(name=name, **SWIGLU_CONFIGS[name])

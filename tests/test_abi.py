@@ -130,6 +130,7 @@ def test_linear_path_choice(lib):
     assert path(4096, 128, 2848, 5760, 4, n.DTYPE_BF16) == n.PATH_GEMV     # G odd
     assert path(640, 512, 64, 48, 16, n.DTYPE_BF16) == n.PATH_GEMM
     assert path(640, 600, 64, 48, 16, n.DTYPE_BF16) == n.PATH_GEMV         # > 512 experts
+    assert path(640, 0, 64, 48, 16, n.DTYPE_BF16) == n.PATH_GEMV           # no experts
 
 
 def test_router_argument_checks(lib):
@@ -148,3 +149,39 @@ def test_router_argument_checks(lib):
     # nothing to do
     assert lib.mxfp4_router_topk(None, None, 0, 8, 2, f, None, None, None) == 0
     assert lib.mxfp4_router_topk(None, None, 5, 8, 0, f, None, None, None) == 0
+
+
+def test_swiglu_argument_checks(lib):
+    # Checked before anything is enqueued: no GPU needed.
+    from mxfp4_routed_expert_route_gb300 import _native as n
+    f = lib.mxfp4_swiglu_expert
+    P = ctypes.c_void_p
+    x, gu, gs, dn, ds = P(1 << 24), P(1 << 28), P(1 << 29), P(1 << 30), P(1 << 31)
+    sel, p, ys, out = P(1 << 32), P(1 << 33), P(1 << 34), P(1 << 35)
+    ok = [x, gu, gs, dn, ds, sel, p, ys, out]
+    assert f(*ok, 4, 4, 64, 48, 8, 2, 0, 0, None) == n.ERR_INVALID_ARGUMENT   # F % 32
+    assert f(*ok, 4, 4, 60, 64, 8, 2, 0, 0, None) == n.ERR_INVALID_ARGUMENT   # I % 32
+    assert f(*ok, 4, 4, 64, 0, 8, 2, 0, 0, None) == n.ERR_INVALID_ARGUMENT    # F == 0
+    assert f(*ok, 4, 4, 64, 64, 8, 2, 3, 0, None) == n.ERR_UNSUPPORTED_DTYPE
+    assert f(*ok, 4, 4, 64, 64, 8, 2, 0, 2, None) == n.ERR_UNSUPPORTED_DTYPE
+    assert f(*ok, 0, 4, 64, 64, 8, 2, 0, 0, None) == n.OK                    # T == 0
+    assert f(*ok, 4, 4, 64, 64, 0, 2, 0, 0, None) == n.OK                    # O == 0
+    assert f(*ok, 1 << 40, 4, 64, 64, 8, 2, 0, 0, None) == n.ERR_TOO_LARGE
+    # a missing down matrix
+    assert f(x, gu, gs, None, ds, sel, p, ys, out, 4, 4, 64, 64, 8, 2, 0, 0,
+             None) == n.ERR_INVALID_ARGUMENT
+    # misaligned down matrix
+    assert f(x, gu, gs, P((1 << 30) + 8), ds, sel, p, ys, out, 4, 4, 64, 64, 8, 2, 0, 0,
+             None) == n.ERR_INVALID_ARGUMENT
+    # out overlapping the down scales
+    assert f(x, gu, gs, dn, ds, sel, p, ys, P((1 << 31) + 4), 4, 4, 64, 64, 8, 2, 0, 0,
+             None) == n.ERR_ALIAS
+    ws = lib.mxfp4_swiglu_expert_workspace_size
+    bad = ctypes.c_size_t(-1).value
+    assert ws(4, 4, 64, 48, 8, 2, 0) == bad
+    assert ws(0, 4, 64, 64, 8, 2, 0) == 0
+    # gate/up scratch (T K pairs x 2F) + down scratch (T K pairs x O) + h
+    n1 = ws(8, 128, 2880, 2880, 2880, 4, 1)
+    assert n1 >= 32 * 5760 * 4 + 32 * 2880 * 4 + 32 * 2880 * 2 and n1 % 256 == 0
+    g = lib.mxfp4_swiglu_expert_with_workspace
+    assert g(*ok, 4, 4, 64, 64, 8, 2, 0, 0, None, 0, None) == n.ERR_WORKSPACE

@@ -128,6 +128,21 @@ def test_no_experts_at_all():
     assert torch.equal(out.cpu(), wl.y_shared)
 
 
+@pytest.mark.parametrize("T,K,dtype", [(64, 2, torch.bfloat16), (4200, 2, torch.bfloat16),
+                                       (5, 3, torch.float32)])
+def test_zero_experts_counts_every_id(T, K, dtype):
+    # E == 0: every id is out of range; the call returns the shared output
+    # and counts every pair, on every path the sizes would otherwise pick.
+    wl = workloads.make(T, 1, K, 64, 24, dtype=dtype, seed=13)
+    d = wl.device_tensors("cuda")
+    device_errors()
+    sel = torch.randint(-3, 5, (T, K), dtype=torch.int64, device="cuda")
+    out = mxfp4_expert_linear(d["x"], d["packed"][:0], d["scales"][:0], sel, d["p"],
+                              d["y_shared"])
+    assert torch.equal(out.cpu(), wl.y_shared)
+    assert device_errors() == T * K
+
+
 def test_int64_ids_match_int32():
     wl = workloads.make(11, 7, 3, 96, 30, dtype=torch.bfloat16, seed=12)
     a = run_gpu(wl)
