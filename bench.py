@@ -42,6 +42,10 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the router and SwiGLU-expert fields (clean launch lists)")
+    ap.add_argument("--swiglu-only", action="store_true",
+                    help="time only the SwiGLU expert at the workload's layer shape")
     return ap.parse_args()
 
 
@@ -487,9 +491,10 @@ def run_ours(args, rank, world):
     d2h = out_h.numel() * out_h.element_size()
 
     peaks, peaks_src = load_peaks()
-    router = measure_router(wl, d, dev, stream, flush, W, min(K, 200), peaks)
+    router = None if args.no_extras else measure_router(wl, d, dev, stream, flush, W,
+                                                          min(K, 200), peaks)
     swiglu = (measure_swiglu(SWIGLU_FOR[wl.name], dev, stream, flush, W, min(K, 100), peaks)
-              if wl.name in SWIGLU_FOR else None)
+              if wl.name in SWIGLU_FOR and not args.no_extras else None)
     if rank != 0:
         return
     gemm = lib.mxfp4el_linear_path(wl.T, wl.E, wl.I, wl.O, wl.K,
@@ -560,6 +565,24 @@ def run_ours(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_swiglu_only(args, rank):
+    """The SwiGLU expert alone at the workload's layer shape (for profiling)."""
+    import torch
+    from mxfp4_routed_expert_route_gb300 import build
+    if args.workload not in SWIGLU_FOR:
+        raise SystemExit(f"no SwiGLU shape for workload {args.workload}")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peaks, _ = load_peaks()
+    r = measure_swiglu(SWIGLU_FOR[args.workload], dev, torch.cuda.current_stream(dev), flush,
+                       args.warmup, args.steps, peaks)
+    if rank == 0:
+        print(json.dumps(r), flush=True)
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -573,7 +596,10 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
     try:
-        run_ours(args, rank, world)
+        if args.swiglu_only:
+            run_swiglu_only(args, rank)
+        else:
+            run_ours(args, rank, world)
     finally:
         if world > 1:
             import torch.distributed as dist

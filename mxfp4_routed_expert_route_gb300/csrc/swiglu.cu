@@ -15,48 +15,71 @@
 // selection is a copy of the ids in which an out-of-range id becomes expert
 // 0 with h = 0 (the combine, which reads the original ids, skips that pair),
 // so an invalid id is counted once per call.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace mxfp4el {
 namespace {
 
+__device__ __forceinline__ float silu_times(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// Four consecutive h values of one pair, stored in the token dtype.
+__device__ __forceinline__ void store4(float* h, float4 v) { *reinterpret_cast<float4*>(h) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* h, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&a);
+  w.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(h) = w;
+}
+
 template <typename Tok, typename Idx>
 __global__ void __launch_bounds__(256)
 swiglu_kernel(const float* __restrict__ part, int ncol, const Idx* __restrict__ sel, int64_t E,
-              int64_t P, int64_t F, Tok* __restrict__ h, int32_t* __restrict__ sel2) {
+              int64_t P, int F, Tok* __restrict__ h, int32_t* __restrict__ sel2) {
   pdl_wait();                  // the gate/up projection's partial results are complete
   pdl_launch_dependents();
-  const int64_t n = P * F;
-  const int64_t row = (int64_t)ncol * 2 * F;       // floats per pair
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t pair = idx / F, f = idx - pair * F;
+  // x: four consecutive intermediate indices f per thread (F is a multiple
+  // of 32, so a pair's rows and columns start on 16-byte boundaries); y:
+  // pairs, in steps of the grid's height.
+  const int f = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  const int64_t col = 2 * (int64_t)F;              // floats per group column of a pair
+  for (int64_t pair = blockIdx.y; pair < P; pair += gridDim.y) {
     const long long e = (long long)sel[pair];
     const bool valid = e >= 0 && e < E;
-    float v = 0.f;
-    if (valid) {
-      const float* pp = part + pair * row + f;
-      float g = pp[0], u = pp[F];
-      for (int c = 1; c < ncol; ++c) {
-        g += pp[(int64_t)c * 2 * F];
-        u += pp[(int64_t)c * 2 * F + F];
+    if (f < F) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (valid) {
+        const float* pp = part + pair * ncol * col + f;
+        float4 g = __ldg(reinterpret_cast<const float4*>(pp));
+        float4 u = __ldg(reinterpret_cast<const float4*>(pp + F));
+        for (int c = 1; c < ncol; ++c) {         // group columns in order
+          const float4 gc = __ldg(reinterpret_cast<const float4*>(pp + c * col));
+          const float4 uc = __ldg(reinterpret_cast<const float4*>(pp + c * col + F));
+          g.x += gc.x; g.y += gc.y; g.z += gc.z; g.w += gc.w;
+          u.x += uc.x; u.y += uc.y; u.z += uc.z; u.w += uc.w;
+        }
+        v = make_float4(silu_times(g.x, u.x), silu_times(g.y, u.y), silu_times(g.z, u.z),
+                        silu_times(g.w, u.w));
       }
-      v = g / (1.f + expf(-g)) * u;
+      store4(h + pair * F + f, v);
     }
-    h[idx] = TokenIO<Tok>::from_f32(v);
-    if (f == 0) sel2[pair] = valid ? (int32_t)e : 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) sel2[pair] = valid ? (int32_t)e : 0;
   }
 }
 
 template <typename Tok, typename Idx>
 cudaError_t launch_typed(const float* part, int ncol, const Idx* sel, int64_t E, int64_t P,
                          int64_t F, Tok* h, int32_t* sel2, cudaStream_t stream) {
-  const int64_t n = P * F;
-  if (n == 0) return cudaSuccess;
-  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 16);
-  return launch_after_previous(swiglu_kernel<Tok, Idx>, dim3((unsigned)blocks), dim3(256), 0,
-                               stream, part, ncol, sel, E, P, F, h, sel2);
+  if (P == 0 || F == 0) return cudaSuccess;
+  const int64_t bx = (F / 4 + 255) / 256;
+  // About 16 blocks per SM in all; each block row loops over its pairs.
+  const int64_t by = std::max<int64_t>(1, std::min<int64_t>({P, 65535, (152 * 16 + bx - 1) / bx}));
+  return launch_after_previous(swiglu_kernel<Tok, Idx>, dim3((unsigned)bx, (unsigned)by),
+                               dim3(256), 0, stream, part, ncol, sel, E, P, (int)F, h, sel2);
 }
 
 }  // namespace
