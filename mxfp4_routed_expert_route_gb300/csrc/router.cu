@@ -9,25 +9,17 @@
 // in float32, each divided by that sum plus 1e-20 and multiplied by the
 // scaling factor.
 //
-// One warp per token: the raw and choice scores go to shared memory, then K
-// rounds of a warp-wide argmax (greater score, or equal score and lower
-// index) each take one expert and mark it taken, in shared memory only. An expert whose choice is NaN is
-// never taken; slots left without an expert get id -1 and weight 0 (the
-// linear skips such pairs).
+// One warp per token (router_token_warp in router.cuh): an expert whose
+// choice is NaN is never taken; slots left without an expert get id -1 and
+// weight 0 (the linear skips such pairs).
 #include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
+#include "router.cuh"
 
 namespace mxfp4el {
 namespace {
-
-__device__ __forceinline__ float sigmoid_f32(float x) { return 1.f / (1.f + expf(-x)); }
-
-// (c, e) beats (bc, be): greater choice, or equal choice and lower index.
-__device__ __forceinline__ bool better(float c, int e, float bc, int be) {
-  return c > bc || (c == bc && e < be);
-}
 
 __global__ void __launch_bounds__(kRouterThreads)
 router_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int64_t T,
@@ -35,52 +27,10 @@ router_topk_kernel(const float* __restrict__ logits, const float* __restrict__ b
                    float* __restrict__ p) {
   extern __shared__ float router_smem[];   // per warp: E raw, E choice, K chosen scores
   pdl_launch_dependents();
-  const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* raw = router_smem + (size_t)warp * (2 * E + K);
-  float* choice = raw + E;
-  float* chosen = choice + E;
-  for (int64_t t = (int64_t)blockIdx.x * warps + warp; t < T; t += (int64_t)gridDim.x * warps) {
-    const float* row = logits + t * E;
-    for (int e = lane; e < E; e += 32) {
-      const float r = sigmoid_f32(row[e]);
-      raw[e] = r;
-      choice[e] = r + (bias != nullptr ? bias[e] : 0.f);
-    }
-    __syncwarp();
-    for (int k = 0; k < K; ++k) {
-      float bc = -INFINITY;
-      int be = 0x7fffffff;
-      for (int e = lane; e < E; e += 32) {
-        const float c = choice[e];
-        if (c == c && better(c, e, bc, be)) {   // c == c: not NaN (taken or invalid)
-          bc = c;
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float oc = __shfl_xor_sync(kFullMask, bc, o);
-        const int oe = __shfl_xor_sync(kFullMask, be, o);
-        if (better(oc, oe, bc, be)) {
-          bc = oc;
-          be = oe;
-        }
-      }
-      if (lane == 0) {
-        const bool found = be != 0x7fffffff;
-        sel[t * K + k] = found ? be : -1;
-        chosen[k] = found ? raw[be] : 0.f;
-        if (found) choice[be] = __int_as_float(0x7fffffff);   // NaN: taken
-      }
-      __syncwarp();
-    }
-    if (lane == 0) {
-      float total = 0.f;
-      for (int k = 0; k < K; ++k) total += chosen[k];        // left to right
-      for (int k = 0; k < K; ++k) p[t * K + k] = chosen[k] / (total + 1e-20f) * scaling;
-    }
-    __syncwarp();
-  }
+  const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5;
+  float* scratch = router_smem + (size_t)warp * router_scratch_floats(E, K);
+  for (int64_t t = (int64_t)blockIdx.x * warps + warp; t < T; t += (int64_t)gridDim.x * warps)
+    router_token_warp(logits + t * E, bias, E, K, scaling, scratch, sel + t * K, p + t * K);
 }
 
 }  // namespace

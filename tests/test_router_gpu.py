@@ -13,8 +13,9 @@ import pytest
 import torch
 
 from oracle import router as R
-from mxfp4_routed_expert_route_gb300 import (mxfp4_expert_linear, mxfp4_expert_linear_routed,
-                                             router_topk, wait_timeouts, workloads)
+from mxfp4_routed_expert_route_gb300 import (device_errors, mxfp4_expert_linear,
+                                             mxfp4_expert_linear_routed, router_topk,
+                                             wait_timeouts, workloads)
 from gpu_util import TOL, assert_parity
 import oracle
 
@@ -105,3 +106,43 @@ def test_routed_linear(name):
     want, absm, _ = oracle.expert_linear(wl.x, wl.packed, wl.scales, sel.cpu().long(),
                                          p.cpu(), wl.y_shared, rows=rows)
     assert_parity(out[torch.from_numpy(rows).cuda()], want, absm, wl.dtype, f"routed {name}")
+
+
+@pytest.mark.parametrize("T,E,K,dtype", [(8, 128, 4, torch.bfloat16), (16, 384, 8, torch.bfloat16),
+                                         (3, 40, 3, torch.float32), (1, 8, 8, torch.bfloat16),
+                                         (200, 64, 5, torch.bfloat16)])
+def test_routed_call_matches_router_then_linear(T, E, K, dtype):
+    # Ties within a token and a scaling factor: the routed call gives the
+    # same bits as the router, then the linear on its output.
+    wl = workloads.make(T, E, K, 320, 96, dtype=dtype, seed=T + E)
+    rng = np.random.default_rng(T * E)
+    logits = _logits(rng, T, E)
+    logits[0, :4] = logits[0, 4]
+    bias = rng.normal(0, 0.1, E).astype(np.float32)
+    d = wl.device_tensors("cuda")
+    lg, b = torch.from_numpy(logits).cuda(), torch.from_numpy(bias).cuda()
+    out, sel, p = mxfp4_expert_linear_routed(d["x"], d["packed"], d["scales"], lg, b, K,
+                                             d["y_shared"], scaling=2.5)
+    sel2, p2 = router_topk(lg, b, K, 2.5)
+    out2 = mxfp4_expert_linear(d["x"], d["packed"], d["scales"], sel2, p2, d["y_shared"])
+    torch.cuda.synchronize()
+    assert wait_timeouts() == 0
+    assert torch.equal(sel, sel2) and torch.equal(p, p2) and torch.equal(out, out2)
+    check_router(logits, bias, K, 2.5, sel, p)
+
+
+def test_routed_call_with_nan_logits():
+    # A token whose logits are all NaN gets no expert: ids -1, weights 0,
+    # counted as invalid pairs, and its output is the shared output.
+    wl = workloads.make(4, 16, 2, 64, 40, dtype=torch.float32, seed=5)
+    logits = np.random.default_rng(3).standard_normal((4, 16)).astype(np.float32)
+    logits[2, :] = np.nan
+    d = wl.device_tensors("cuda")
+    device_errors()
+    out, sel, p = mxfp4_expert_linear_routed(d["x"], d["packed"], d["scales"],
+                                             torch.from_numpy(logits).cuda(), None, 2,
+                                             d["y_shared"])
+    torch.cuda.synchronize()
+    assert sel[2].tolist() == [-1, -1] and p[2].tolist() == [0.0, 0.0]
+    assert device_errors() == 2
+    assert torch.equal(out[2].cpu(), wl.y_shared[2])
