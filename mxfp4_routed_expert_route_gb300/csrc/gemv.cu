@@ -538,24 +538,27 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
   }
 }
 
-// Both scale sources for one pass (the choice is uniform per tile).
+// Both scale sources for one pass (the choice is uniform per tile); the
+// global address of the lane's scale bytes is formed only when the tile's
+// scales were not staged (expert e, group gc).
 template <typename Elem, int RWS, int NTA>
 __device__ __forceinline__ void stream_pass_any(const StreamArgs& a,
                                                 const GroupToken<Elem> (&xt)[NTA],
                                                 const int (&pair)[NTA],
                                                 const int (&soff)[NTA], uint32_t sp_lane,
-                                                uint32_t ss_lane, const uint8_t* gs_lane,
-                                                bool staged, int o0, int rows, int rbase, int c,
-                                                int lane) {
-  if (staged && rbase + RWS <= rows)
-    stream_pass<Elem, RWS, NTA, true, true>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane, o0,
+                                                uint32_t ss_lane, int e, int gc, bool staged,
+                                                int o0, int rows, int rbase, int c, int lane) {
+  if (staged && rbase + RWS <= rows) {
+    stream_pass<Elem, RWS, NTA, true, true>(a, xt, pair, soff, sp_lane, ss_lane, nullptr, o0,
                                             rows, rbase, c, lane);
-  else if (staged)
-    stream_pass<Elem, RWS, NTA, true, false>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane, o0,
+  } else if (staged) {
+    stream_pass<Elem, RWS, NTA, true, false>(a, xt, pair, soff, sp_lane, ss_lane, nullptr, o0,
                                              rows, rbase, c, lane);
-  else
+  } else {
+    const uint8_t* gs_lane = a.scales + ((size_t)e * a.O + o0 + rbase) * a.G + gc;
     stream_pass<Elem, RWS, NTA, false, false>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane,
                                               o0, rows, rbase, c, lane);
+  }
 }
 
 // Token operands (this lane's group) and pair ids of the pass starting at
@@ -765,10 +768,11 @@ gemv_stream_kernel(const StreamArgs a) {
       return;
     }
     const unsigned char* hp = stage_base + (size_t)st * a.stage_bytes;
-    const StageHeader* h = reinterpret_cast<const StageHeader*>(hp);
-    const int e = h->e;
+    // The header in one 16-byte load: expert, first row, rows, scale offset.
+    const int4 hv = *reinterpret_cast<const int4*>(hp);
+    const int e = hv.x;
     if (e < 0) break;
-    const int o0 = h->o0, rows = h->rows, scale_off = h->scale_off;
+    const int o0 = hv.y, rows = hv.z, scale_off = hv.w;
     const unsigned char* sp = hp + sizeof(StageHeader);
 
     if (working && rbase < rows) {
@@ -784,18 +788,16 @@ gemv_stream_kernel(const StreamArgs a) {
       const uint32_t ss_lane =
           smem_addr(sp) + a.packed_stage_bytes + (uint32_t)(scale_off + rbase * G + gc);
       const bool staged = scale_off >= 0;
-      const uint8_t* gs_lane =
-          staged ? nullptr : a.scales + ((size_t)e * O + o0 + rbase) * G + gc;
       for (int base = seg_beg;;) {
         if (seg_end - base >= NT) {
-          stream_pass_any<Elem, RWS, NT>(a, x0, pair0, soff0, sp_lane, ss_lane, gs_lane,
-                                         staged, o0, rows, rbase, c, lane);
+          stream_pass_any<Elem, RWS, NT>(a, x0, pair0, soff0, sp_lane, ss_lane, e, gc, staged,
+                                         o0, rows, rbase, c, lane);
         } else {                              // one token left (NT == 2)
           stream_pass_any<Elem, RWS, 1>(
               a, reinterpret_cast<const GroupToken<Elem>(&)[1]>(x0[0]),
               reinterpret_cast<const int(&)[1]>(pair0[0]),
-              reinterpret_cast<const int(&)[1]>(soff0[0]), sp_lane, ss_lane, gs_lane,
-              staged, o0, rows, rbase, c, lane);
+              reinterpret_cast<const int(&)[1]>(soff0[0]), sp_lane, ss_lane, e, gc, staged,
+              o0, rows, rbase, c, lane);
         }
         base += NT;
         if (base >= seg_end) break;
