@@ -113,7 +113,7 @@ namespace {
 cudaError_t run_linear(const void* x, const uint8_t* packed, const uint8_t* scales,
                        const void* sel, int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
                        int token_dtype, int index_dtype, const Workspace& ws,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const SwigluTiles& swiglu = SwigluTiles{}) {
   unsigned long long* status = device_status_words();
   if (status == nullptr) return cudaErrorUnknown;
   if (E == 0) {
@@ -142,14 +142,14 @@ cudaError_t run_linear(const void* x, const uint8_t* packed, const uint8_t* scal
   if (err != cudaSuccess) return err;
   if (gemm) {
     mark(MXFP4EL_STAGE_GATHER, true, stream);
-    err = launch_gather_tokens(x, ws.plan, ws.grouped, T, I, K, stream);
+    err = launch_gather_tokens(x, ws.plan, ws.grouped, T, I, K, swiglu.sel2, stream);
     mark(MXFP4EL_STAGE_GATHER, false, stream);
     if (err != cudaSuccess) return err;
   }
   mark(MXFP4EL_STAGE_LINEAR, true, stream);
   if (gemm)
     err = launch_gemm_tc(x, packed, scales, ws.plan, ws.grouped, ws.part, status, T, E, I, O, K,
-                         stream);
+                         swiglu, stream);
   else
     err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, sel, index_dtype, packed, scales,
                       ws.plan, ws.part, status, T, E, I, O, K, stream);
@@ -215,6 +215,17 @@ int validate_swiglu(const void* x, const uint8_t* gu_packed, const uint8_t* gu_s
   return MXFP4EL_OK;
 }
 
+// Whether the gate/up projection of a SwiGLU call runs on the tensor cores
+// in gate/up tiles. Test knob: MXFP4EL_SWIGLU_TILES=0 keeps the separate
+// SwiGLU kernel.
+bool swiglu_tiles_used(int64_t T, int64_t E, int64_t I, int64_t F, int64_t K,
+                       int token_dtype) {
+  if (const char* env = std::getenv("MXFP4EL_SWIGLU_TILES"))
+    if (std::strcmp(env, "0") == 0) return false;
+  return choose_path(T, E, I, 2 * F, K, token_dtype) == LinearPath::kGemm &&
+         gemm_tc_swiglu_supported(E, I, F);
+}
+
 struct SwigluWorkspace {
   Workspace gate_up, down;   // the two projections' own workspaces
   void* h = nullptr;         // (P, F) token dtype
@@ -247,11 +258,21 @@ int run_swiglu(const void* x, const uint8_t* gu_packed, const uint8_t* gu_scales
   if (K > 0) {
     // Invalid ids are counted here, once; the down projection sees expert 0
     // with h = 0 in their place and the combine skips them.
+    // On the tensor cores the gate/up kernel forms h itself (tiles of gate
+    // rows and their up rows), so the partial results never leave it.
+    const bool tiles = E > 0 && swiglu_tiles_used(T, E, I, F, K, token_dtype);
+    SwigluTiles st;
+    if (tiles) {
+      st.F = F;
+      st.h = sw.h;
+      st.sel2 = sw.sel2;
+    }
     if (run_linear(x, gu_packed, gu_scales, sel, T, E, I, 2 * F, K, token_dtype, index_dtype,
-                   sw.gate_up, stream) != cudaSuccess)
+                   sw.gate_up, stream, st) != cudaSuccess)
       return MXFP4EL_ERR_CUDA;
     if (E > 0) {
-      if (launch_swiglu(sw.gate_up.part,
+      if (!tiles &&
+          launch_swiglu(sw.gate_up.part,
                         linear_partial_columns(T, E, I, 2 * F, K, token_dtype), sel,
                         index_dtype, E, P, F, token_dtype, sw.h, sw.sel2,
                         stream) != cudaSuccess)

@@ -89,11 +89,19 @@ struct TcArgs {
   int mtiles;                    // ceil(O / 128)
   int stages_a;
   uint32_t scale_cap;            // bytes per scale buffer
+  // Gate/up tiles of the SwiGLU expert (F > 0; the matrix has 2F rows, gate
+  // rows first): tile rows 0..63 are gate rows f0.., rows 64..127 the
+  // matching up rows F + f0..; the epilogue writes h = silu(gate) * up in
+  // bf16 and the pairs' expert ids instead of the partial results.
+  int F;
+  __nv_bfloat16* h;              // (P, F)
+  int32_t* sel2;                 // (P): expert of each pair (zeroed by the gather)
 };
 
 struct TcMaps {
   CUtensorMap a;                 // packed weights as uint8 [E*O, G*16], box {32, 128}
   CUtensorMap b[kNumLoads];      // grouped tokens bf16 [P, I], box {64, rows}, 128B swizzle
+  CUtensorMap a_half;            // packed weights, box {32, 64} (gate/up tiles)
 };
 
 struct __align__(16) TcShared {
@@ -117,6 +125,9 @@ struct __align__(16) TcShared {
   int ex_beg[kMaxExpertsTc];
   int ex_cnt[kMaxExpertsTc];
   int unit_prefix[kMaxExpertsTc + 1];
+  // Gate/up tiles only.
+  int scale_off_up[2];           // per scale buffer: offset of the up rows' first byte
+  uint64_t epi_bar;              // the four epilogue warps
 };
 
 // Position in a ring of n slots: slot index and the parity of its use.
@@ -142,6 +153,7 @@ struct Unit {
   int load;       // token box: load_rows(load) >= nmma
 };
 
+template <bool kSplit>
 __device__ __forceinline__ Unit unit_at(const TcArgs& a, const TcShared& sh, int idx) {
   // Binary search the expert whose block range holds idx / mtiles.
   const int blk = idx / a.mtiles;
@@ -165,8 +177,10 @@ __device__ __forceinline__ Unit unit_at(const TcArgs& a, const TcShared& sh, int
   w.nmma = (w.ntok + 15) / 16 * 16;
   w.load = 0;
   while (load_rows(w.load) < w.nmma) ++w.load;
-  w.m0 = mt * kBM;
-  w.rows = min(kBM, a.O - w.m0);
+  // Gate/up tiles: m0 is the first gate row f0, rows the valid rows of each half.
+  constexpr int tm = kSplit ? kBM / 2 : kBM;
+  w.m0 = mt * tm;
+  w.rows = min(tm, (kSplit ? a.F : a.O) - w.m0);
   return w;
 }
 
@@ -342,7 +356,63 @@ __device__ __forceinline__ bool pop_unit(TcShared& sh, RingPos& pu, int lane, in
   return true;
 }
 
-template <int SB>
+// Barrier of the four epilogue warps, on an mbarrier of four arrivals so
+// that the wait is bounded like every other; false if it gave up.
+__device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool done = mbar_wait(bar, phase);
+  phase ^= 1u;
+  return done;
+}
+
+__device__ __forceinline__ float silu_times(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// Epilogue of a gate/up tile: 16 token columns at a time, each epilogue warp
+// moves its 32 accumulator rows into shared memory (column-major, all four
+// warps' rows side by side); then thread (cq, rp) forms h = silu(gate) * up
+// for gate rows 2rp, 2rp+1 of the tile (their up rows sit 64 rows further,
+// two warps on) and token columns 4cq..4cq+3, in float32, and stores each
+// pair of rows as one bf16x2. The tile of the first rows of a token block
+// also writes its pairs' expert for the down projection. Returns false if a
+// wait gave up.
+__device__ bool swiglu_epilogue(const TcArgs& a, const Unit& w, uint32_t d_cols,
+                                uint32_t lane_base, float* epi_all, int q, int lane,
+                                uint64_t* bar, uint32_t& phase) {
+  float* mine = epi_all + q * (kEpiStage / 4);
+  const int et = 32 * q + lane;
+  const int rp = et & 31, cq = et >> 5;
+  const int r0 = 2 * rp;
+  const float* gsrc = epi_all + (r0 >> 5) * (kEpiStage / 4) + (r0 & 31);
+  const float* usrc = gsrc + 2 * (kEpiStage / 4);
+  const bool row_ok = r0 < w.rows;             // rows is even: r0 + 1 too
+  for (int c0 = 0; c0 < w.nmma; c0 += 16) {
+    uint32_t v[16];
+    tmem_ld16(d_cols + lane_base + (uint32_t)c0, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mine[i * 32 + lane] = __uint_as_float(v[i]);
+    if (!epi_sync(bar, phase, lane)) return false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = 4 * cq + j;
+      if (row_ok && c0 + c < w.ntok) {
+        const int pair = a.plan.pair_list[w.tok0 + c0 + c];
+        const float h0 = silu_times(gsrc[c * 32], usrc[c * 32]);
+        const float h1 = silu_times(gsrc[c * 32 + 1], usrc[c * 32 + 1]);
+        *reinterpret_cast<__nv_bfloat162*>(a.h + (size_t)pair * a.F + w.m0 + r0) =
+            __floats2bfloat162_rn(h0, h1);
+      }
+    }
+    if (!epi_sync(bar, phase, lane)) return false;
+  }
+  if (w.m0 == 0)
+    for (int c = et; c < w.ntok; c += 128) a.sel2[a.plan.pair_list[w.tok0 + c]] = w.e;
+  return true;
+}
+
+// kSplit: gate/up tiles of the SwiGLU expert (see TcArgs::F).
+template <int SB, bool kSplit>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   static_assert(SB >= kRing && SB <= kStagesBMax, "token ring depth");
@@ -375,6 +445,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       mbar_init(&sh.s_empty[b], kDequantWarps);
     }
     mbar_init(&sh.drain, 1);
+    if (kSplit) mbar_init(&sh.epi_bar, 4);
     for (int r = 0; r < kUnitRing; ++r) {
       mbar_init(&sh.u_full[r], 1);
       mbar_init(&sh.u_empty[r], kUnitReaders);
@@ -443,7 +514,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         pu.next(kUnitRing);
         if (idx < 0) break;
         next = atomicAdd(counter, 1);
-        const Unit w = unit_at(a, sh, idx);
+        const Unit w = unit_at<kSplit>(a, sh, idx);
         if (w.ntok <= 0) { --it; continue; }
         // The tile's scale bytes, by one bulk copy of the aligned span that
         // holds them when it stays inside the scales buffer.
@@ -453,13 +524,24 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         const uintptr_t s_lo = reinterpret_cast<uintptr_t>(a.scales + row0 * G);
         const uintptr_t s_hi = s_lo + (uintptr_t)w.rows * G;
         const uintptr_t c_lo = s_lo & ~(uintptr_t)15, c_hi = (s_hi + 15) & ~(uintptr_t)15;
-        const bool copy = c_hi <= reinterpret_cast<uintptr_t>(a.scales_end) &&
-                          c_hi - c_lo <= a.scale_cap;
+        const uintptr_t end = reinterpret_cast<uintptr_t>(a.scales_end);
+        // Gate/up tiles: the up rows' scale bytes are a second span, copied
+        // right after the first.
+        const uintptr_t u_lo = s_lo + (uintptr_t)a.F * G, u_hi = u_lo + (uintptr_t)w.rows * G;
+        const uintptr_t d_lo = u_lo & ~(uintptr_t)15, d_hi = (u_hi + 15) & ~(uintptr_t)15;
+        const uint32_t bytes1 = (uint32_t)(c_hi - c_lo);
+        const uint32_t bytes2 = kSplit ? (uint32_t)(d_hi - d_lo) : 0u;
+        const bool copy = c_hi <= end && (!kSplit || d_hi <= end) &&
+                          (size_t)bytes1 + bytes2 <= a.scale_cap;
         sh.scale_off[sb] = copy ? (int)(s_lo - c_lo) : -1;
+        if constexpr (kSplit) sh.scale_off_up[sb] = copy ? (int)(bytes1 + (u_lo - d_lo)) : -1;
         if (copy) {
-          mbar_arrive_expect_tx(&sh.s_full[sb], (uint32_t)(c_hi - c_lo));
-          bulk_copy_g2s(scale_buf + (size_t)sb * a.scale_cap, reinterpret_cast<const void*>(c_lo),
-                        (uint32_t)(c_hi - c_lo), &sh.s_full[sb], pol);
+          unsigned char* dst = scale_buf + (size_t)sb * a.scale_cap;
+          mbar_arrive_expect_tx(&sh.s_full[sb], bytes1 + bytes2);
+          bulk_copy_g2s(dst, reinterpret_cast<const void*>(c_lo), bytes1, &sh.s_full[sb], pol);
+          if (bytes2)
+            bulk_copy_g2s(dst + bytes1, reinterpret_cast<const void*>(d_lo), bytes2,
+                          &sh.s_full[sb], pol);
         } else {
           mbar_arrive(&sh.s_full[sb]);
         }
@@ -469,8 +551,16 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
             break;
           }
           mbar_arrive_expect_tx(&sh.full_a[pa.idx], kStageA);
-          tma_load_2d(ring_a + (size_t)pa.idx * kStageA, &maps.a, kc * 32, (int)row0,
-                      &sh.full_a[pa.idx], pol);
+          unsigned char* stage = ring_a + (size_t)pa.idx * kStageA;
+          if constexpr (kSplit) {
+            // 64 gate rows, then the 64 matching up rows (same swizzle phase:
+            // the second box starts 2048 bytes in).
+            tma_load_2d(stage, &maps.a_half, kc * 32, (int)row0, &sh.full_a[pa.idx], pol);
+            tma_load_2d(stage + kStageA / 2, &maps.a_half, kc * 32, (int)(row0 + a.F),
+                        &sh.full_a[pa.idx], pol);
+          } else {
+            tma_load_2d(stage, &maps.a, kc * 32, (int)row0, &sh.full_a[pa.idx], pol);
+          }
           pa.next(a.stages_a);
         }
       }
@@ -496,7 +586,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       while (ok) {
         if (!pop_unit<false>(sh, pu, 0, &idx)) { ok = false; break; }
         if (idx < 0) break;
-        const Unit w = unit_at(a, sh, idx);
+        const Unit w = unit_at<kSplit>(a, sh, idx);
         if (w.ntok <= 0) continue;
         const uint32_t tx = (uint32_t)load_rows(w.load) * 128u;
         for (int kc = 0; kc < nk; ++kc, ++issued) {
@@ -528,7 +618,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     for (; ok; ++it) {
       if (!pop_unit<true>(sh, pu, lane, &idx)) { ok = false; break; }
       if (idx < 0) break;
-      const Unit w = unit_at(a, sh, idx);
+      const Unit w = unit_at<kSplit>(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int db = it & 1;
       if (!mbar_wait(&sh.d_empty[db], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
@@ -576,20 +666,25 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     for (; ok; ++it) {
       if (!pop_unit<true>(sh, pu, lane, &idx)) { ok = false; break; }
       if (idx < 0) break;
-      const Unit w = unit_at(a, sh, idx);
+      const Unit w = unit_at<kSplit>(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int sb = it & 1;
       if (!mbar_wait(&sh.s_full[sb], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
-      const int soff = sh.scale_off[sb];
+      // Row m's place in its span: gate/up tiles hold two spans of rows
+      // (m < 64: gate row f0 + m; else up row F + f0 + m - 64).
+      const bool up = kSplit && m >= kBM / 2;
+      const int hrow = min(kSplit ? (m & (kBM / 2 - 1)) : m, w.rows - 1);
+      const int soff = up ? sh.scale_off_up[sb] : sh.scale_off[sb];
       // The choice of scale source is the same for the whole tile: take it
       // once, so the chunk loop holds no global load.
       if (soff >= 0) {
         const unsigned char* srow =
-            scale_buf + (size_t)sb * a.scale_cap + soff + (size_t)min(m, w.rows - 1) * G;
+            scale_buf + (size_t)sb * a.scale_cap + soff + (size_t)hrow * G;
         ok = dequant_tile<SB>(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk,
                               tp, [&](int g) { return (uint32_t)srow[g]; });
       } else {
-        const uint8_t* grow = a.scales + ((size_t)w.e * O + w.m0 + min(m, w.rows - 1)) * G;
+        const uint8_t* grow =
+            a.scales + ((size_t)w.e * O + (up ? a.F : 0) + w.m0 + hrow) * G;
         ok = dequant_tile<SB>(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk,
                               tp, [&](int g) { return (uint32_t)__ldg(grow + g); });
       }
@@ -606,15 +701,27 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     const int m = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     int it = 0, idx;
+    uint32_t epi_phase = 0;
     RingPos pu;
     for (; ok; ++it) {
       if (!pop_unit<true>(sh, pu, lane, &idx)) { ok = false; break; }
       if (idx < 0) break;
-      const Unit w = unit_at(a, sh, idx);
+      const Unit w = unit_at<kSplit>(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int db = it & 1;
       if (!mbar_wait(&sh.d_full[db], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
       tc_fence_after_sync();
+      if constexpr (kSplit) {
+        if (!swiglu_epilogue(a, w, tmem + kDCol + (uint32_t)db * kNMax, lane_base, epi_stage, q,
+                             lane, &sh.epi_bar, epi_phase)) {
+          ok = false;
+          break;
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.d_empty[db]);
+        continue;
+      }
       const bool row_ok = m < w.rows;
       float* out_col = a.part + w.m0 + m;
       // Four consecutive rows per store: this warp's 32 rows x 16 columns go
@@ -670,11 +777,17 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
 // x rows grouped by expert: xg[pos, :] = x[pair_list[pos] / K, :].
 __global__ void __launch_bounds__(256)
 gather_tokens_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xg,
-                     RoutePlan plan, int I, int K) {
+                     RoutePlan plan, int I, int K, int32_t* __restrict__ zero_ids,
+                     int64_t nzero) {
   pdl_launch_dependents();
   pdl_wait();                    // the bucketer's lists are ready
   // The tensor-core kernel after this one takes its units from this counter.
   if (blockIdx.x == 0 && threadIdx.x == 0) plan.meta[kMetaUnitCounter] = 0;
+  // Gate/up tiles: the down projection's ids start at expert 0 (the kernel
+  // after this one writes the valid pairs' experts).
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nzero;
+       i += (int64_t)gridDim.x * blockDim.x)
+    zero_ids[i] = 0;
   const int npairs = plan.meta[kMetaNumPairs];
   const int vec_per_row = I / 8;
   const int warps = blockDim.x / 32;
@@ -720,7 +833,7 @@ size_t tc_shared_bytes(int stages_a, int stages_b, uint32_t scale_cap) {
 
 constexpr size_t kSmemLimit = 227 * 1024;
 
-template <int SB>
+template <int SB, bool kSplit>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& args, size_t smem, cudaStream_t stream) {
   static std::mutex mu;
   static size_t opted[64] = {};
@@ -729,33 +842,46 @@ cudaError_t launch_tc(const TcMaps& maps, const TcArgs& args, size_t smem, cudaS
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && opted[dev] < smem) {
-      cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel<SB>,
+      cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel<SB, kSplit>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (err != cudaSuccess) return err;
       opted[dev] = smem;
     }
   }
-  return launch_after_previous(gemm_tc_kernel<SB>, dim3((unsigned)num_sms_tc()), dim3(kTcThreads),
+  return launch_after_previous(gemm_tc_kernel<SB, kSplit>, dim3((unsigned)num_sms_tc()), dim3(kTcThreads),
                                smem, stream, maps, args);
 }
 
 }  // namespace
 
 cudaError_t launch_gather_tokens(const void* x, const RoutePlan& plan, void* grouped,
-                                 int64_t T, int64_t I, int64_t K, cudaStream_t stream) {
+                                 int64_t T, int64_t I, int64_t K, int32_t* zero_ids,
+                                 cudaStream_t stream) {
   const int64_t P = T * K;
   const int64_t blocks = std::min<int64_t>((P + 7) / 8, (int64_t)num_sms_tc() * 8);
   return launch_after_previous(gather_tokens_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)),
                                dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x),
-                               static_cast<__nv_bfloat16*>(grouped), plan, (int)I, (int)K);
+                               static_cast<__nv_bfloat16*>(grouped), plan, (int)I, (int)K,
+                               zero_ids, zero_ids != nullptr ? P : (int64_t)0);
+}
+
+// Bytes per scale buffer: one tile's span, or the two spans of a gate/up tile.
+uint32_t tc_scale_cap(int64_t G, bool halves) {
+  const uint32_t whole = (uint32_t)((kBM * G + 31) / 16 * 16);
+  const uint32_t two = 2u * (uint32_t)(((kBM / 2) * G + 31) / 16 * 16);
+  return halves ? std::max(whole, two) : whole;
 }
 
 bool gemm_tc_supported(int64_t E, int64_t I, int64_t O) {
   const int64_t G = I / 32;
   if (G % 2 != 0) return false;                    // K chunks of 64
   if (E > kMaxExpertsTc || E * O > 0x7fffffff) return false;
-  const uint32_t scale_cap = (uint32_t)((kBM * G + 31) / 16 * 16);
-  return tc_shared_bytes(kRing, kRing, scale_cap) <= kSmemLimit;
+  return tc_shared_bytes(kRing, kRing, tc_scale_cap(G, false)) <= kSmemLimit;
+}
+
+bool gemm_tc_swiglu_supported(int64_t E, int64_t I, int64_t F) {
+  return F > 0 && F % 32 == 0 && gemm_tc_supported(E, I, 2 * F) &&
+         tc_shared_bytes(kRing, kRing, tc_scale_cap(I / 32, true)) <= kSmemLimit;
 }
 
 size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I) {
@@ -765,7 +891,10 @@ size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I) {
 cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* scales,
                            const RoutePlan& plan, void* grouped, float* part,
                            unsigned long long* status, int64_t T, int64_t E, int64_t I,
-                           int64_t O, int64_t K, cudaStream_t stream) {
+                           int64_t O, int64_t K, const SwigluTiles& swiglu,
+                           cudaStream_t stream) {
+  if (swiglu.F > 0 && (O != 2 * swiglu.F || !gemm_tc_swiglu_supported(E, I, swiglu.F)))
+    return cudaErrorInvalidValue;
   const int64_t G = I / 32, P = T * K;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -780,6 +909,11 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    const cuuint32_t half_box[2] = {32, (cuuint32_t)(kBM / 2)};
+    if (enc(&maps.a_half, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed), dims,
+            strides, half_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -803,8 +937,12 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
   args.G = (int)G;
   args.O = (int)O;
   args.K = (int)K;
-  args.mtiles = (int)((O + kBM - 1) / kBM);
-  args.scale_cap = (uint32_t)((kBM * G + 31) / 16 * 16);
+  args.F = (int)swiglu.F;
+  args.h = static_cast<__nv_bfloat16*>(swiglu.h);
+  args.sel2 = swiglu.sel2;
+  args.mtiles = swiglu.F > 0 ? (int)((swiglu.F + kBM / 2 - 1) / (kBM / 2))
+                             : (int)((O + kBM - 1) / kBM);
+  args.scale_cap = tc_scale_cap(G, swiglu.F > 0);
   // As many token stages as fit next to 8 packed-weight stages (their
   // refill latency is what the MMAs wait on), then as deep a packed-weight
   // ring as shared memory allows, a multiple of kRing so that each
@@ -816,9 +954,15 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
   args.stages_a = sa;
   const size_t smem = tc_shared_bytes(sa, sb, args.scale_cap);
   switch (sb) {
-    case 6: return launch_tc<6>(maps, args, smem, stream);
-    case 5: return launch_tc<5>(maps, args, smem, stream);
-    default: return launch_tc<4>(maps, args, smem, stream);
+    case 6:
+      return swiglu.F > 0 ? launch_tc<6, true>(maps, args, smem, stream)
+                          : launch_tc<6, false>(maps, args, smem, stream);
+    case 5:
+      return swiglu.F > 0 ? launch_tc<5, true>(maps, args, smem, stream)
+                          : launch_tc<5, false>(maps, args, smem, stream);
+    default:
+      return swiglu.F > 0 ? launch_tc<4, true>(maps, args, smem, stream)
+                          : launch_tc<4, false>(maps, args, smem, stream);
   }
 }
 

@@ -131,12 +131,27 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16,
 // Prefill-regime grouped GEMM on the tensor cores (bf16 tokens).
 bool gemm_tc_supported(int64_t E, int64_t I, int64_t O);
 size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I);
+
+// Gate/up tiles for the SwiGLU expert (F > 0): the tensor-core kernel runs
+// the stacked gate/up projection (O = 2F rows, gate rows first) in tiles of
+// 64 gate rows plus the matching 64 up rows and writes h = silu(gate) * up
+// (bf16, (P, F)) and each pair's expert (sel2) instead of partial results.
+struct SwigluTiles {
+  int64_t F = 0;
+  void* h = nullptr;
+  int32_t* sel2 = nullptr;
+};
+bool gemm_tc_swiglu_supported(int64_t E, int64_t I, int64_t F);
+
+// zero_ids (P ints) or nullptr: also set to 0 (gate/up tiles).
 cudaError_t launch_gather_tokens(const void* x, const RoutePlan& plan, void* grouped,
-                                 int64_t T, int64_t I, int64_t K, cudaStream_t stream);
+                                 int64_t T, int64_t I, int64_t K, int32_t* zero_ids,
+                                 cudaStream_t stream);
 cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* scales,
                            const RoutePlan& plan, void* grouped, float* part,
                            unsigned long long* status, int64_t T, int64_t E, int64_t I,
-                           int64_t O, int64_t K, cudaStream_t stream);
+                           int64_t O, int64_t K, const SwigluTiles& swiglu,
+                           cudaStream_t stream);
 
 // Which kernel computes the routed linear for these sizes.
 enum class LinearPath { kGemv, kGemm };

@@ -226,3 +226,35 @@ def test_alias_and_shape_checks():
     d = wl.device_tensors("cuda")
     with pytest.raises(_native.MXFP4Error):
         mxfp4_swiglu_expert(*[d[k] for k in wl.ARGS], out=d["y_shared"])
+
+
+# ------------------------------------------------ gate/up tiles (prefill) --
+@pytest.mark.parametrize("T,E,K,I,F,O,bad,i64", [(300, 6, 2, 256, 128, 192, False, False),
+                                                 (257, 5, 3, 64, 96, 80, False, True),
+                                                 (1000, 16, 4, 320, 160, 128, False, False),
+                                                 (400, 7, 2, 128, 64, 64, True, False)])
+def test_gate_up_tiles_match_separate_swiglu(monkeypatch, T, E, K, I, F, O, bad, i64):
+    # On the tensor cores the gate/up kernel forms h in tiles of 64 gate rows
+    # and their 64 up rows (partial tiles when F is not a multiple of 64); the
+    # separate SwiGLU kernel (MXFP4EL_SWIGLU_TILES=0) reads the partial
+    # results instead. Same arithmetic, so the same bits.
+    wl = workloads.make_swiglu(T=T, E=E, K=K, I=I, F=F, O=O, dtype=torch.bfloat16,
+                               seed=T + F, scale_lo=120, scale_hi=126)
+    if bad:
+        sel = wl.sel.clone()
+        sel[3, 0] = -1
+        sel[10, 1] = E
+        sel[T - 1, 0] = 1 << 20
+        wl.sel = sel
+    if i64:
+        wl.sel = wl.sel.long()
+    device_errors()
+    out = run(wl)
+    n_bad = device_errors()
+    monkeypatch.setenv("MXFP4EL_SWIGLU_TILES", "0")
+    ref = run(wl)
+    assert device_errors() == n_bad == (3 if bad else 0)
+    assert torch.equal(out, ref)
+    rows = np.array(sorted({0, 3, 10, T - 1, *np.random.default_rng(T).integers(0, T, 8)}))
+    r = check(out[torch.from_numpy(rows).cuda()], wl, rows=rows, what=f"tiles T={T} F={F}")
+    assert r["bad"] == (3 if bad else 0)
