@@ -238,7 +238,9 @@ void carve_swiglu(void* base, int64_t T, int64_t E, int64_t I, int64_t F, int64_
   const int64_t P = T * K;
   const size_t tb = token_dtype == MXFP4EL_DTYPE_BF16 ? 2 : 4;
   auto at = [&](size_t off) { return base ? static_cast<char*>(base) + off : nullptr; };
-  carve_workspace(base, T, E, I, 2 * F, K, token_dtype, &sw->gate_up);
+  // Gate/up tiles write h directly: no partial results for that projection.
+  const bool tiles = K > 0 && E > 0 && swiglu_tiles_used(T, E, I, F, K, token_dtype);
+  carve_workspace(base, T, E, I, 2 * F, K, token_dtype, &sw->gate_up, !tiles);
   size_t off = align_up(sw->gate_up.bytes);
   carve_workspace(at(off), P, E, F, O, 1, token_dtype, &sw->down);
   off = align_up(off + sw->down.bytes);
@@ -334,7 +336,7 @@ int cached_workspace(size_t bytes, cudaStream_t s, void** base) {
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
-                     int64_t K, int token_dtype, Workspace* ws) {
+                     int64_t K, int token_dtype, Workspace* ws, bool with_part) {
   const int64_t P = T * K;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -359,7 +361,9 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
   ws->plan.unit_begin =
       K > 0 && !gemm ? reinterpret_cast<int*>(take((kMaxSplitCtas + 1) * sizeof(int))) : nullptr;
   const size_t ncol = (size_t)linear_partial_columns(T, E, I, O, K, token_dtype);
-  ws->part = reinterpret_cast<float*>(take((size_t)P * ncol * (size_t)O * sizeof(float)));
+  ws->part = with_part
+                 ? reinterpret_cast<float*>(take((size_t)P * ncol * (size_t)O * sizeof(float)))
+                 : nullptr;
   ws->bytes = off;
   return true;
 }

@@ -68,8 +68,10 @@ struct Workspace {
 };
 
 // Offsets of every region for the given sizes; base == nullptr only sizes.
+// with_part = false: no partial-result buffer (ws->part = nullptr), for a
+// linear whose kernel writes something else (gate/up tiles).
 bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
-                     int64_t K, int token_dtype, Workspace* ws);
+                     int64_t K, int token_dtype, Workspace* ws, bool with_part = true);
 
 // Partial results per (pair, row) that the chosen linear kernel writes.
 int linear_partial_columns(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
