@@ -226,6 +226,12 @@ bool swiglu_tiles_used(int64_t T, int64_t E, int64_t I, int64_t F, int64_t K,
          gemm_tc_swiglu_supported(E, I, F);
 }
 
+// Whether the down projection of a SwiGLU call whose gate/up projection
+// runs in gate/up tiles also runs on the tensor cores, on the gate/up lists.
+bool down_reuses_lists(int64_t P, int64_t E, int64_t F, int64_t O, int token_dtype) {
+  return choose_path(P, E, F, O, 1, token_dtype) == LinearPath::kGemm;
+}
+
 struct SwigluWorkspace {
   Workspace gate_up, down;   // the two projections' own workspaces
   void* h = nullptr;         // (P, F) token dtype
@@ -263,11 +269,17 @@ int run_swiglu(const void* x, const uint8_t* gu_packed, const uint8_t* gu_scales
     // On the tensor cores the gate/up kernel forms h itself (tiles of gate
     // rows and their up rows), so the partial results never leave it.
     const bool tiles = E > 0 && swiglu_tiles_used(T, E, I, F, K, token_dtype);
+    // With the down projection on the tensor cores too, it runs on the
+    // gate/up lists (the same experts, the pairs in the same order), so the
+    // gate/up tiles write h already grouped by expert: no second bucketer,
+    // no gather.
+    const bool reuse = tiles && down_reuses_lists(P, E, F, O, token_dtype);
     SwigluTiles st;
     if (tiles) {
       st.F = F;
       st.h = sw.h;
-      st.sel2 = sw.sel2;
+      st.sel2 = reuse ? nullptr : sw.sel2;
+      st.grouped = reuse;
     }
     if (run_linear(x, gu_packed, gu_scales, sel, T, E, I, 2 * F, K, token_dtype, index_dtype,
                    sw.gate_up, stream, st) != cudaSuccess)
@@ -279,9 +291,19 @@ int run_swiglu(const void* x, const uint8_t* gu_packed, const uint8_t* gu_scales
                         index_dtype, E, P, F, token_dtype, sw.h, sw.sel2,
                         stream) != cudaSuccess)
         return MXFP4EL_ERR_CUDA;
-      if (run_linear(sw.h, dn_packed, dn_scales, sw.sel2, P, E, F, O, 1, token_dtype,
-                     MXFP4EL_INDEX_I32, sw.down, stream) != cudaSuccess)
+      if (reuse) {
+        unsigned long long* status = device_status_words();
+        if (status == nullptr) return MXFP4EL_ERR_CUDA;
+        mark(MXFP4EL_STAGE_LINEAR, true, stream);
+        const cudaError_t err =
+            launch_gemm_tc(sw.h, dn_packed, dn_scales, sw.gate_up.plan, sw.h, sw.down.part,
+                           status, P, E, F, O, 1, SwigluTiles{}, stream, kMetaUnitCounter2);
+        mark(MXFP4EL_STAGE_LINEAR, false, stream);
+        if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
+      } else if (run_linear(sw.h, dn_packed, dn_scales, sw.sel2, P, E, F, O, 1, token_dtype,
+                            MXFP4EL_INDEX_I32, sw.down, stream) != cudaSuccess) {
         return MXFP4EL_ERR_CUDA;
+      }
     }
   }
   mark(MXFP4EL_STAGE_COMBINE, true, stream);

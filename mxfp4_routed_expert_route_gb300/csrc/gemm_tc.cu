@@ -94,8 +94,10 @@ struct TcArgs {
   // matching up rows F + f0..; the epilogue writes h = silu(gate) * up in
   // bf16 and the pairs' expert ids instead of the partial results.
   int F;
-  __nv_bfloat16* h;              // (P, F)
-  int32_t* sel2;                 // (P): expert of each pair (zeroed by the gather)
+  __nv_bfloat16* h;              // (P, F), row = pair (or position in the lists: h_grouped)
+  int32_t* sel2;                 // (P): expert of each pair (zeroed by the gather), or null
+  int h_grouped;
+  int counter_word;              // plan.meta word this kernel takes its units from
 };
 
 struct TcMaps {
@@ -397,16 +399,17 @@ __device__ bool swiglu_epilogue(const TcArgs& a, const Unit& w, uint32_t d_cols,
     for (int j = 0; j < 4; ++j) {
       const int c = 4 * cq + j;
       if (row_ok && c0 + c < w.ntok) {
-        const int pair = a.plan.pair_list[w.tok0 + c0 + c];
+        const int pos = w.tok0 + c0 + c;
+        const int row = a.h_grouped ? pos : a.plan.pair_list[pos];
         const float h0 = silu_times(gsrc[c * 32], usrc[c * 32]);
         const float h1 = silu_times(gsrc[c * 32 + 1], usrc[c * 32 + 1]);
-        *reinterpret_cast<__nv_bfloat162*>(a.h + (size_t)pair * a.F + w.m0 + r0) =
+        *reinterpret_cast<__nv_bfloat162*>(a.h + (size_t)row * a.F + w.m0 + r0) =
             __floats2bfloat162_rn(h0, h1);
       }
     }
     if (!epi_sync(bar, phase, lane)) return false;
   }
-  if (w.m0 == 0)
+  if (w.m0 == 0 && a.sel2 != nullptr)
     for (int c = et; c < w.ntok; c += 128) a.sel2[a.plan.pair_list[w.tok0 + c]] = w.e;
   return true;
 }
@@ -504,7 +507,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const uint64_t pol = l2_evict_first_policy();     // weights: read once
       int it = 0, issued = 0;
       RingPos pa, pu;
-      int* counter = &a.plan.meta[kMetaUnitCounter];
+      int* counter = &a.plan.meta[a.counter_word];
       int next = atomicAdd(counter, 1);                  // one unit ahead
       for (;; ++it) {
         const int idx = next < num_units ? next : -1;
@@ -782,7 +785,10 @@ gather_tokens_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restr
   pdl_launch_dependents();
   pdl_wait();                    // the bucketer's lists are ready
   // The tensor-core kernel after this one takes its units from this counter.
-  if (blockIdx.x == 0 && threadIdx.x == 0) plan.meta[kMetaUnitCounter] = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    plan.meta[kMetaUnitCounter] = 0;
+    plan.meta[kMetaUnitCounter2] = 0;      // a second tensor-core kernel on these lists
+  }
   // Gate/up tiles: the down projection's ids start at expert 0 (the kernel
   // after this one writes the valid pairs' experts).
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nzero;
@@ -892,7 +898,7 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
                            const RoutePlan& plan, void* grouped, float* part,
                            unsigned long long* status, int64_t T, int64_t E, int64_t I,
                            int64_t O, int64_t K, const SwigluTiles& swiglu,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int counter_word) {
   if (swiglu.F > 0 && (O != 2 * swiglu.F || !gemm_tc_swiglu_supported(E, I, swiglu.F)))
     return cudaErrorInvalidValue;
   const int64_t G = I / 32, P = T * K;
@@ -940,6 +946,8 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
   args.F = (int)swiglu.F;
   args.h = static_cast<__nv_bfloat16*>(swiglu.h);
   args.sel2 = swiglu.sel2;
+  args.h_grouped = swiglu.grouped ? 1 : 0;
+  args.counter_word = counter_word;
   args.mtiles = swiglu.F > 0 ? (int)((swiglu.F + kBM / 2 - 1) / (kBM / 2))
                              : (int)((O + kBM - 1) / kBM);
   args.scale_cap = tc_scale_cap(G, swiglu.F > 0);

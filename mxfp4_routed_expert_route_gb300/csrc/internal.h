@@ -28,6 +28,8 @@ constexpr int kMetaNumActive = 0;   // experts with at least one valid pair
 constexpr int kMetaNumPairs = 1;    // valid pairs
 constexpr int kMetaUnitCounter = 2; // next unit of the tensor-core kernel (reset by the gather)
 constexpr int kMetaPoolCounter = 3; // next pool unit of the staged GEMV (reset by the GEMV)
+constexpr int kMetaUnitCounter2 = 4; // next unit of a second tensor-core kernel on the same
+                                     // lists (the SwiGLU down projection; reset by the gather)
 constexpr int kMetaWords = 64;
 
 // Routing lists written by the bucketer, all in device memory.
@@ -141,7 +143,8 @@ size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I);
 struct SwigluTiles {
   int64_t F = 0;
   void* h = nullptr;
-  int32_t* sel2 = nullptr;
+  int32_t* sel2 = nullptr;   // or nullptr: not needed
+  bool grouped = false;      // h rows in the lists' (expert-grouped) order, not by pair
 };
 bool gemm_tc_swiglu_supported(int64_t E, int64_t I, int64_t F);
 
@@ -153,7 +156,7 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
                            const RoutePlan& plan, void* grouped, float* part,
                            unsigned long long* status, int64_t T, int64_t E, int64_t I,
                            int64_t O, int64_t K, const SwigluTiles& swiglu,
-                           cudaStream_t stream);
+                           cudaStream_t stream, int counter_word = kMetaUnitCounter);
 
 // Which kernel computes the routed linear for these sizes.
 enum class LinearPath { kGemv, kGemm };
