@@ -185,3 +185,18 @@ def test_swiglu_argument_checks(lib):
     assert n1 >= 32 * 5760 * 4 + 32 * 2880 * 4 + 32 * 2880 * 2 and n1 % 256 == 0
     g = lib.mxfp4_swiglu_expert_with_workspace
     assert g(*ok, 4, 4, 64, 64, 8, 2, 0, 0, None, 0, None) == n.ERR_WORKSPACE
+
+
+def test_swiglu_scratch_follows_the_gate_up_tiles(lib, monkeypatch):
+    # Prefill shape on the tensor cores: the gate/up tiles write h directly,
+    # so the call needs no float32 partial results for the gate/up
+    # projection (T*K*2F*4 bytes); the separate-kernel path (test knob) does.
+    ws = lib.mxfp4_swiglu_expert_workspace_size
+    T, E, I, F, O, K = 4096, 128, 2880, 2880, 2880, 4
+    tiles, fp32, decode = ws(T, E, I, F, O, K, 1), ws(T, E, I, F, O, K, 0), ws(8, E, I, F, O, K, 1)
+    monkeypatch.setenv("MXFP4EL_SWIGLU_TILES", "0")
+    separate = ws(T, E, I, F, O, K, 1)
+    assert separate - tiles >= T * K * 2 * F * 4
+    # fp32 tokens and decode batches never take the tensor cores: the knob
+    # changes nothing there.
+    assert ws(T, E, I, F, O, K, 0) == fp32 and ws(8, E, I, F, O, K, 1) == decode
