@@ -41,6 +41,14 @@
 // overlap. Every wait is bounded;
 // a role whose wait gives up records it, stops, and the CTA still waits
 // (bounded) for its own copies and MMAs before freeing TMEM.
+//
+// Gate/up tiles (gemm_tc_kernel<SB, true>, the SwiGLU expert's stacked
+// gate/up projection, 2F rows with the gate rows first): a tile's 128 rows
+// are 64 gate rows f0.. and the matching 64 up rows F + f0.. (two 64-row TMA
+// boxes into one stage, two scale spans), so the epilogue holds g and u of
+// the same (pair, f) and writes h = silu(g) * u in bf16 instead of partial
+// results, by pair or in the lists' grouped order; the down projection can
+// then run as a second instance on the same lists (its own unit counter).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
