@@ -2,15 +2,19 @@
 """Benchmark of the MXFP4 routed expert linear on one GB300 (or N replicas).
 
 One step = one call of the whole path (routing bucketer, routed expert
-linear, combine) over one batch of the named workload, inputs resident in HBM.
-Default workload: decode (T=8 tokens, E=128 experts, K=4, I=2880, O=5760,
-bf16 tokens, MXFP4 weights), uniform distinct picks, seeded synthetic data.
+linear, combine) over one batch of a named workload, inputs resident in HBM.
+The headline workload is the largest single-GPU one, skewed prefill (T=8192
+tokens, E=384 experts, K=8 picks from Zipf(1.2) popularity, I=7168,
+O=4096, bf16 tokens, MXFP4 weights); decode, wide decode and prefill are
+measured in the same run and reported under "configs", each with its own
+roofline, end-to-end number, clocks and CPU baseline. Seeded synthetic data.
 
 Prints one JSON line (rank 0). The path does not exchange data between
 GPUs: with --gpus N every rank runs its own replica (weak scaling) and the
-value is the bytes all ranks moved divided by the slowest rank's time.
+value is the work all ranks did divided by the slowest rank's time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--configs all|none|a,b]
   python bench.py --impl reference ...   # the float64 CPU oracle, timed
 """
 from __future__ import annotations
@@ -30,6 +34,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "routed-expert GB/s and TFLOP/s at 1 GB300, % of HBM/bf16 roofline"
 FLUSH_BYTES = 512 << 20          # > 129 MB of L2: written between steps
+# The headline: the largest single-GPU workload (8192 tokens, 384 experts,
+# 8 picks, Zipf(1.2) popularity); the others are measured in the same run.
+HEADLINE = "skewed_prefill"
+ALL_CONFIGS = ("decode", "wide_decode", "prefill", "skewed_prefill")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 
@@ -37,10 +45,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="the workload of the line's headline value")
+    ap.add_argument("--configs", default="all",
+                    help="other workloads measured in the same run and reported under "
+                         "'configs': 'all', 'none' or a comma-separated list")
+    ap.add_argument("--cpu-budget", type=float, default=6.0,
+                    help="seconds of oracle time per workload for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the router and SwiGLU-expert fields (clean launch lists)")
@@ -235,7 +249,7 @@ def sample_bytes(wl, rows):
     return path_bytes(wl, U, T=len(rows))
 
 
-def cpu_baseline(wl, hbm_bound, budget_s=15.0):
+def cpu_baseline(wl, hbm_bound, budget_s=6.0):
     """The oracle as it stands on this host's cores, on a bounded token sample."""
     import numpy as np
     import oracle
@@ -248,6 +262,15 @@ def cpu_baseline(wl, hbm_bound, budget_s=15.0):
             "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"tokens 0..{n - 1} of the {wl.name} batch ({n}/{wl.T}), "
                       f"all O={wl.O} rows, one run of {t:.2f} s"}
+
+
+def workload_config(wl, U, world):
+    """The workload description both arms print as ``config``."""
+    return {"workload": wl.name, "T": wl.T, "E": wl.E, "K": wl.K, "I": wl.I, "O": wl.O,
+            "tokens": "bf16" if token_bytes(wl) == 2 else "fp32",
+            "weights": "mxfp4 (e2m1 codes + e8m0 scale per 32)",
+            "picks": wl.meta["picks"], "experts_touched": U, "seed": wl.meta["seed"],
+            "parallelism": f"replicas x{world}"}
 
 
 def run_reference(args, rank):
@@ -275,11 +298,11 @@ def run_reference(args, rank):
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "K": wl.K, "I": wl.I,
-                   "O": wl.O, "sample_tokens": n, "seed": wl.meta["seed"]},
+        "config": workload_config(wl, U, 1),
         "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": f"tokens 0..{n - 1} of the {wl.name} batch per step"},
+                         "sample": f"tokens 0..{n - 1} of the {wl.name} batch "
+                                   f"({n}/{wl.T}), all O={wl.O} rows, per step"},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -330,6 +353,7 @@ def measure_router(wl, d, dev, stream, flush, warmup, n, peaks):
 
 
 SWIGLU_FOR = {"decode": "swiglu_decode", "prefill": "swiglu_prefill"}
+ROUTER_FOR = ("decode", "prefill")
 
 
 def measure_swiglu(name, dev, stream, flush, warmup, n, peaks):
@@ -379,27 +403,33 @@ def measure_swiglu(name, dev, stream, flush, warmup, n, peaks):
             "frac": t_roof / (us * 1e-6)}
 
 
-def run_ours(args, rank, world):
+def linear_dtype_label(wl, gemm):
+    """What the routed linear computes in, for the line's ``dtype``."""
+    if gemm:
+        return "bf16 x bf16 -> f32 (tensor cores; exact MXFP4 decode to bf16)"
+    if token_bytes(wl) == 2:
+        return "f16x2 products summed in chains of 8, f32 across groups (bf16 tokens)"
+    return "f32"
+
+
+def measure_workload(name, args, lib, dev, rank, world):
+    """Every number of one workload: whole steps (device-timed, L2 flushed),
+    the dominant kernel's CUDA-event duration inside the same steps, the
+    end-to-end steps through the public call with pinned host I/O, the
+    router and SwiGLU extras where they apply, and the oracle's CPU
+    baseline (rank 0 at N=1)."""
     import ctypes
 
-    import numpy as np
     import torch
     import torch.distributed as dist
 
-    from mxfp4_routed_expert_route_gb300 import (_native, build, mxfp4_expert_linear,
-                                                 workloads)
+    from mxfp4_routed_expert_route_gb300 import (_native, mxfp4_expert_linear, workloads,
+                                                 workspace_size)
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    build.build()
-    lib = _native.load()
-
-    wl = workloads.named(args.workload)
+    wl = workloads.named(name)
     U = workloads.experts_touched(wl.sel, wl.E)
     d = wl.device_tensors(dev)
     out = torch.empty((wl.T, wl.O), dtype=wl.dtype, device=dev)
-    from mxfp4_routed_expert_route_gb300 import workspace_size
     ws = torch.empty(max(1, workspace_size(wl.T, wl.E, wl.I, wl.O, wl.K, wl.dtype)),
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -424,11 +454,11 @@ def run_ours(args, rank, world):
         flush.zero_()
         step()
 
-    # Timed loop A: whole steps, for the headline value. Nothing is recorded
-    # between the library's kernels, so their launches may overlap.
+    # Timed loop A: whole steps, for the value. Nothing is recorded between
+    # the library's kernels, so their launches may overlap.
     ev = [(new_event(), new_event()) for _ in range(K)]
     barrier()
-    sampler = ClockSampler(gpu_id_for(local))
+    sampler = ClockSampler(gpu_id_for(dev.index))
     sampler.start()
     launches0 = lib.mxfp4el_kernel_launches()
     barrier()
@@ -522,12 +552,11 @@ def run_ours(args, rank, world):
     d2h = out_h[0].numel() * out_h[0].element_size()
 
     peaks, peaks_src = load_peaks()
-    router = None if args.no_extras else measure_router(wl, d, dev, stream, flush, W,
-                                                          min(K, 200), peaks)
+    extras = not args.no_extras
+    router = (measure_router(wl, d, dev, stream, flush, W, min(K, 200), peaks)
+              if extras and wl.name in ROUTER_FOR else None)
     swiglu = (measure_swiglu(SWIGLU_FOR[wl.name], dev, stream, flush, W, min(K, 100), peaks)
-              if wl.name in SWIGLU_FOR and not args.no_extras else None)
-    if rank != 0:
-        return
+              if extras and wl.name in SWIGLU_FOR else None)
     gemm = lib.mxfp4el_linear_path(wl.T, wl.E, wl.I, wl.O, wl.K,
                                    _native.DTYPE_BF16 if token_bytes(wl) == 2
                                    else _native.DTYPE_F32) == _native.PATH_GEMM
@@ -564,18 +593,12 @@ def run_ours(args, rank, world):
                     "bytes_per_launch": lin_bytes, "launch_us": lin_mean_s * 1e6}
     roofline["traffic"] = ncu_traffic(kernel, wl.name)
     e2e_v = whole_job_rate(bytes_step if hbm_bound else flops_step, K, world, e2e_max)
-    line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
-        "steps": K, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if gemm else "f32",
-        "data": "synthetic",
-        "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "K": wl.K, "I": wl.I,
-                   "O": wl.O, "tokens": "bf16" if token_bytes(wl) == 2 else "fp32",
-                   "weights": "mxfp4 (e2m1 codes + e8m0 scale per 32)",
-                   "picks": wl.meta["picks"], "experts_touched": U,
-                   "seed": wl.meta["seed"], "parallelism": f"replicas x{world}",
-                   "linear": "tensor-core grouped GEMM" if gemm else "CUDA-core GEMV",
-                   "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)"},
+    res = {
+        "value": value, "unit": unit, "ms_per_step": ms_step,
+        "dtype": linear_dtype_label(wl, gemm),
+        "config": workload_config(wl, U, world),
+        "linear": "tensor-core grouped GEMM" if gemm else "CUDA-core GEMV",
+        "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)",
         "gbps": gbps, "tflops": tflops,
         "path_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_step * 1e3,
                           "frac": t_roof / (ms_step / 1e3), "bytes_alg": bytes_step,
@@ -589,13 +612,48 @@ def run_ours(args, rank, world):
                             "computes, double-buffered; all copies inside the timed span",
                 "l2": "not flushed: each step streams more than L2 (its selected weights)"},
         "gpu_launches": int(launches),
-        "router": router,
-        "swiglu_expert": swiglu,
         "clocks": clocks,
         "wall_s": wall,
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, hbm_bound)
+    if router is not None:
+        res["router"] = router
+    if swiglu is not None:
+        res["swiglu_expert"] = swiglu
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, hbm_bound, budget_s=args.cpu_budget)
+    return res
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    from mxfp4_routed_expert_route_gb300 import _native, build
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    lib = _native.load()
+
+    names = [args.workload]
+    if args.configs != "none":
+        listed = ALL_CONFIGS if args.configs == "all" else args.configs.split(",")
+        names = [n for n in listed if n != args.workload] + [args.workload]
+    results = {}
+    for name in names:
+        results[name] = measure_workload(name, args, lib, dev, rank, world)
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return
+    head = results[args.workload]
+    line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": head["dtype"], "data": "synthetic"}
+    line.update({k: v for k, v in head.items() if k not in line and k != "value"})
+    if len(results) > 1:
+        line["configs"] = {n: results[n] for n in ALL_CONFIGS if n in results}
+        line["configs"].update({n: r for n, r in results.items() if n not in line["configs"]})
     print(json.dumps(line), flush=True)
 
 

@@ -257,9 +257,15 @@ int mxfp4_swiglu_expert_with_workspace(const void* latent_tokens,
  * of T=8 tokens, K=4, I=2880, O=5760 needs about 2.2 MiB and fits, while
  * T=16, K=8, I=7168, O=4096 needs about 14 MiB and is refused.
  *
+ * Arguments are checked exactly as by mxfp4_expert_linear, in the same
+ * order, so a call that has another error returns that error's code; only a
+ * call those checks accept can be refused with MXFP4EL_ERR_TOO_LARGE.
+ *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with the device current); make that first
- * call before any stream capture. Every call on a device shares the one
+ * call before any stream capture. The address is kept until the process
+ * exits: do not use this entry point on a device after cudaDeviceReset (or
+ * any other teardown of its primary context). Every call on a device shares the one
  * array, which keeps the previous call's contents; nothing in it needs to
  * start at zero, because the kernels initialise everything they read. Calls
  * that overlap on the GPU (on different streams, or from different threads

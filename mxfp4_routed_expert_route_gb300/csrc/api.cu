@@ -37,7 +37,23 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
   return a0 < b0 + bn && b0 < a0 + an;
 }
 
-int validate(const void* x, const uint8_t* packed, const uint8_t* scales,
+std::atomic<int64_t> g_launches{0};
+
+struct StageEvents {
+  cudaEvent_t start = nullptr, end = nullptr;
+};
+StageEvents g_stage[MXFP4EL_NUM_STAGES];
+
+void mark(int stage, bool begin, cudaStream_t stream) {
+  const cudaEvent_t ev = begin ? g_stage[stage].start : g_stage[stage].end;
+  if (ev != nullptr) cudaEventRecord(ev, stream);
+}
+
+}  // namespace
+
+// Argument checks of every routed-linear entry point, in the order the
+// header documents; returns MXFP4EL_OK or the first error found.
+int validate_linear(const void* x, const uint8_t* packed, const uint8_t* scales,
              const void* sel, const float* p, const void* ys, void* out,
              int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
              int token_dtype, int index_dtype) {
@@ -69,20 +85,6 @@ int validate(const void* x, const uint8_t* packed, const uint8_t* scales,
     if (overlaps(out, out_bytes, inputs[i], sizes[i])) return MXFP4EL_ERR_ALIAS;
   return MXFP4EL_OK;
 }
-
-std::atomic<int64_t> g_launches{0};
-
-struct StageEvents {
-  cudaEvent_t start = nullptr, end = nullptr;
-};
-StageEvents g_stage[MXFP4EL_NUM_STAGES];
-
-void mark(int stage, bool begin, cudaStream_t stream) {
-  const cudaEvent_t ev = begin ? g_stage[stage].start : g_stage[stage].end;
-  if (ev != nullptr) cudaEventRecord(ev, stream);
-}
-
-}  // namespace
 
 LinearPath choose_path(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype) {
   const bool tc_ok = token_dtype == MXFP4EL_DTYPE_BF16 && E > 0 && gemm_tc_supported(E, I, O);
@@ -413,7 +415,7 @@ extern "C" int mxfp4_expert_linear_with_workspace(
     const float* mixture_weights, const void* shared_output, void* out,
     int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype,
     int index_dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = validate(latent_tokens, packed_weights, scale_bytes, selected_experts,
+  int rc = validate_linear(latent_tokens, packed_weights, scale_bytes, selected_experts,
                     mixture_weights, shared_output, out, T, E, I, O, K,
                     token_dtype, index_dtype);
   if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
@@ -437,7 +439,7 @@ extern "C" int mxfp4_expert_linear(const void* latent_tokens,
                                    int64_t T, int64_t E, int64_t I, int64_t O,
                                    int64_t K, int token_dtype, int index_dtype,
                                    void* stream) {
-  int rc = validate(latent_tokens, packed_weights, scale_bytes, selected_experts,
+  int rc = validate_linear(latent_tokens, packed_weights, scale_bytes, selected_experts,
                     mixture_weights, shared_output, out, T, E, I, O, K,
                     token_dtype, index_dtype);
   if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
@@ -488,7 +490,7 @@ extern "C" int mxfp4_expert_linear_routed(const void* latent_tokens,
                                           int64_t K, int token_dtype, void* stream) {
   // Check the linear's arguments first: nothing is enqueued for a call that
   // would fail half way.
-  int rc = validate(latent_tokens, packed_weights, scale_bytes, selected_experts,
+  int rc = validate_linear(latent_tokens, packed_weights, scale_bytes, selected_experts,
                     mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
                     MXFP4EL_INDEX_I32);
   if (rc != MXFP4EL_OK) return rc;

@@ -158,6 +158,13 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
                            int64_t O, int64_t K, const SwigluTiles& swiglu,
                            cudaStream_t stream, int counter_word = kMetaUnitCounter);
 
+// Argument checks shared by every routed-linear entry point (api.cu):
+// MXFP4EL_OK or the first error, in the order the public header documents.
+int validate_linear(const void* x, const uint8_t* packed, const uint8_t* scales,
+                    const void* sel, const float* p, const void* ys, void* out,
+                    int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                    int token_dtype, int index_dtype);
+
 // Which kernel computes the routed linear for these sizes.
 enum class LinearPath { kGemv, kGemm };
 LinearPath choose_path(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype);

@@ -15,7 +15,9 @@
 // In host code the array's name is only a host-side stand-in for the device
 // symbol: it is not a device address. The device address is looked up once
 // per device, with that device current, by cudaGetSymbolAddress, and that
-// address is what the kernels receive.
+// address is what the kernels receive. The looked-up address is kept for the
+// life of the process, so this entry point must not be used on a device
+// after cudaDeviceReset (or any other teardown of its primary context).
 #include <mutex>
 
 #include "../../include/mxfp4_expert_linear.h"
@@ -62,21 +64,18 @@ extern "C" int mxfp4_expert_linear_static_scratch(
     const float* mixture_weights, const void* shared_output, void* out,
     int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype,
     int index_dtype, void* stream) {
+  // The same checks, in the same order, as the other entry points; only a
+  // call they accept can be refused for its size.
+  const int rc = mxfp4el::validate_linear(latent_tokens, packed_weights, scale_bytes,
+                                          selected_experts, mixture_weights, shared_output,
+                                          out, T, E, I, O, K, token_dtype, index_dtype);
+  if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
   const size_t need = mxfp4_expert_linear_workspace_size(T, E, I, O, K, token_dtype);
-  if (need == (size_t)-1) {
-    // Sizes or dtype the library rejects: report the same code as the
-    // other entry points would.
-    if (token_dtype != MXFP4EL_DTYPE_F32 && token_dtype != MXFP4EL_DTYPE_BF16)
-      return MXFP4EL_ERR_UNSUPPORTED_DTYPE;
-    if (T < 0 || E < 0 || O < 0 || K < 0 || I <= 0 || I % 32 != 0)
-      return MXFP4EL_ERR_INVALID_ARGUMENT;
-    return MXFP4EL_ERR_TOO_LARGE;
-  }
-  if (need > mxfp4el::kStaticScratchBytes) return MXFP4EL_ERR_TOO_LARGE;
+  if (need == (size_t)-1 || need > mxfp4el::kStaticScratchBytes) return MXFP4EL_ERR_TOO_LARGE;
   void* scratch = nullptr;
   if (need > 0) {
-    const int rc = mxfp4el::scratch_address(&scratch);
-    if (rc != MXFP4EL_OK) return rc;
+    const int arc = mxfp4el::scratch_address(&scratch);
+    if (arc != MXFP4EL_OK) return arc;
   }
   return mxfp4_expert_linear_with_workspace(
       latent_tokens, packed_weights, scale_bytes, selected_experts,

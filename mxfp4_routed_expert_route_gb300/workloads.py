@@ -11,8 +11,12 @@ uint8, scale bytes (E, O, G) uint8, selected experts (T, K), mixture weights
 
 Recipe (the same for every named workload):
   * numpy ``default_rng(seed)``; bytes are drawn on the host, then uploaded.
-  * packed bytes uniform over 0..255 (``rng.bytes``);
-  * scale bytes uniform over the stated inclusive range;
+  * packed bytes uniform over 0..255 and scale bytes uniform over the stated
+    inclusive range, each array drawn in 64 MiB chunks: chunk c of stream s
+    comes from ``default_rng((seed, s, c)).integers(lo, hi + 1, uint8)``
+    (s = 1 packed bytes, 2 scale bytes; for the SwiGLU expert 1 and 2 are the
+    gate/up matrix, 3 and 4 the down matrix), so the bytes do not depend on
+    how many threads draw them;
   * x and y_shared ~ N(0, 1), rounded to nearest-even bf16 where the
     workload is bf16;
   * mixture weights = softmax of N(0, 1) logits over the K picks, stored fp32;
@@ -23,6 +27,8 @@ Recipe (the same for every named workload):
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -106,8 +112,27 @@ def softmax_weights(rng, T: int, K: int) -> np.ndarray:
     return (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
 
 
-def random_bytes(rng, n: int) -> np.ndarray:
-    return np.frombuffer(rng.bytes(n), dtype=np.uint8).copy()
+CHUNK = 64 << 20
+
+
+def uniform_bytes(seed: int, stream: int, n: int, lo: int = 0, hi: int = 255) -> np.ndarray:
+    """n bytes uniform over [lo, hi]: chunk c of CHUNK bytes is drawn by
+    default_rng((seed, stream, c)), the chunks in parallel threads."""
+    out = np.empty(n, dtype=np.uint8)
+
+    def fill(c):
+        a, b = c * CHUNK, min(n, (c + 1) * CHUNK)
+        out[a:b] = np.random.default_rng((seed, stream, c)).integers(
+            lo, hi + 1, size=b - a, dtype=np.uint8)
+
+    nchunks = (n + CHUNK - 1) // CHUNK
+    if nchunks <= 1:
+        for c in range(nchunks):
+            fill(c)
+    else:
+        with ThreadPoolExecutor(max_workers=min(nchunks, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(nchunks)))
+    return out
 
 
 def make(T: int, E: int, K: int, I: int, O: int, dtype=torch.bfloat16,
@@ -119,9 +144,8 @@ def make(T: int, E: int, K: int, I: int, O: int, dtype=torch.bfloat16,
         raise ValueError("I must be a multiple of 32")
     G = I // 32
     rng = np.random.default_rng(seed)
-    packed = random_bytes(rng, E * O * G * 16).reshape(E, O, G, 16)
-    scales = rng.integers(scale_lo, scale_hi + 1, size=(E, O, G),
-                          dtype=np.int64).astype(np.uint8)
+    packed = uniform_bytes(seed, 1, E * O * G * 16).reshape(E, O, G, 16)
+    scales = uniform_bytes(seed, 2, E * O * G, scale_lo, scale_hi).reshape(E, O, G)
     x = _normal(rng, (T, I), dtype)
     y_shared = _normal(rng, (T, O), dtype)
     if sel is None:
@@ -208,10 +232,11 @@ def make_swiglu(T: int, E: int, K: int, I: int, F: int, O: int, dtype=torch.bflo
     if I % 32 or F % 32:
         raise ValueError("I and F must be multiples of 32")
     rng = np.random.default_rng(seed)
-    gu = random_bytes(rng, E * 2 * F * (I // 32) * 16).reshape(E, 2 * F, I // 32, 16)
-    gus = rng.integers(scale_lo, scale_hi + 1, size=(E, 2 * F, I // 32)).astype(np.uint8)
-    dn = random_bytes(rng, E * O * (F // 32) * 16).reshape(E, O, F // 32, 16)
-    dns = rng.integers(scale_lo, scale_hi + 1, size=(E, O, F // 32)).astype(np.uint8)
+    gu = uniform_bytes(seed, 1, E * 2 * F * (I // 32) * 16).reshape(E, 2 * F, I // 32, 16)
+    gus = uniform_bytes(seed, 2, E * 2 * F * (I // 32), scale_lo, scale_hi).reshape(
+        E, 2 * F, I // 32)
+    dn = uniform_bytes(seed, 3, E * O * (F // 32) * 16).reshape(E, O, F // 32, 16)
+    dns = uniform_bytes(seed, 4, E * O * (F // 32), scale_lo, scale_hi).reshape(E, O, F // 32)
     x = _normal(rng, (T, I), dtype)
     y_shared = _normal(rng, (T, O), dtype)
     if picks == "uniform":

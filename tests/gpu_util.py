@@ -52,6 +52,30 @@ def digest(*tensors) -> str:
     return h.hexdigest()
 
 
+def parity_rows(wl: workloads.Workload, n_random: int = 256, seed: int = 0) -> np.ndarray:
+    """Token rows for an element-by-element check of a full-size batch whose
+    every row the oracle cannot afford: every token of the least-loaded
+    expert, the first 192 tokens of the most-loaded expert (which cover its
+    first token block of the tensor-core kernel, at most 192 tokens) and its
+    last 64 (its last block), the first and last token, and n_random more
+    drawn at random."""
+    rng = np.random.default_rng(seed)
+    sel = wl.sel.numpy()
+    counts = np.bincount(sel[(sel >= 0) & (sel < wl.E)].reshape(-1), minlength=wl.E)
+    hot = int(counts.argmax())
+    used = np.nonzero(counts)[0]
+    cold = int(used[counts[used].argmin()])
+    hot_tokens = np.nonzero((sel == hot).any(1))[0]
+    pick = {0, wl.T - 1}
+    pick.update(np.nonzero((sel == cold).any(1))[0].tolist())
+    pick.update(hot_tokens[:192].tolist())
+    pick.update(hot_tokens[-64:].tolist())
+    target = len(pick) + min(n_random, wl.T - len(pick))
+    while len(pick) < target:
+        pick.add(int(rng.integers(0, wl.T)))
+    return np.array(sorted(pick), dtype=np.int64)
+
+
 def sample_rows(wl: workloads.Workload, n: int, seed: int = 0) -> np.ndarray:
     """Tokens for a sampled full-size check: the first and last token, tokens of
     the most and least loaded experts, and random ones."""

@@ -200,3 +200,39 @@ def test_swiglu_scratch_follows_the_gate_up_tiles(lib, monkeypatch):
     # fp32 tokens and decode batches never take the tensor cores: the knob
     # changes nothing there.
     assert ws(T, E, I, F, O, K, 0) == fp32 and ws(8, E, I, F, O, K, 1) == decode
+
+
+def test_static_scratch_checks_like_the_other_entry_points(lib):
+    # The allocation-free entry point runs the same argument checks, in the
+    # same order, before its own size limit: a call with another error gets
+    # that error's code even when it is also too large for the fixed array.
+    # Every case returns before any GPU work.
+    from mxfp4_routed_expert_route_gb300 import _native as n
+    static, main = lib.mxfp4_expert_linear_static_scratch, lib.mxfp4_expert_linear
+    assert lib.mxfp4_expert_linear_static_scratch_bytes() == 8 << 20
+    P = ctypes.c_void_p
+    x, w, s, sel, p, ys = P(1 << 24), P(1 << 28), P(1 << 29), P(1 << 30), P(1 << 31), P(1 << 32)
+    out = P(1 << 40)
+    # 64 tokens x 8 slots x 8192 rows of float32 partial results: 16 MiB of
+    # scratch, over the 8 MiB array.
+    big = (64, 16, 256, 8192, 8)
+    cases = [
+        ((x, w, s, sel, p, ys, out) + big + (n.DTYPE_BF16, 7), n.ERR_UNSUPPORTED_DTYPE),
+        ((x, w, s, sel, p, ys, out) + big + (5, n.INDEX_I32), n.ERR_UNSUPPORTED_DTYPE),
+        ((x, w, s, sel, p, ys, ys) + big + (n.DTYPE_BF16, n.INDEX_I32), n.ERR_ALIAS),
+        ((P((1 << 24) + 8), w, s, sel, p, ys, out) + big + (n.DTYPE_BF16, n.INDEX_I32),
+         n.ERR_INVALID_ARGUMENT),
+        ((None, w, s, sel, p, ys, out) + big + (n.DTYPE_BF16, n.INDEX_I32),
+         n.ERR_INVALID_ARGUMENT),
+        ((x, w, s, sel, p, ys, out, 64, 16, 250, 8192, 8, n.DTYPE_BF16, n.INDEX_I32),
+         n.ERR_INVALID_ARGUMENT),
+        ((x, w, s, sel, p, ys, out, 0) + big[1:] + (n.DTYPE_BF16, n.INDEX_I32), n.OK),
+        ((x, w, s, sel, p, ys, out, 1 << 40) + big[1:] + (n.DTYPE_BF16, n.INDEX_I32),
+         n.ERR_TOO_LARGE),
+    ]
+    for args, code in cases:
+        assert main(*args, None) == code, args
+        assert static(*args, None) == code, args
+    # Valid for the other entry points, too large only for the fixed array.
+    assert static(x, w, s, sel, p, ys, out, *big, n.DTYPE_BF16, n.INDEX_I32,
+                  None) == n.ERR_TOO_LARGE

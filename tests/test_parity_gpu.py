@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (TOL, assert_parity, digest, oracle_rows, run_gpu,
+from gpu_util import (TOL, assert_parity, digest, oracle_rows, parity_rows, run_gpu,
                       sample_rows)
 from mxfp4_routed_expert_route_gb300 import (_native, device_errors, wait_timeouts,
                                              mxfp4_expert_linear, workloads)
@@ -43,9 +43,13 @@ def test_named_workload_sampled(name):
     wl = workloads.named(name)
     out = run_gpu(wl)
     assert torch.isfinite(out.float()).all()
-    rows = sample_rows(wl, 12)
+    # At least 256 token rows element by element, including every token of
+    # the least-loaded expert and whole token blocks of the most-loaded one.
+    rows = parity_rows(wl)
+    assert len(rows) >= 256
     want, absm, _ = oracle_rows(wl, rows=rows)
-    assert_parity(out[torch.from_numpy(rows).cuda()], want, absm, wl.dtype, name)
+    assert_parity(out[torch.from_numpy(rows).cuda()], want, absm, wl.dtype,
+                  f"{name} ({len(rows)} rows)")
     # Token permutation permutes the output rows, bit for bit, at full size.
     perm = torch.from_numpy(np.random.default_rng(1).permutation(wl.T))
     d = wl.device_tensors("cuda")

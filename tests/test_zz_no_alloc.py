@@ -1,15 +1,27 @@
 """The allocation-free entry point, mxfp4_expert_linear_static_scratch.
 
-It serves callers that cannot allocate device memory: its scratch is a fixed
-array compiled into the library. This file is collected last on purpose.
+It is for callers that cannot allocate device memory while they run (a
+serving process whose memory budget is fixed at start-up, a plugin inside a
+host framework that owns every device allocation): its scratch is a fixed
+array compiled into the library. The tests check that, on each kernel path
+the library picks (the GEMV routing for itself, the GEMV after the separate
+bucketer, the tensor-core GEMM), the call gives exactly the bits of the
+caller-workspace entry point and matches the float64 oracle within the
+tolerance of the other parity tests; that two calls in a row (the array
+keeping the previous call's contents) stay correct; and that the calls leave
+the device's free memory unchanged.
+
+This file is collected last on purpose, so that a run stopping at its first
+failure has run every other test.
 """
 import ctypes
 
 import pytest
 import torch
 
-from gpu_util import TOL, oracle_rows, worst_ratio
-from mxfp4_routed_expert_route_gb300 import _native, mxfp4_expert_linear, workloads
+from gpu_util import assert_parity, oracle_rows
+from mxfp4_routed_expert_route_gb300 import (_native, mxfp4_expert_linear, workloads,
+                                             workspace_size)
 
 
 @pytest.fixture(scope="module")
@@ -32,34 +44,68 @@ def _call_static(lib, d, wl, out):
         dtype, _native.INDEX_I32, stream)
 
 
-@pytest.mark.gpu
-def test_static_scratch_matches_workspace_entry_point_twice(lib):
-    # Two different calls in a row: the second must not see the first's scratch.
-    cases = [workloads.make(8, 32, 4, 512, 640, dtype=torch.bfloat16, seed=71,
-                            name="first"),
-             workloads.make(13, 20, 3, 256, 300, dtype=torch.float32, seed=72,
-                            name="second")]
-    for wl in cases:
-        d = wl.device_tensors("cuda")
-        ref = mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"],
-                                  d["y_shared"])
-        out = torch.full_like(ref, float("nan"))
-        assert _call_static(lib, d, wl, out) == _native.OK
-        torch.cuda.synchronize()
-        _, abs_terms, _ = oracle_rows(wl)
-        assert worst_ratio(out, ref.cpu().double().numpy(), abs_terms) <= TOL[wl.dtype], wl.name
+# (workload, environment): the three kernel paths, each within the 8 MiB array.
+CASES = [
+    # 32 pairs: the GEMV routes for itself (bf16 tokens scaled on load).
+    (dict(T=8, E=32, K=4, I=512, O=640, dtype=torch.bfloat16, seed=71), {}),
+    # fp32 tokens, ragged sizes.
+    (dict(T=13, E=20, K=3, I=256, O=300, dtype=torch.float32, seed=72), {}),
+    # The separate bucketer launch before the GEMV, with its own scratch.
+    (dict(T=40, E=24, K=4, I=320, O=200, dtype=torch.bfloat16, seed=73),
+     {"MXFP4EL_ROUTE": "bucketer"}),
+    # The tensor-core GEMM: 256 pairs over 4 experts (64 tokens per expert),
+    # grouped tokens and partial results in the array.
+    (dict(T=128, E=4, K=2, I=256, O=192, dtype=torch.bfloat16, seed=74),
+     {"MXFP4EL_PATH": "gemm"}),
+]
 
 
 @pytest.mark.gpu
-def test_static_scratch_rejects_oversized_calls(lib):
+def test_static_scratch_matches_workspace_entry_point_twice(lib, monkeypatch):
     limit = lib.mxfp4_expert_linear_static_scratch_bytes()
-    assert limit == 8 << 20
-    # 64 tokens x 8 slots x 8192 rows of float32 partials is 16 MiB: refused
-    # before any GPU work (the pointers are never touched).
-    fake = ctypes.c_void_p(1 << 24)
-    out = ctypes.c_void_p(1 << 40)
-    rc = lib.mxfp4_expert_linear_static_scratch(fake, fake, fake, fake, fake, fake,
-                                                out, 64, 16, 256, 8192, 8,
-                                                _native.DTYPE_BF16, _native.INDEX_I32,
-                                                None)
-    assert rc == _native.ERR_TOO_LARGE
+    runs = []
+    for cfg, env in CASES:
+        wl = workloads.make(name=f"static_{cfg['seed']}", **cfg)
+        need = workspace_size(wl.T, wl.E, wl.I, wl.O, wl.K, wl.dtype)
+        assert 0 < need <= limit, (cfg, need)
+        d = wl.device_tensors("cuda")
+        for k in ("MXFP4EL_ROUTE", "MXFP4EL_PATH"):
+            monkeypatch.delenv(k, raising=False)
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        # The reference: the caller-workspace entry point on a torch buffer.
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        ref = mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"],
+                                  d["y_shared"], workspace=ws)
+        outs = [torch.full_like(ref, float("nan")) for _ in range(2)]
+        runs.append((wl, env, d, ref, outs))
+    torch.cuda.synchronize()
+
+    # First call on this device: it looks up the array's address (and may load
+    # the library's device code); not part of the measured calls below.
+    wl0, env0, d0, _, outs0 = runs[0]
+    for k, v in env0.items():
+        monkeypatch.setenv(k, v)
+    assert _call_static(lib, d0, wl0, outs0[0]) == _native.OK
+    torch.cuda.synchronize()
+
+    free_before = torch.cuda.mem_get_info()[0]
+    # Every case twice in a row; the array keeps whatever the previous call
+    # (another case, or the same one) left in it.
+    for rep in range(2):
+        for wl, env, d, ref, outs in runs:
+            for k in ("MXFP4EL_ROUTE", "MXFP4EL_PATH"):
+                monkeypatch.delenv(k, raising=False)
+            for k, v in env.items():
+                monkeypatch.setenv(k, v)
+            assert _call_static(lib, d, wl, outs[rep]) == _native.OK, (wl.name, rep)
+    torch.cuda.synchronize()
+    free_after = torch.cuda.mem_get_info()[0]
+    assert free_after == free_before, "the allocation-free calls changed free device memory"
+
+    for wl, env, d, ref, outs in runs:
+        want, abs_terms, bad = oracle_rows(wl)
+        assert bad == 0
+        for rep in range(2):
+            assert torch.equal(outs[rep], ref), (wl.name, env, rep)
+            assert_parity(outs[rep], want, abs_terms, wl.dtype, f"static {wl.name} call {rep}")
