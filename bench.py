@@ -403,10 +403,29 @@ def measure_swiglu(name, dev, stream, flush, warmup, n, peaks):
             "frac": t_roof / (us * 1e-6)}
 
 
+def f16_tile_share(wl, rows_per_tile=128, max_span=26):
+    """Share of the tensor-core kernel's 128-row weight tiles that run on f16
+    operands: those whose every row's scale bytes span at most 26 binades
+    (the others run on bf16)."""
+    import numpy as np
+
+    sc = wl.scales.numpy()
+    span = sc.max(axis=-1).astype(np.int16) - sc.min(axis=-1).astype(np.int16)   # (E, O)
+    E, O = span.shape
+    tiles = -(-O // rows_per_tile)
+    pad = np.zeros((E, tiles * rows_per_tile), dtype=np.int16)
+    pad[:, :O] = span
+    ok = (pad.reshape(E, tiles, rows_per_tile) <= max_span).all(axis=-1)
+    return float(ok.mean())
+
+
 def linear_dtype_label(wl, gemm):
     """What the routed linear computes in, for the line's ``dtype``."""
     if gemm:
-        return "bf16 x bf16 -> f32 (tensor cores; exact MXFP4 decode to bf16)"
+        share = f16_tile_share(wl)
+        return (f"f16 x f16 -> f32 on {100 * share:.0f}% of weight tiles, bf16 x bf16 -> f32 on "
+                "the rest (tensor cores; MXFP4 decoded exactly, with powers of two per weight "
+                "row and per token)")
     if token_bytes(wl) == 2:
         return "f16x2 products summed in chains of 8, f32 across groups (bf16 tokens)"
     return "f32"

@@ -144,15 +144,25 @@ cudaError_t run_linear(const void* x, const uint8_t* packed, const uint8_t* scal
   if (err != cudaSuccess) return err;
   if (gemm) {
     mark(MXFP4EL_STAGE_GATHER, true, stream);
-    err = launch_gather_tokens(x, ws.plan, ws.grouped, T, I, K, swiglu.sel2, stream);
+    err = launch_tile_scan(scales, E, I, O, swiglu.F, ws.tile_mode, ws.row_off, stream);
+    if (err == cudaSuccess)
+      err = launch_group_tokens(x, ws.plan, ws.grouped, ws.gsigma, T, I, K, swiglu.sel2, stream);
     mark(MXFP4EL_STAGE_GATHER, false, stream);
     if (err != cudaSuccess) return err;
   }
   mark(MXFP4EL_STAGE_LINEAR, true, stream);
-  if (gemm)
-    err = launch_gemm_tc(x, packed, scales, ws.plan, ws.grouped, ws.part, status, T, E, I, O, K,
-                         swiglu, stream);
-  else
+  if (gemm) {
+    TcTokens tok;
+    tok.rows = ws.grouped;
+    tok.sigma = ws.gsigma;
+    tok.f16 = true;
+    tok.nrows = T * K;
+    TcTileModes modes;
+    modes.tile_mode = ws.tile_mode;
+    modes.row_off = ws.row_off;
+    err = launch_gemm_tc(tok, modes, packed, scales, ws.plan, ws.part, status, E, I, O, K, swiglu,
+                         stream);
+  } else
     err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, sel, index_dtype, packed, scales,
                       ws.plan, ws.part, status, T, E, I, O, K, stream);
   mark(MXFP4EL_STAGE_LINEAR, false, stream);
@@ -248,7 +258,7 @@ void carve_swiglu(void* base, int64_t T, int64_t E, int64_t I, int64_t F, int64_
   auto at = [&](size_t off) { return base ? static_cast<char*>(base) + off : nullptr; };
   // Gate/up tiles write h directly: no partial results for that projection.
   const bool tiles = K > 0 && E > 0 && swiglu_tiles_used(T, E, I, F, K, token_dtype);
-  carve_workspace(base, T, E, I, 2 * F, K, token_dtype, &sw->gate_up, !tiles);
+  carve_workspace(base, T, E, I, 2 * F, K, token_dtype, &sw->gate_up, !tiles, tiles ? F : 0);
   size_t off = align_up(sw->gate_up.bytes);
   carve_workspace(at(off), P, E, F, O, 1, token_dtype, &sw->down);
   off = align_up(off + sw->down.bytes);
@@ -297,9 +307,15 @@ int run_swiglu(const void* x, const uint8_t* gu_packed, const uint8_t* gu_scales
         unsigned long long* status = device_status_words();
         if (status == nullptr) return MXFP4EL_ERR_CUDA;
         mark(MXFP4EL_STAGE_LINEAR, true, stream);
+        // The down projection's token rows are h's rows, already in the
+        // lists' order (bf16 operands: h has no f16 copy).
+        TcTokens tok;
+        tok.rows = sw.h;
+        tok.nrows = P;
         const cudaError_t err =
-            launch_gemm_tc(sw.h, dn_packed, dn_scales, sw.gate_up.plan, sw.h, sw.down.part,
-                           status, P, E, F, O, 1, SwigluTiles{}, stream, kMetaUnitCounter2);
+            launch_gemm_tc(tok, TcTileModes{}, dn_packed, dn_scales, sw.gate_up.plan,
+                           sw.down.part, status, E, F, O, 1, SwigluTiles{}, stream,
+                           kMetaUnitCounter2);
         mark(MXFP4EL_STAGE_LINEAR, false, stream);
         if (err != cudaSuccess) return MXFP4EL_ERR_CUDA;
       } else if (run_linear(sw.h, dn_packed, dn_scales, sw.sel2, P, E, F, O, 1, token_dtype,
@@ -360,7 +376,8 @@ int cached_workspace(size_t bytes, cudaStream_t s, void** base) {
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
-                     int64_t K, int token_dtype, Workspace* ws, bool with_part) {
+                     int64_t K, int token_dtype, Workspace* ws, bool with_part,
+                     int64_t tiles_F) {
   const int64_t P = T * K;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -381,7 +398,12 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
   ws->wc_global = wc_words ? reinterpret_cast<int*>(take(wc_words * sizeof(int))) : nullptr;
   ws->x16 = prep ? reinterpret_cast<__half*>(take((size_t)T * I * sizeof(__half))) : nullptr;
   ws->sigma = prep ? reinterpret_cast<int*>(take((size_t)T * sizeof(int))) : nullptr;
-  ws->grouped = gemm ? take(gemm_tc_grouped_bytes(T, K, I)) : nullptr;
+  ws->grouped = gemm ? reinterpret_cast<__half*>(take(gemm_tc_grouped_bytes(T, K, I))) : nullptr;
+  ws->gsigma = gemm ? reinterpret_cast<int*>(take((size_t)P * sizeof(int))) : nullptr;
+  ws->tile_mode = gemm ? reinterpret_cast<uint8_t*>(
+                             take((size_t)E * (size_t)gemm_tc_row_tiles(O, tiles_F)))
+                       : nullptr;
+  ws->row_off = gemm ? reinterpret_cast<int16_t*>(take((size_t)E * O * sizeof(int16_t))) : nullptr;
   ws->plan.unit_begin =
       K > 0 && !gemm ? reinterpret_cast<int*>(take((kMaxSplitCtas + 1) * sizeof(int))) : nullptr;
   const size_t ncol = (size_t)linear_partial_columns(T, E, I, O, K, token_dtype);

@@ -248,6 +248,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// mbar_wait by a whole warp: every lane waits, then the lanes vote, so the
+// result is the same in every lane and the warp is converged on return (as
+// the .sync.aligned tcgen05 instructions that often follow require: lanes
+// leave a spin loop at different times and need not reconverge by
+// themselves before the next instruction).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
+}
+
 // As mbar_wait, but each test may suspend the thread in hardware until the
 // phase completes (or about 20 us pass) instead of spinning on issue slots
 // that other warps of the SM need.
@@ -289,6 +298,17 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+
+// Orders this thread's earlier shared-memory accesses through the generic
+// proxy (ordinary loads and stores) before later accesses through the async
+// proxy (TMA and bulk copies, tensor-core operand reads). A consumer that read
+// a staging buffer with ordinary loads calls it before it releases the buffer
+// to a producer that refills it by copy: the release alone does not order the
+// two proxies, and a refill can then overwrite bytes that a load still in
+// flight reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // L2 policy for data read exactly once (the packed weights and scales).
@@ -394,13 +414,17 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 
 // ---------------------------------------------------------- token prep -----
-// Prepared tokens for the staged GEMV with bf16 tokens: per token t a power
-// of two 2^sigma_t and x16[t, i] = f16(x[t, i] 2^sigma_t).
-// One warp per token: sigma_t from max|x_t|, then x16[t] = f16(x_t 2^sigma_t)
-// with max|x_t| 2^sigma_t in [2^8, 2^9).
+// Prepared bf16 tokens: per token t a power of two 2^sigma_t and
+// x16[t, i] = f16(x[t, i] 2^sigma_t). One warp per token: sigma_t from
+// max|x_t|, then x16[t] = f16(x_t 2^sigma_t) with max|x_t| 2^sigma_t in
+// [2^top, 2^(top+1)): top = 8 for the GEMV, whose f16 partial sums of 8
+// products must not overflow, and 14 for the tensor cores, which only need
+// the operands themselves in range. A bf16 value keeps its 8 significant
+// bits in f16 wherever the scaled value is a normal f16 number.
 __device__ __forceinline__ void prep_token(const __nv_bfloat16* __restrict__ x,
                                            __half* __restrict__ x16,
-                                           int* __restrict__ sigma, int t, int I, int lane) {
+                                           int* __restrict__ sigma, int t, int I, int lane,
+                                           int top = 8) {
   const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * I);
   const int nvec = I / 8;
   uint32_t m = 0;                                // max |x| as float32 bits
@@ -417,7 +441,7 @@ __device__ __forceinline__ void prep_token(const __nv_bfloat16* __restrict__ x,
   for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(kFullMask, m, o));
   const int ex = (int)(m >> 23);                 // biased exponent of max|x|
   int s = 0;
-  if (m != 0 && ex < 255) s = min(126, 135 - ex);   // max|x| 2^s in [2^8, 2^9)
+  if (m != 0 && ex < 255) s = min(126, 127 + top - ex);   // max|x| 2^s in [2^top, 2^(top+1))
   const float up = __uint_as_float((uint32_t)(s + 127) << 23);
   uint4* out = reinterpret_cast<uint4*>(x16 + (size_t)t * I);
   for (int i = lane; i < nvec; i += 32) {

@@ -1,46 +1,54 @@
 // gemm_tc.cu -- prefill-regime routed expert grouped GEMM on the 5th-gen
 // tensor cores (tcgen05, TMEM, TMA).
 //
-// For every selected expert e and each block of up to 192 of its tokens it
-// computes part[t*K+k, o] = sum_i W_e[o, i] x[t, i] for all output rows o,
-// with W_e decoded from MXFP4 as in the problem statement ("MXFP4 Routed
-// Expert Linear", Kimi K3): W_e[o, 32g+2j (+1)] = LUT[low (high) nibble of
+// For every selected expert e and each block of its tokens it computes
+// part[t*K+k, o] = sum_i W_e[o, i] x[t, i] for all output rows o, with W_e
+// decoded from MXFP4 as in the problem statement ("MXFP4 Routed Expert
+// Linear", Kimi K3): W_e[o, 32g+2j (+1)] = LUT[low (high) nibble of
 // packed[e,o,g,j]] * 2^(scales[e,o,g] - 127).
 //
 // Shape ("swap AB"): M = 128 weight rows per tile, N = the tokens of one
 // block (16..192, a multiple of 16), K = I in chunks of 64 (two groups).
-//   * A (weights) is decoded exactly to bf16 -- every E2M1 value times a
-//     power of two is a bf16 number while it stays in bf16's range -- and
-//     written straight into tensor memory: row m in TMEM lane m, two K
-//     elements per 32-bit column.
-//   * B (tokens) is a copy of x with the rows grouped by expert (written by
-//     gather_tokens_kernel); TMA loads 64-wide K chunks with the 128-byte
-//     swizzle that the K-major shared-memory descriptor describes.
-//   * tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), accumulator in TMEM.
+//   * A (weights) is decoded exactly and written straight into tensor
+//     memory: row m in TMEM lane m, two K elements per 32-bit column.
+//   * B (tokens) is a copy of the token rows grouped by expert, written by
+//     group_tokens_kernel in f16 scaled per row by a power of two; TMA loads
+//     each 64-wide K chunk with the 128-byte swizzle that the K-major
+//     shared-memory descriptor describes.
+//   * tcgen05.mma kind::f16, fp32 accumulator in TMEM.
+//
+// Two exact operand modes, chosen per tile:
+//   * f16: tokens pre-scaled per token by 2^sigma_t (max |x_t| 2^sigma_t in
+//     [2^14, 2^15)), weights decoded by the hardware E2M1 -> f16x2
+//     conversion and one f16x2 multiply by 2^(s - 127 - r_m), where r_m is a
+//     per-row offset chosen so that every scaled weight of the row is a normal
+//     f16 number; the epilogue multiplies by 2^(r_m - sigma_t). Possible when
+//     every row's scale bytes span at most 26 binades. The mode of each tile
+//     and the row offsets come from tile_scan_kernel, run before this kernel.
+//   * bf16: weights decoded to their exact bf16 bit patterns (byte-permute
+//     tables), any scale byte; the dequantizers convert the chunk's f16 token
+//     rows to bf16 in shared memory (exact: they came from bf16 values) and
+//     the epilogue multiplies by 2^-sigma_t.
+// Products are exact in both modes and accumulate in fp32, so the modes give
+// the same result up to the accumulation order inside the MMA.
 //
 // Warp roles in a CTA of 24 warps (one CTA per SM, persistent over units
 // (expert, token block, 128-row tile), which CTAs take from a global counter
-// as they go, so the cost differences between units even out):
-//   warp 0      producer of scales and packed weights (lane 0; a deep ring
-//               of 4 KB stages covers HBM latency) and TMEM allocation; it
-//               takes each next unit from the counter and hands its index to
-//               the other roles through a small shared-memory ring
+// as they go):
+//   warp 0      producer of scales and packed weights (lane 0) and TMEM
+//               allocation; takes each next unit from the counter and hands
+//               its index to the other roles through a shared-memory ring
 //   warp 1      MMA issuer (the whole warp waits, one elected lane issues)
-//   warp 2      per-expert lists in shared memory at start
+//   warp 2      per-expert lists at start
 //   warp 3      producer of token tiles (lane 0)
-//   warps 4-19  dequantize, in four teams of 4 warps: team t owns A buffer t
-//               and takes chunks t, t+4, t+8, ..., so the teams' decode,
-//               waits and stores interleave; in a team thread m (one weight
-//               row) decodes both groups of the chunk into 32 TMEM columns
-//   warps 20-23 epilogue: TMEM -> registers -> shared memory (transposed) ->
-//               float32 partial results, four consecutive rows per store
-// Four A buffers and two accumulators in TMEM, and a ring of four to six
-// token stages in shared memory (a stage is refilled only after its chunk's
-// MMAs finish, so its TMA latency needs several chunks of cover), let the
-// loads, dequantize, MMA and epilogue of consecutive chunks and units
-// overlap. Every wait is bounded;
-// a role whose wait gives up records it, stops, and the CTA still waits
-// (bounded) for its own copies and MMAs before freeing TMEM.
+//   warps 4-19  dequantize, in four teams of 4 warps: team t owns TMEM A
+//               buffer t and takes chunks t, t+4, ...; thread m decodes both
+//               groups of the chunk for weight row m
+//   warps 20-23 epilogue: TMEM -> registers (mode scaling) -> shared memory
+//               (transposed) -> float32 partial results
+// Every wait is bounded; a role whose wait gives up records it, stops, and
+// the CTA still waits (bounded) for its own copies and MMAs before freeing
+// TMEM.
 //
 // Gate/up tiles (gemm_tc_kernel<SB, true>, the SwiGLU expert's stacked
 // gate/up projection, 2F rows with the gate rows first): a tile's 128 rows
@@ -48,10 +56,13 @@
 // boxes into one stage, two scale spans), so the epilogue holds g and u of
 // the same (pair, f) and writes h = silu(g) * u in bf16 instead of partial
 // results, by pair or in the lists' grouped order; the down projection can
-// then run as a second instance on the same lists (its own unit counter).
+// then run as a second instance on the same lists (its own unit counter),
+// its token rows being the grouped rows of h.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -62,30 +73,32 @@ namespace {
 
 constexpr int kTcThreads = 768;
 constexpr int kBM = 128;                    // weight rows per tile
-constexpr int kBK = 64;                     // K elements per stage
-constexpr int kNMax = 192;                  // tokens per block
-constexpr int kStagesAMax = 16;            // packed-weight ring (from HBM)
-constexpr int kRing = 4;                   // TMEM A buffers (one per dequantizer team)
-constexpr int kStagesBMax = 6;             // token stages, as shared memory allows
-constexpr uint32_t kStageB = kNMax * 128;   // token tile, 128 B per row
-constexpr uint32_t kStageA = kBM * 32;      // packed bytes, 32 B per row
-static_assert(kStageB % 1024 == 0 && kStageA % 1024 == 0, "stages keep 1024-byte alignment");
+constexpr int kBK = 64;                     // K elements per chunk (two groups)
+constexpr int kNMax = 192;                  // token columns per block (TMEM accumulator width)
+constexpr int kABufs = 4;                   // TMEM A buffers (one per dequantizer team)
+constexpr int kStagesAMax = 16;             // packed-weight ring (from HBM)
+constexpr int kStagesBMax = 6;              // token stages, as shared memory allows
+constexpr uint32_t kStageA = kBM * 32;      // packed bytes of a chunk, 32 B per row
+static_assert(kStageA % 1024 == 0, "stages keep 1024-byte alignment");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 0;               // two accumulators of kNMax columns
-constexpr uint32_t kACol = 2 * kNMax;       // kRing A buffers of 32 columns
-static_assert(kACol + kRing * 32 <= kTmemCols, "TMEM budget");
+constexpr uint32_t kACol = 2 * kNMax;       // kABufs A buffers of 32 columns
+static_assert(kACol + kABufs * 32 <= kTmemCols, "TMEM budget");
 constexpr int kMaxExpertsTc = 512;          // per-expert lists kept in shared memory
 constexpr uint32_t kEpiStage = 16 * 32 * 4; // epilogue staging per warp: 16 columns x 32 rows
 constexpr int kUnitRing = 4;                // unit indices handed from producer A
+constexpr int kListWarp = 2, kProdBWarp = 3;
+constexpr int kNumLoads = kNMax / 16;       // token-box heights: 16, 32, ..., 192 rows
+__host__ __device__ constexpr int load_rows(int l) { return 16 * (l + 1); }
 constexpr int kDequantWarp0 = 4, kDequantWarps = 16, kTeamWarps = 4, kEpiWarp0 = 20;
-// Readers of the unit ring, one arrival each: producer B, the MMA warp, the
-// dequantizer warps and the epilogue warps.
+// Readers of the unit ring, one arrival each: producer B (one thread), the
+// MMA warp, the dequantizer warps and the epilogue warps.
 constexpr int kUnitReaders = 2 + kDequantWarps + (kTcThreads / 32 - kEpiWarp0);
-static_assert(kDequantWarps == kRing * kTeamWarps, "one team per A buffer");
-constexpr int kNumLoads = 5;                // token-box heights
-__host__ __device__ constexpr int load_rows(int l) {
-  return l == 0 ? 16 : l == 1 ? 32 : l == 2 ? 64 : l == 3 ? 128 : 192;
-}
+static_assert(kDequantWarps == kABufs * kTeamWarps, "one team per A buffer");
+// The widest span of scale bytes within one row that f16 operands hold
+// exactly: LUT values 0.5..6 times 2^d are normal f16 numbers for
+// -13 <= d <= 13.
+constexpr int kF16Span = 26;
 
 struct TcArgs {
   RoutePlan plan;
@@ -93,33 +106,43 @@ struct TcArgs {
   const uint8_t* scales_end;
   float* part;                   // [T*K, O]
   unsigned long long* status;
+  const int* sigma;              // per grouped row: the power of two of its f16 copy
   int G, O, K;
-  int mtiles;                    // ceil(O / 128)
+  int mtiles;                    // ceil(O / 128) (or ceil(F / 64) for gate/up tiles)
   int stages_a;
+  int nmax;                      // token columns per block (<= kNMax)
+  uint32_t stage_b;              // bytes per token stage: nmax rows x 128 B
   uint32_t scale_cap;            // bytes per scale buffer
+  int b_f16;                      // the grouped rows are f16 copies scaled by 2^sigma
+                                 // (else plain bf16 rows: every tile takes the bf16 mode)
+  int f16_tiles;                  // tiles may take the f16 mode (b_f16, unless a test
+                                 // keeps every tile in bf16)
+  const uint8_t* tile_mode;      // [E][mtiles]: 1 = the tile's rows fit f16 operands
+  const int16_t* row_off;        // [E*O]: row offset r of every weight row (f16 mode)
   // Gate/up tiles of the SwiGLU expert (F > 0; the matrix has 2F rows, gate
   // rows first): tile rows 0..63 are gate rows f0.., rows 64..127 the
   // matching up rows F + f0..; the epilogue writes h = silu(gate) * up in
   // bf16 and the pairs' expert ids instead of the partial results.
   int F;
   __nv_bfloat16* h;              // (P, F), row = pair (or position in the lists: h_grouped)
-  int32_t* sel2;                 // (P): expert of each pair (zeroed by the gather), or null
+  int32_t* sel2;                 // (P): expert of each pair (zeroed by the token prep), or null
   int h_grouped;
   int counter_word;              // plan.meta word this kernel takes its units from
 };
 
 struct TcMaps {
-  CUtensorMap a;                 // packed weights as uint8 [E*O, G*16], box {32, 128}
-  CUtensorMap b[kNumLoads];      // grouped tokens bf16 [P, I], box {64, rows}, 128B swizzle
+  CUtensorMap a;                 // packed weights as uint8 [E*O, G*16], box {32, 128}, 32B swizzle
   CUtensorMap a_half;            // packed weights, box {32, 64} (gate/up tiles)
+  CUtensorMap b[kNumLoads];      // grouped token rows [P, I], box {64, rows}, 128B swizzle
 };
 
 struct __align__(16) TcShared {
   uint64_t full_a[kStagesAMax], empty_a[kStagesAMax];
-  // Chunk c uses token stage c % SB and TMEM A buffer c % kRing.
-  uint64_t full_b[kStagesBMax];  // tokens landed (TMA)
+  // Chunk c uses token stage c % SB and TMEM A buffer c % kABufs.
+  uint64_t b_full[kStagesBMax];  // the chunk's token rows have landed
+  uint64_t a_full[kABufs];       // A buffer written (and, for bf16 tiles on f16
+                                 // token rows, the chunk's token rows converted)
   uint64_t done[kStagesBMax];    // the chunk's MMAs finished: its stage and A buffer free
-  uint64_t a_full[kRing];        // A buffer written (dequantizers)
   uint64_t d_full[2], d_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t drain;
@@ -127,6 +150,7 @@ struct __align__(16) TcShared {
   int unit_ring[kUnitRing];      // unit indices in the order this CTA takes them; -1 ends
   uint32_t tmem_base;
   int scale_off[2];              // per scale buffer: offset of the tile's first byte, or -1
+  int scale_off_up[2];           // per scale buffer: offset of the up rows' first byte
   int num_units;
   int num_active;
   // Per active expert u: id, first position in the grouped list, tokens,
@@ -135,9 +159,7 @@ struct __align__(16) TcShared {
   int ex_beg[kMaxExpertsTc];
   int ex_cnt[kMaxExpertsTc];
   int unit_prefix[kMaxExpertsTc + 1];
-  // Gate/up tiles only.
-  int scale_off_up[2];           // per scale buffer: offset of the up rows' first byte
-  uint64_t epi_bar;              // the four epilogue warps
+  uint64_t epi_bar;              // the four epilogue warps (gate/up tiles)
 };
 
 // Position in a ring of n slots: slot index and the parity of its use.
@@ -161,6 +183,7 @@ struct Unit {
   int ntok;       // tokens in the block
   int nmma;       // MMA N: ntok rounded up to 16
   int load;       // token box: load_rows(load) >= nmma
+  int mt;         // row tile index
 };
 
 template <bool kSplit>
@@ -185,21 +208,22 @@ __device__ __forceinline__ Unit unit_at(const TcArgs& a, const TcShared& sh, int
   w.tok0 = beg + j * bsz;
   w.ntok = min(bsz, cnt - j * bsz);
   w.nmma = (w.ntok + 15) / 16 * 16;
-  w.load = 0;
-  while (load_rows(w.load) < w.nmma) ++w.load;
+  w.load = w.nmma / 16 - 1;
   // Gate/up tiles: m0 is the first gate row f0, rows the valid rows of each half.
   constexpr int tm = kSplit ? kBM / 2 : kBM;
+  w.mt = mt;
   w.m0 = mt * tm;
   w.rows = min(tm, (kSplit ? a.F : a.O) - w.m0);
   return w;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
-// both K-major, shape M x N.
-__device__ __forceinline__ uint32_t mma_idesc(int m, int n) {
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B both f16
+// or both bf16, both K-major, shape M x N.
+__device__ __forceinline__ uint32_t mma_idesc(int m, int n, bool f16) {
+  const uint32_t ab = f16 ? 0u : 1u;     // operand format: 0 f16, 1 bf16
   return (1u << 4)                       // D format: fp32
-         | (1u << 7)                     // A format: bf16
-         | (1u << 10)                    // B format: bf16
+         | (ab << 7)                     // A format
+         | (ab << 10)                    // B format
          | ((uint32_t)(n >> 3) << 17)    // N / 8
          | ((uint32_t)(m >> 4) << 24);   // M / 16
 }
@@ -280,6 +304,54 @@ __device__ __forceinline__ void dequant_group_bf16(const uint4& q, uint32_t s, u
   decode_word(q.w, t, w + 12);
 }
 
+// The same group as 16 f16x2 words LUT[code] * 2^(s - 127 - r): the hardware
+// conversion gives LUT[code] in f16 (exact), one f16x2 multiply applies the
+// power of two. Exact when -13 <= s - 127 - r <= 13 (then every nonzero
+// product lies in [2^-14, 49152], the normal f16 range).
+__device__ __forceinline__ void dequant_group_f16(const uint4& q, uint32_t s, int r,
+                                                  uint32_t (&w)[16]) {
+  const uint32_t f = (uint32_t)((int)s - 112 - r) * 0x04000400u;   // f16x2 2^(s-127-r)
+  const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2x4(qq[i], h);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[4 * i + j] = hmul2(h[j], f);
+  }
+}
+
+// The tile's operand mode (1: f16) and, for weight row `row` of expert e,
+// its offset r.
+__device__ __forceinline__ bool tile_f16(const TcArgs& a, const Unit& w) {
+  return a.f16_tiles && a.tile_mode[(size_t)w.e * a.mtiles + w.mt] != 0;
+}
+
+// A 16-byte global store with an L2 eviction policy.
+__device__ __forceinline__ void st_f4_policy(float* p, const float4& v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+
+// v * 2^e for any integer e, exact unless the result itself leaves the
+// float32 range: one multiply by a normal power of two when |e| allows it,
+// else several.
+__device__ __forceinline__ float scale_pow2(float v, int e) {
+  if (e >= -126 && e <= 127) return v * __uint_as_float((uint32_t)(e + 127) << 23);
+  while (e > 127) {
+    v *= __uint_as_float(254u << 23);     // 2^127
+    e -= 127;
+  }
+  while (e < -126) {
+    v *= __uint_as_float(1u << 23);       // 2^-126
+    e += 126;
+  }
+  return v * __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
+// One lane of a fully converged warp (elect.sync; the elected lane may
+// differ from call to call).
 __device__ __forceinline__ bool elect_one() {
   uint32_t e;
   asm volatile(
@@ -294,52 +366,82 @@ __device__ __forceinline__ bool elect_one() {
 }
 
 // A dequantizer team's place in the chunk sequence of its CTA: the global
-// index of its next chunk (chunks of earlier tiles included), that chunk's
-// packed stage and phase, and the use parity of the team's A buffer.
+// index of its next chunk (chunks of earlier tiles included) and that
+// chunk's packed stage and phase.
 struct TeamPos {
   int next;
   int stage;
   uint32_t stage_phase;
-  uint32_t buf_phase;
 };
 
 // The dequantizer's chunk loop for one tile whose chunks have global indices
-// base .. base+nk-1: thread m of team t decodes groups 2kc and 2kc+1 of row
-// m into A buffer t for each of the team's chunks kc. The packed tile
-// arrives with the 32-byte swizzle: the two 16-byte halves of row m are
-// exchanged when bit 2 of m is set, so eight consecutive rows read eight
-// different bank groups. scale(g) returns the row's scale byte of group g.
-// Returns false if a wait gave up.
+// base .. base+nk-1: thread m of team t decodes groups 2kc and 2kc+1 of row m
+// into A buffer t for each of the team's chunks kc. The packed tile arrives
+// with the 32-byte swizzle: the two 16-byte halves of row m are exchanged
+// when bit 2 of m is set, so eight consecutive rows read eight different
+// bank groups. scale(g) returns the row's scale byte of group g; f16 selects
+// the f16 decode with row offset r; convert: the chunk's token rows are f16
+// and this tile runs on bf16 operands. Returns false if a wait gave up.
 template <int SB, typename ScaleFn>
 __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* ring_a,
+                                             unsigned char* ring_b, uint32_t stage_b,
                                              int stages_a, uint32_t tmem, uint32_t lane_base,
-                                             int team, int m, int lane, int base, int nk,
-                                             TeamPos& tp, ScaleFn scale) {
+                                             int team, int m, int lane, int tid, int base, int nk,
+                                             int nmma, TeamPos& tp, ScaleFn scale, bool f16,
+                                             int r, bool convert) {
   const uint32_t sw = (uint32_t)(m >> 2) & 1u;
   const uint32_t off0 = (uint32_t)m * 32u + sw * 16u, off1 = (uint32_t)m * 32u + (sw ^ 1u) * 16u;
   const uint32_t a_col = tmem + lane_base + kACol + (uint32_t)team * 32;
-  for (; tp.next < base + nk; tp.next += kRing) {
+  for (; tp.next < base + nk; tp.next += kABufs) {
     const int kc = tp.next - base;
-    if (!mbar_wait(&sh.full_a[tp.stage], tp.stage_phase)) return false;
+    if (!mbar_wait_warp(&sh.full_a[tp.stage], tp.stage_phase)) return false;
     const unsigned char* stage = ring_a + (size_t)tp.stage * kStageA;
     const uint4 pk0 = *reinterpret_cast<const uint4*>(stage + off0);
     const uint4 pk1 = *reinterpret_cast<const uint4*>(stage + off1);
     const uint32_t s0 = scale(2 * kc), s1 = scale(2 * kc + 1);
+    fence_proxy_async_smem();                             // before the refill's TMA writes
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty_a[tp.stage]);   // packed bytes consumed
-    tp.stage += kRing;                                    // stages_a is a multiple of kRing
+    tp.stage += kABufs;                                   // stages_a is a multiple of kABufs
     if (tp.stage >= stages_a) {
       tp.stage -= stages_a;
       tp.stage_phase ^= 1u;
     }
     uint32_t v0[16], v1[16];
-    dequant_group_bf16(pk0, s0, v0);
-    dequant_group_bf16(pk1, s1, v1);
+    if (f16) {
+      dequant_group_f16(pk0, s0, r, v0);
+      dequant_group_f16(pk1, s1, r, v1);
+    } else {
+      dequant_group_bf16(pk0, s0, v0);
+      dequant_group_bf16(pk1, s1, v1);
+    }
     // The buffer is free once the MMAs of this team's previous chunk finished
-    // (chunk next - kRing, whose token stage is (next - kRing) % SB).
-    if (tp.next >= kRing) {
-      const int pc = tp.next - kRing;
-      if (!mbar_wait(&sh.done[pc % SB], (uint32_t)(pc / SB) & 1u)) return false;
+    // (chunk next - kABufs, whose token stage is (next - kABufs) % SB).
+    if (tp.next >= kABufs) {
+      const int pc = tp.next - kABufs;
+      if (!mbar_wait_warp(&sh.done[pc % SB], (uint32_t)(pc / SB) & 1u)) return false;
+    }
+    // bf16 tiles on f16 token rows: once the chunk's rows have landed,
+    // convert them in place, each of the team's 128 threads a share of the
+    // 16-byte pieces (f16 -> bf16 is exact for these values, which came from
+    // bf16), then make the writes visible to the tensor cores' reads.
+    const int st = tp.next % SB;
+    if (convert) {
+      if (!mbar_wait_warp(&sh.b_full[st], (uint32_t)(tp.next / SB) & 1u)) return false;
+      uint4* sb_base = reinterpret_cast<uint4*>(ring_b + (size_t)st * stage_b);
+      for (int i = tid; i < nmma * 8; i += kTeamWarps * 32) {
+        uint4 v = sb_base[i];
+        uint32_t* wv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = f16x2_to_f32x2(wv[k]);
+          const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+          wv[k] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        sb_base[i] = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
     }
     tc_fence_after_sync();
     tmem_st16(a_col, v0);
@@ -348,7 +450,6 @@ __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* 
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.a_full[team]);
-    tp.buf_phase ^= 1u;
   }
   return true;
 }
@@ -358,7 +459,9 @@ __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* 
 // false if the wait gave up; *idx < 0 means no more units.
 template <bool kWarp>
 __device__ __forceinline__ bool pop_unit(TcShared& sh, RingPos& pu, int lane, int* idx) {
-  if (!mbar_wait(&sh.u_full[pu.idx], pu.phase)) return false;
+  if (kWarp ? !mbar_wait_warp(&sh.u_full[pu.idx], pu.phase)
+            : !mbar_wait(&sh.u_full[pu.idx], pu.phase))
+    return false;
   *idx = sh.unit_ring[pu.idx];
   if (kWarp) __syncwarp();
   if (lane == 0) mbar_arrive(&sh.u_empty[pu.idx]);
@@ -371,7 +474,7 @@ __device__ __forceinline__ bool pop_unit(TcShared& sh, RingPos& pu, int lane, in
 __device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, int lane) {
   __syncwarp();
   if (lane == 0) mbar_arrive(bar);
-  const bool done = mbar_wait(bar, phase);
+  const bool done = mbar_wait_warp(bar, phase);
   phase ^= 1u;
   return done;
 }
@@ -380,15 +483,15 @@ __device__ __forceinline__ float silu_times(float g, float u) { return g / (1.f 
 
 // Epilogue of a gate/up tile: 16 token columns at a time, each epilogue warp
 // moves its 32 accumulator rows into shared memory (column-major, all four
-// warps' rows side by side); then thread (cq, rp) forms h = silu(gate) * up
-// for gate rows 2rp, 2rp+1 of the tile (their up rows sit 64 rows further,
-// two warps on) and token columns 4cq..4cq+3, in float32, and stores each
-// pair of rows as one bf16x2. The tile of the first rows of a token block
-// also writes its pairs' expert for the down projection. Returns false if a
-// wait gave up.
+// warps' rows side by side), scaled back from the f16 operands' powers of
+// two in f16 mode; then thread (cq, rp) forms h = silu(gate) * up for gate
+// rows 2rp, 2rp+1 of the tile (their up rows sit 64 rows further, two warps
+// on) and token columns 4cq..4cq+3, in float32, and stores each pair of rows
+// as one bf16x2. The tile of the first rows of a token block also writes its
+// pairs' expert for the down projection. Returns false if a wait gave up.
 __device__ bool swiglu_epilogue(const TcArgs& a, const Unit& w, uint32_t d_cols,
                                 uint32_t lane_base, float* epi_all, int q, int lane,
-                                uint64_t* bar, uint32_t& phase) {
+                                uint64_t* bar, uint32_t& phase, int roff) {
   float* mine = epi_all + q * (kEpiStage / 4);
   const int et = 32 * q + lane;
   const int rp = et & 31, cq = et >> 5;
@@ -397,11 +500,19 @@ __device__ bool swiglu_epilogue(const TcArgs& a, const Unit& w, uint32_t d_cols,
   const float* usrc = gsrc + 2 * (kEpiStage / 4);
   const bool row_ok = r0 < w.rows;             // rows is even: r0 + 1 too
   for (int c0 = 0; c0 < w.nmma; c0 += 16) {
+    // sigma of the grouped rows of these 16 columns: one load per lane, then broadcast.
+    int my_sig = 0;
+    if (a.b_f16 && lane < 16 && c0 + lane < w.ntok) my_sig = a.sigma[w.tok0 + c0 + lane];
     uint32_t v[16];
+    __syncwarp();
     tmem_ld16(d_cols + lane_base + (uint32_t)c0, v);
     tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 16; ++i) mine[i * 32 + lane] = __uint_as_float(v[i]);
+    for (int i = 0; i < 16; ++i) {
+      const int sg = __shfl_sync(kFullMask, my_sig, i);
+      const float x = __uint_as_float(v[i]);
+      mine[i * 32 + lane] = a.b_f16 ? scale_pow2(x, roff - sg) : x;
+    }
     if (!epi_sync(bar, phase, lane)) return false;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -426,12 +537,12 @@ __device__ bool swiglu_epilogue(const TcArgs& a, const Unit& w, uint32_t d_cols,
 template <int SB, bool kSplit>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
-  static_assert(SB >= kRing && SB <= kStagesBMax, "token ring depth");
+  static_assert(SB >= kABufs && SB <= kStagesBMax, "token ring depth");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // Token stages need 1024-byte alignment (128-byte swizzle atoms).
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* ring_b = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  unsigned char* ring_a = ring_b + (size_t)SB * kStageB;
+  unsigned char* ring_a = ring_b + (size_t)SB * a.stage_b;
   unsigned char* scale_buf = ring_a + (size_t)a.stages_a * kStageA;
   TcShared& sh = *reinterpret_cast<TcShared*>(scale_buf + 2 * a.scale_cap);
   float* epi_stage = reinterpret_cast<float*>(&sh + 1);   // 16-byte aligned (TcShared is)
@@ -445,17 +556,17 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       mbar_init(&sh.empty_a[s], kTeamWarps);
     }
     for (int r = 0; r < SB; ++r) {
-      mbar_init(&sh.full_b[r], 1);
+      mbar_init(&sh.b_full[r], 1);               // producer B (bytes)
       mbar_init(&sh.done[r], 1);
     }
-    for (int r = 0; r < kRing; ++r) mbar_init(&sh.a_full[r], kTeamWarps);
+    for (int r = 0; r < kABufs; ++r) mbar_init(&sh.a_full[r], kTeamWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.d_full[b], 1);
       mbar_init(&sh.d_empty[b], 4);
       mbar_init(&sh.s_full[b], 1);
       mbar_init(&sh.s_empty[b], kDequantWarps);
     }
-    mbar_init(&sh.drain, 1);
+    mbar_init(&sh.drain, 32);                    // every lane of the MMA warp
     if (kSplit) mbar_init(&sh.epi_bar, 4);
     for (int r = 0; r < kUnitRing; ++r) {
       mbar_init(&sh.u_full[r], 1);
@@ -467,9 +578,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  pdl_wait();                    // routing lists and grouped tokens are ready
-  if (warp == 2) {
-    // Per active expert: id, segment and token-block count (ceil(cnt / 192));
+  pdl_wait();                    // routing lists and prepared tokens are ready
+  if (warp == kListWarp) {
+    // Per active expert: id, segment and token-block count (ceil(cnt / nmax));
     // units are (expert, token block, 128-row tile).
     const int na = a.plan.meta[kMetaNumActive];
     int run = 0;
@@ -483,7 +594,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         sh.ex_id[u] = e;
         sh.ex_beg[u] = beg;
         sh.ex_cnt[u] = cnt;
-        nb = (cnt + kNMax - 1) / kNMax;
+        nb = (cnt + a.nmax - 1) / a.nmax;
       }
       int incl = nb;
 #pragma unroll
@@ -506,7 +617,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   const uint32_t tmem = sh.tmem_base;
   const int num_units = sh.num_units;
   const int G = a.G, O = a.O;
-  const int nk = G / 2;                              // chunks of 64 = 2 groups
+  const int nk = G / 2;                              // chunks of 64 = two groups
   bool ok = true;
 
   if (warp == 0) {
@@ -588,7 +699,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)(k >> 1) & 1u)) break;
     }
     __syncwarp();
-  } else if (warp == 3) {
+  } else if (warp == kProdBWarp) {
     // ------------------------------------------------------ producer B: tokens
     if (lane == 0) {
       const uint64_t pol = l2_evict_last_policy();      // tokens: reread per tile
@@ -599,31 +710,36 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         if (idx < 0) break;
         const Unit w = unit_at<kSplit>(a, sh, idx);
         if (w.ntok <= 0) continue;
-        const uint32_t tx = (uint32_t)load_rows(w.load) * 128u;
+        const uint32_t box = (uint32_t)load_rows(w.load) * 128u;
         for (int kc = 0; kc < nk; ++kc, ++issued) {
           if (!mbar_wait(&sh.done[pr.idx], pr.phase ^ 1u)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sh.full_b[pr.idx], tx);
-          tma_load_2d(ring_b + (size_t)pr.idx * kStageB, &maps.b[w.load], kc * kBK, w.tok0,
-                      &sh.full_b[pr.idx], pol);
+          mbar_arrive_expect_tx(&sh.b_full[pr.idx], box);
+          tma_load_2d(ring_b + (size_t)pr.idx * a.stage_b, &maps.b[w.load], kc * kBK, w.tok0,
+                      &sh.b_full[pr.idx], pol);
           pr.next(SB);
         }
       }
       if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
       for (int k = 0; k < min(issued, SB); ++k) {
-        int idx = pr.idx - 1 - k;
+        int ridx = pr.idx - 1 - k;
         uint32_t ph = pr.phase;
-        if (idx < 0) { idx += SB; ph ^= 1u; }
-        if (!mbar_wait(&sh.full_b[idx], ph)) break;
+        if (ridx < 0) { ridx += SB; ph ^= 1u; }
+        if (!mbar_wait(&sh.b_full[ridx], ph)) break;
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    // The whole warp runs the loop and waits; one elected lane (always the
-    // same one, so its commits track its own MMAs) issues.
+    // The whole warp runs the loop and waits; one elected lane issues a
+    // chunk's MMAs and, in the same block, the commits that depend on them
+    // (a commit tracks only the MMAs of the thread that issues it). elect.sync
+    // need not pick the same lane each time, and MMAs into one accumulator
+    // from different threads are ordered only across a thread
+    // synchronisation bracketed by the tcgen05 fences: the issuing lane
+    // fences before the warp synchronises, every lane after its waits.
     int it = 0, idx;
     RingPos pr, pb, pu;               // A buffer, token stage, unit ring
     for (; ok; ++it) {
@@ -634,16 +750,16 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const int db = it & 1;
       if (!mbar_wait(&sh.d_empty[db], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
       tc_fence_after_sync();
-      const uint32_t idesc = mma_idesc(kBM, w.nmma);
       const uint32_t d_tmem = tmem + kDCol + (uint32_t)db * kNMax;
+      const uint32_t idesc = mma_idesc(kBM, w.nmma, tile_f16(a, w));
       for (int kc = 0; kc < nk; ++kc) {
-        if (!mbar_wait(&sh.full_b[pb.idx], pb.phase) ||
+        if (!mbar_wait(&sh.b_full[pb.idx], pb.phase) ||
             !mbar_wait(&sh.a_full[pr.idx], pr.phase)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t b_addr = smem_addr(ring_b + (size_t)pb.idx * kStageB);
+        const uint32_t b_addr = smem_addr(ring_b + (size_t)pb.idx * a.stage_b);
         const uint32_t a_tmem = tmem + kACol + (uint32_t)pr.idx * 32;
         if (elect_one()) {
 #pragma unroll
@@ -651,27 +767,28 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
             tc_mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
                       (kc > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&sh.done[pb.idx]);     // token stage and A buffer free once these finish
+          if (kc == nk - 1) tc_commit(&sh.d_full[db]);   // accumulator complete
+          tc_fence_before_sync();
         }
         __syncwarp();
-        pr.next(kRing);
+        pr.next(kABufs);
         pb.next(SB);
       }
       if (!ok) break;
-      if (elect_one()) tc_commit(&sh.d_full[db]);   // accumulator complete
-      __syncwarp();
     }
     if (!ok && lane == 0) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
-    // Do not free TMEM under running MMAs: wait (bounded) for all of them.
-    if (elect_one()) tc_commit(&sh.drain);
-    __syncwarp();
+    // Do not free TMEM under running MMAs: every lane commits (whichever
+    // lanes issued MMAs), and the drain completes when all of them have.
+    tc_commit(&sh.drain);
     mbar_wait(&sh.drain, 0);
   } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + kDequantWarps) {
     // -------------------------------------------------------- dequantizers
-    const int team = (warp - kDequantWarp0) / kTeamWarps;
+    const int sub = warp - kDequantWarp0;
+    const int team = sub / kTeamWarps;
     const int q = warp & 3;                          // TMEM lane quarter
     const int m = 32 * q + lane;                     // weight row in the tile
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    TeamPos tp{team, team, 0u, 0u};                  // chunk `team` is the team's first
+    TeamPos tp{team, team, 0u};                      // chunk `team` is the team's first
     int it = 0, base = 0, idx;
     RingPos pu;
     for (; ok; ++it) {
@@ -680,27 +797,34 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const Unit w = unit_at<kSplit>(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int sb = it & 1;
-      if (!mbar_wait(&sh.s_full[sb], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
+      if (!mbar_wait_warp(&sh.s_full[sb], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
       // Row m's place in its span: gate/up tiles hold two spans of rows
       // (m < 64: gate row f0 + m; else up row F + f0 + m - 64).
       const bool up = kSplit && m >= kBM / 2;
       const int hrow = min(kSplit ? (m & (kBM / 2 - 1)) : m, w.rows - 1);
+      const bool f16 = tile_f16(a, w);
+      const int r = f16 ? a.row_off[(size_t)w.e * O + (up ? a.F : 0) + w.m0 + hrow] : 0;
+      const bool convert = !f16 && a.b_f16 != 0;     // bf16 tile on f16 token rows
+      const int tid = (sub % kTeamWarps) * 32 + lane;
       const int soff = up ? sh.scale_off_up[sb] : sh.scale_off[sb];
       // The choice of scale source is the same for the whole tile: take it
       // once, so the chunk loop holds no global load.
       if (soff >= 0) {
         const unsigned char* srow =
             scale_buf + (size_t)sb * a.scale_cap + soff + (size_t)hrow * G;
-        ok = dequant_tile<SB>(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk,
-                              tp, [&](int g) { return (uint32_t)srow[g]; });
+        ok = dequant_tile<SB>(sh, ring_a, ring_b, a.stage_b, a.stages_a, tmem, lane_base, team,
+                              m, lane, tid, base, nk, w.nmma, tp,
+                              [&](int g) { return (uint32_t)srow[g]; }, f16, r, convert);
       } else {
         const uint8_t* grow =
             a.scales + ((size_t)w.e * O + (up ? a.F : 0) + w.m0 + hrow) * G;
-        ok = dequant_tile<SB>(sh, ring_a, a.stages_a, tmem, lane_base, team, m, lane, base, nk,
-                              tp, [&](int g) { return (uint32_t)__ldg(grow + g); });
+        ok = dequant_tile<SB>(sh, ring_a, ring_b, a.stage_b, a.stages_a, tmem, lane_base, team,
+                              m, lane, tid, base, nk, w.nmma, tp,
+                              [&](int g) { return (uint32_t)__ldg(grow + g); }, f16, r, convert);
       }
       base += nk;
       if (!ok) break;
+      fence_proxy_async_smem();                      // scale bytes read: the next copy may land
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
     }
@@ -720,11 +844,19 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const Unit w = unit_at<kSplit>(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int db = it & 1;
-      if (!mbar_wait(&sh.d_full[db], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
-      tc_fence_after_sync();
+      // The accumulator holds 2^(sigma - r) times the result for f16 token
+      // rows (r = 0 in bf16 mode).
+      int roff = 0;
+      if (tile_f16(a, w)) {
+        const bool up = kSplit && m >= kBM / 2;
+        const int hrow = min(kSplit ? (m & (kBM / 2 - 1)) : m, w.rows - 1);
+        roff = a.row_off[(size_t)w.e * O + (up ? a.F : 0) + w.m0 + hrow];
+      }
       if constexpr (kSplit) {
+        if (!mbar_wait_warp(&sh.d_full[db], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
+        tc_fence_after_sync();
         if (!swiglu_epilogue(a, w, tmem + kDCol + (uint32_t)db * kNMax, lane_base, epi_stage, q,
-                             lane, &sh.epi_bar, epi_phase)) {
+                             lane, &sh.epi_bar, epi_phase, roff)) {
           ok = false;
           break;
         }
@@ -735,6 +867,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       }
       const bool row_ok = m < w.rows;
       float* out_col = a.part + w.m0 + m;
+
       // Four consecutive rows per store: this warp's 32 rows x 16 columns go
       // through shared memory (column-major), then lane (c, j) of each round
       // stores rows 4j..4j+3 of column c. Needs whole 4-row groups inside
@@ -742,13 +875,49 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const bool vec = (O & 3) == 0 && 32 * q + 32 <= w.rows;
       const int jr = lane & 7;                       // 4-row group of the lane
       float* part_rows = a.part + w.m0 + 32 * q + 4 * jr;
+      // Partial results are written once and read once by the combine: keep
+      // them from evicting the token rows, which every row tile rereads.
+      const uint64_t st_pol = l2_evict_first_policy();
+      if (!mbar_wait_warp(&sh.d_full[db], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
+      tc_fence_after_sync();
       for (int c0 = 0; c0 < w.nmma; c0 += 16) {
-        // Pair ids of these 16 columns: one load per lane, then broadcast.
-        const int my_pair = (lane < 16 && c0 + lane < w.ntok)
-                                ? a.plan.pair_list[w.tok0 + c0 + lane] : 0;
+        // Pair ids (and for f16 rows the powers of two) of these 16 columns:
+        // one load per lane, then broadcast.
+        int my_pair = 0, my_sig = 0;
+        if (lane < 16 && c0 + lane < w.ntok) {
+          my_pair = a.plan.pair_list[w.tok0 + c0 + lane];
+          if (a.b_f16) my_sig = a.sigma[w.tok0 + c0 + lane];
+        }
         uint32_t v[16];
+        __syncwarp();
         tmem_ld16(tmem + lane_base + kDCol + (uint32_t)db * kNMax + (uint32_t)c0, v);
         tmem_wait_ld();
+        if (a.b_f16) {
+          // One multiply by 2^(r - sigma) per element; the range check once
+          // per 16 columns (the smallest and largest sigma of the group).
+          int smin = lane < 16 && c0 + lane < w.ntok ? my_sig : 1 << 20;
+          int smax = lane < 16 && c0 + lane < w.ntok ? my_sig : -(1 << 20);
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) {
+            smin = min(smin, __shfl_xor_sync(kFullMask, smin, o));
+            smax = max(smax, __shfl_xor_sync(kFullMask, smax, o));
+          }
+          smin = __shfl_sync(kFullMask, smin, 0);
+          smax = __shfl_sync(kFullMask, smax, 0);
+          if (roff - smax >= -126 && roff - smin <= 127) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int e = roff - __shfl_sync(kFullMask, my_sig, i) + 127;
+              v[i] = __float_as_uint(__uint_as_float(v[i]) * __uint_as_float((uint32_t)e << 23));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int sg = __shfl_sync(kFullMask, my_sig, i);
+              v[i] = __float_as_uint(scale_pow2(__uint_as_float(v[i]), roff - sg));
+            }
+          }
+        }
         if (vec) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) stage[i * 32 + lane] = __uint_as_float(v[i]);
@@ -758,8 +927,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
             const int c = 4 * r + (lane >> 3);
             const int pair = __shfl_sync(kFullMask, my_pair, c);
             if (c0 + c < w.ntok)
-              *reinterpret_cast<float4*>(part_rows + (size_t)pair * O) =
-                  *reinterpret_cast<const float4*>(stage + c * 32 + 4 * jr);
+              st_f4_policy(part_rows + (size_t)pair * O,
+                           *reinterpret_cast<const float4*>(stage + c * 32 + 4 * jr), st_pol);
           }
           __syncwarp();
         } else {
@@ -785,11 +954,14 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   }
 }
 
-// x rows grouped by expert: xg[pos, :] = x[pair_list[pos] / K, :].
+// Token rows grouped by expert for the tensor-core kernel: row p of xg is
+// token t = pair_list[p] / K as f16(x[t] 2^sigma) with max |x_t| 2^sigma in
+// [2^14, 2^15), sigma[p] its power of two; one warp per row. Also resets the
+// kernel's unit counters and, for gate/up tiles, the down projection's ids.
 __global__ void __launch_bounds__(256)
-gather_tokens_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xg,
-                     RoutePlan plan, int I, int K, int32_t* __restrict__ zero_ids,
-                     int64_t nzero) {
+group_tokens_kernel(const __nv_bfloat16* __restrict__ x, __half* __restrict__ xg,
+                    int* __restrict__ sigma, RoutePlan plan, int I, int K,
+                    int32_t* __restrict__ zero_ids, int64_t nzero) {
   pdl_launch_dependents();
   pdl_wait();                    // the bucketer's lists are ready
   // The tensor-core kernel after this one takes its units from this counter.
@@ -803,14 +975,78 @@ gather_tokens_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restr
        i += (int64_t)gridDim.x * blockDim.x)
     zero_ids[i] = 0;
   const int npairs = plan.meta[kMetaNumPairs];
-  const int vec_per_row = I / 8;
   const int warps = blockDim.x / 32;
-  for (int pos = blockIdx.x * warps + (threadIdx.x >> 5); pos < npairs; pos += gridDim.x * warps) {
+  for (int pos = blockIdx.x * warps + (threadIdx.x >> 5); pos < npairs;
+       pos += gridDim.x * warps) {
     const int t = plan.pair_list[pos] / K;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * I);
-    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)pos * I);
-    for (int v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    // prep_token addresses row `t` of its arguments: point them at the
+    // token's row and the grouped row, as row 0.
+    prep_token(x + (size_t)t * I, xg + (size_t)pos * I, sigma + pos, 0, I, threadIdx.x & 31, 14);
   }
+}
+
+// Operand modes of the tensor-core kernel's tiles: for tile mt of expert e
+// (128 rows, or for gate/up tiles 64 gate rows and their 64 up rows), every
+// row's smallest and largest scale byte; tile_mode = 1 when every row spans
+// at most kF16Span binades, row_off[row] = largest - 140 (so that the row's
+// largest scaled weight is 6 * 2^13). One block of 128 threads per tile: the
+// tile's scale bytes (one or two contiguous spans of rows) are copied into
+// shared memory with consecutive threads on consecutive bytes, then thread m
+// scans row m. It reads only the weights' scale bytes before it waits for the
+// previous kernel, and writes its outputs only after that wait.
+template <bool kSplit>
+__global__ void __launch_bounds__(128)
+tile_scan_kernel(const uint8_t* __restrict__ scales, int G, int O, int F, int mtiles,
+                 uint8_t* __restrict__ tile_mode, int16_t* __restrict__ row_off) {
+  pdl_launch_dependents();
+  extern __shared__ __align__(16) uint8_t span[];   // kBM * G + 64 bytes
+  const int mt = blockIdx.x, e = blockIdx.y, m = threadIdx.x;
+  // Rows of each span: [r0, r0 + n) of expert e's matrix, stored at span
+  // offset base.
+  constexpr int kSpans = kSplit ? 2 : 1;
+  constexpr int kSpanRows = kBM / kSpans;
+  // Each span through the 16-byte aligned window that holds it (a 16-byte
+  // aligned block never crosses a page, so the window's extra bytes are
+  // always readable); row j of span h then starts at off[h] + j * G.
+  __shared__ int off[kSpans];
+  for (int h = 0; h < kSpans; ++h) {
+    const int first = kSplit ? mt * kSpanRows : mt * kBM;
+    const int limit = kSplit ? F : O;
+    const int n = max(0, min(kSpanRows, limit - first));
+    const int r0 = (kSplit && h == 1 ? F : 0) + first;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(scales + ((size_t)e * O + r0) * G);
+    const uintptr_t w0 = lo & ~(uintptr_t)15, w1 = (lo + (uintptr_t)n * G + 15) & ~(uintptr_t)15;
+    uint4* dst = reinterpret_cast<uint4*>(span + (size_t)h * (kSpanRows * G + 32));
+    const uint4* src = reinterpret_cast<const uint4*>(w0);
+    for (int i = m; i < (int)((w1 - w0) / 16); i += blockDim.x) dst[i] = __ldg(src + i);
+    if (m == 0) off[h] = h * (kSpanRows * G + 32) + (int)(lo - w0);
+  }
+  __syncthreads();
+  int row = -1;
+  if (kSplit) {
+    const int f = mt * kSpanRows + (m & (kSpanRows - 1));
+    if (f < F) row = (m >= kSpanRows ? F : 0) + f;
+  } else if (mt * kBM + m < O) {
+    row = mt * kBM + m;
+  }
+  bool fits = true;
+  uint32_t lo = 255, hi = 0;
+  if (row >= 0) {
+    const uint8_t* p = span + off[kSplit && m >= kSpanRows ? 1 : 0] + (size_t)(m % kSpanRows) * G;
+#pragma unroll 8
+    for (int g = 0; g < G; ++g) {
+      const uint32_t v = p[g];
+      lo = min(lo, v);
+      hi = max(hi, v);
+    }
+    fits = (int)(hi - lo) <= kF16Span;
+  }
+  const int all = __syncthreads_and(fits ? 1 : 0);
+  // The outputs live in the call's scratch, which earlier kernels on the
+  // stream may still be using: write them only once those have finished.
+  pdl_wait();
+  if (row >= 0) row_off[(size_t)e * O + row] = (int16_t)((int)hi - 140);
+  if (m == 0) tile_mode[(size_t)e * mtiles + mt] = all ? 1 : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -840,12 +1076,37 @@ int num_sms_tc() {
   return cached[dev];
 }
 
-size_t tc_shared_bytes(int stages_a, int stages_b, uint32_t scale_cap) {
-  return 1024 + (size_t)stages_b * kStageB + (size_t)stages_a * kStageA + 2 * (size_t)scale_cap +
+size_t tc_shared_bytes(int stages_a, int stages_b, uint32_t stage_b, uint32_t scale_cap) {
+  return 1024 + (size_t)stages_b * stage_b + (size_t)stages_a * kStageA + 2 * (size_t)scale_cap +
          sizeof(TcShared) + (kTcThreads / 32 - kEpiWarp0) * (size_t)kEpiStage;
 }
 
 constexpr size_t kSmemLimit = 227 * 1024;
+
+// Ring sizes and block width for one launch: as many token stages (up to
+// kStagesBMax, at least 4) of the widest block (192, else 128 token columns)
+// as fit beside eight packed-weight stages, then as deep a packed-weight ring
+// as shared memory allows (a multiple of kABufs: each dequantizer team keeps
+// to its own stages). Returns false if nothing fits.
+struct TcConfig {
+  int nmax;
+  int stages_b;
+  int stages_a;
+  uint32_t stage_b;
+};
+bool tc_config(uint32_t scale_cap, TcConfig* c) {
+  for (int nmax : {kNMax, 128}) {
+    const uint32_t sbytes = (uint32_t)nmax * 128u;
+    for (int sb = kStagesBMax; sb >= 4; --sb) {
+      if (tc_shared_bytes(2 * kABufs, sb, sbytes, scale_cap) > kSmemLimit) continue;
+      int sa = kStagesAMax;
+      while (sa > kABufs && tc_shared_bytes(sa, sb, sbytes, scale_cap) > kSmemLimit) sa -= kABufs;
+      *c = TcConfig{nmax, sb, sa, sbytes};
+      return true;
+    }
+  }
+  return false;
+}
 
 template <int SB, bool kSplit>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& args, size_t smem, cudaStream_t stream) {
@@ -862,21 +1123,43 @@ cudaError_t launch_tc(const TcMaps& maps, const TcArgs& args, size_t smem, cudaS
       opted[dev] = smem;
     }
   }
-  return launch_after_previous(gemm_tc_kernel<SB, kSplit>, dim3((unsigned)num_sms_tc()), dim3(kTcThreads),
-                               smem, stream, maps, args);
+  return launch_after_previous(gemm_tc_kernel<SB, kSplit>, dim3((unsigned)num_sms_tc()),
+                               dim3(kTcThreads), smem, stream, maps, args);
 }
 
 }  // namespace
 
-cudaError_t launch_gather_tokens(const void* x, const RoutePlan& plan, void* grouped,
-                                 int64_t T, int64_t I, int64_t K, int32_t* zero_ids,
-                                 cudaStream_t stream) {
+cudaError_t launch_group_tokens(const void* x, const RoutePlan& plan, __half* xg, int* sigma,
+                                int64_t T, int64_t I, int64_t K, int32_t* zero_ids,
+                                cudaStream_t stream) {
   const int64_t P = T * K;
   const int64_t blocks = std::min<int64_t>((P + 7) / 8, (int64_t)num_sms_tc() * 8);
-  return launch_after_previous(gather_tokens_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)),
-                               dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x),
-                               static_cast<__nv_bfloat16*>(grouped), plan, (int)I, (int)K,
-                               zero_ids, zero_ids != nullptr ? P : (int64_t)0);
+  return launch_after_previous(group_tokens_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)),
+                               dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x), xg,
+                               sigma, plan, (int)I, (int)K, zero_ids,
+                               zero_ids != nullptr ? P : (int64_t)0);
+}
+
+size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I) {
+  return (size_t)T * K * I * sizeof(__half);
+}
+
+int64_t gemm_tc_row_tiles(int64_t O, int64_t F) {
+  return F > 0 ? (F + kBM / 2 - 1) / (kBM / 2) : (O + kBM - 1) / kBM;
+}
+
+cudaError_t launch_tile_scan(const uint8_t* scales, int64_t E, int64_t I, int64_t O, int64_t F,
+                             uint8_t* tile_mode, int16_t* row_off, cudaStream_t stream) {
+  const int64_t mtiles = gemm_tc_row_tiles(O, F);
+  if (E <= 0 || mtiles <= 0) return cudaSuccess;
+  const dim3 grid((unsigned)mtiles, (unsigned)E);
+  const size_t smem = (size_t)kBM * (I / 32) + 64;   // a tile's scale bytes, two windows
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;
+  if (F > 0)
+    return launch_after_previous(tile_scan_kernel<true>, grid, dim3(128), smem, stream, scales,
+                                 (int)(I / 32), (int)O, (int)F, (int)mtiles, tile_mode, row_off);
+  return launch_after_previous(tile_scan_kernel<false>, grid, dim3(128), smem, stream, scales,
+                               (int)(I / 32), (int)O, 0, (int)mtiles, tile_mode, row_off);
 }
 
 // Bytes per scale buffer: one tile's span, or the two spans of a gate/up tile.
@@ -888,32 +1171,32 @@ uint32_t tc_scale_cap(int64_t G, bool halves) {
 
 bool gemm_tc_supported(int64_t E, int64_t I, int64_t O) {
   const int64_t G = I / 32;
-  if (G % 2 != 0) return false;                    // K chunks of 64
+  if (G % 2 != 0) return false;                    // chunks of whole group pairs
   if (E > kMaxExpertsTc || E * O > 0x7fffffff) return false;
-  return tc_shared_bytes(kRing, kRing, tc_scale_cap(G, false)) <= kSmemLimit;
+  TcConfig c;
+  return tc_config(tc_scale_cap(G, false), &c);
 }
 
 bool gemm_tc_swiglu_supported(int64_t E, int64_t I, int64_t F) {
+  TcConfig c;
   return F > 0 && F % 32 == 0 && gemm_tc_supported(E, I, 2 * F) &&
-         tc_shared_bytes(kRing, kRing, tc_scale_cap(I / 32, true)) <= kSmemLimit;
+         tc_config(tc_scale_cap(I / 32, true), &c);
 }
 
-size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I) {
-  return (size_t)T * K * I * sizeof(__nv_bfloat16);
-}
-
-cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* scales,
-                           const RoutePlan& plan, void* grouped, float* part,
-                           unsigned long long* status, int64_t T, int64_t E, int64_t I,
-                           int64_t O, int64_t K, const SwigluTiles& swiglu,
-                           cudaStream_t stream, int counter_word) {
+cudaError_t launch_gemm_tc(const TcTokens& tok, const TcTileModes& modes, const uint8_t* packed,
+                           const uint8_t* scales, const RoutePlan& plan, float* part,
+                           unsigned long long* status, int64_t E, int64_t I, int64_t O,
+                           int64_t K, const SwigluTiles& swiglu, cudaStream_t stream,
+                           int counter_word) {
   if (swiglu.F > 0 && (O != 2 * swiglu.F || !gemm_tc_swiglu_supported(E, I, swiglu.F)))
     return cudaErrorInvalidValue;
-  const int64_t G = I / 32, P = T * K;
+  const int64_t G = I / 32;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
+  TcConfig cfg;
+  const uint32_t scale_cap = tc_scale_cap(G, swiglu.F > 0);
+  if (!tc_config(scale_cap, &cfg)) return cudaErrorInvalidValue;
 
-  (void)x;
   // Tensor maps.
   TcMaps maps;
   {
@@ -932,11 +1215,12 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
       return cudaErrorInvalidValue;
   }
   for (int l = 0; l < kNumLoads; ++l) {
-    const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)std::max<int64_t>(P, 1)};
+    const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)std::max<int64_t>(tok.nrows, 1)};
     const cuuint64_t strides[1] = {(cuuint64_t)(I * 2)};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)load_rows(l)};
+    const cuuint32_t box[2] = {64, (cuuint32_t)load_rows(l)};
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&maps.b[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, grouped, dims, strides, box, estr,
+    if (enc(&maps.b[l], tok.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+            2, const_cast<void*>(tok.rows), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -948,6 +1232,7 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
   args.scales_end = scales + (size_t)E * O * G;
   args.part = part;
   args.status = status;
+  args.sigma = tok.sigma;
   args.G = (int)G;
   args.O = (int)O;
   args.K = (int)K;
@@ -956,20 +1241,20 @@ cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* 
   args.sel2 = swiglu.sel2;
   args.h_grouped = swiglu.grouped ? 1 : 0;
   args.counter_word = counter_word;
-  args.mtiles = swiglu.F > 0 ? (int)((swiglu.F + kBM / 2 - 1) / (kBM / 2))
-                             : (int)((O + kBM - 1) / kBM);
-  args.scale_cap = tc_scale_cap(G, swiglu.F > 0);
-  // As many token stages as fit next to 8 packed-weight stages (their
-  // refill latency is what the MMAs wait on), then as deep a packed-weight
-  // ring as shared memory allows, a multiple of kRing so that each
-  // dequantizer team keeps to its own stages.
-  int sb = kRing;
-  while (sb < kStagesBMax && tc_shared_bytes(2 * kRing, sb + 1, args.scale_cap) <= kSmemLimit) ++sb;
-  int sa = kStagesAMax;
-  while (sa > kRing && tc_shared_bytes(sa, sb, args.scale_cap) > kSmemLimit) sa -= kRing;
-  args.stages_a = sa;
-  const size_t smem = tc_shared_bytes(sa, sb, args.scale_cap);
-  switch (sb) {
+  args.mtiles = (int)gemm_tc_row_tiles(O, swiglu.F);
+  args.scale_cap = scale_cap;
+  args.b_f16 = tok.f16 && tok.sigma != nullptr ? 1 : 0;
+  args.f16_tiles = args.b_f16 && modes.tile_mode != nullptr && modes.row_off != nullptr ? 1 : 0;
+  args.tile_mode = modes.tile_mode;
+  args.row_off = modes.row_off;
+  // Test knob: MXFP4EL_TC_MODE=bf16 keeps every tile in the bf16 operand mode.
+  if (const char* env = std::getenv("MXFP4EL_TC_MODE"))
+    if (std::strcmp(env, "bf16") == 0) args.f16_tiles = 0;
+  args.nmax = cfg.nmax;
+  args.stage_b = cfg.stage_b;
+  args.stages_a = cfg.stages_a;
+  const size_t smem = tc_shared_bytes(cfg.stages_a, cfg.stages_b, cfg.stage_b, scale_cap);
+  switch (cfg.stages_b) {
     case 6:
       return swiglu.F > 0 ? launch_tc<6, true>(maps, args, smem, stream)
                           : launch_tc<6, false>(maps, args, smem, stream);

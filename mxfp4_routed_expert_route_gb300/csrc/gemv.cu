@@ -807,6 +807,7 @@ gemv_stream_kernel(const StreamArgs a) {
         cached_e = -1;
       }
     }
+    fence_proxy_async_smem();           // stage read: the refill's bulk copies may land
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
     if (++st == a.stages) {

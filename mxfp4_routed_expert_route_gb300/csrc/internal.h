@@ -62,9 +62,12 @@ struct UnitSplit {
 struct Workspace {
   RoutePlan plan;
   int* wc_global;   // per-warp counters when they do not fit in shared memory
-  __half* x16;      // [T, I] tokens scaled by 2^sigma_t in f16 (bf16 tokens)
-  int* sigma;       // [T] the power of two of each token (bf16 tokens)
-  void* grouped;    // [T*K, I] bf16 tokens grouped by expert (tensor-core path)
+  __half* x16;      // [T, I] tokens scaled by 2^sigma_t in f16 (staged GEMV, bf16 tokens)
+  int* sigma;       // [T] the power of two of each token (staged GEMV, bf16 tokens)
+  __half* grouped;  // [T*K, I] f16 token rows grouped by expert (tensor-core path)
+  int* gsigma;      // [T*K] the power of two of each grouped row
+  uint8_t* tile_mode;  // [E][row tiles] operand mode of each tile (tensor-core path)
+  int16_t* row_off;    // [E*O] row offsets (tensor-core path)
   float* part;      // [T*K, ncol, O] float32 partial results of every pair
   size_t bytes;     // total
 };
@@ -72,8 +75,11 @@ struct Workspace {
 // Offsets of every region for the given sizes; base == nullptr only sizes.
 // with_part = false: no partial-result buffer (ws->part = nullptr), for a
 // linear whose kernel writes something else (gate/up tiles).
+// tiles_F > 0: the tensor-core path runs gate/up tiles of F gate rows (the
+// tile modes then cover 64-row halves).
 bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
-                     int64_t K, int token_dtype, Workspace* ws, bool with_part = true);
+                     int64_t K, int token_dtype, Workspace* ws, bool with_part = true,
+                     int64_t tiles_F = 0);
 
 // Partial results per (pair, row) that the chosen linear kernel writes.
 int linear_partial_columns(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
@@ -134,7 +140,6 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16,
 
 // Prefill-regime grouped GEMM on the tensor cores (bf16 tokens).
 bool gemm_tc_supported(int64_t E, int64_t I, int64_t O);
-size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I);
 
 // Gate/up tiles for the SwiGLU expert (F > 0): the tensor-core kernel runs
 // the stacked gate/up projection (O = 2F rows, gate rows first) in tiles of
@@ -148,15 +153,41 @@ struct SwigluTiles {
 };
 bool gemm_tc_swiglu_supported(int64_t E, int64_t I, int64_t F);
 
-// zero_ids (P ints) or nullptr: also set to 0 (gate/up tiles).
-cudaError_t launch_gather_tokens(const void* x, const RoutePlan& plan, void* grouped,
-                                 int64_t T, int64_t I, int64_t K, int32_t* zero_ids,
-                                 cudaStream_t stream);
-cudaError_t launch_gemm_tc(const void* x, const uint8_t* packed, const uint8_t* scales,
-                           const RoutePlan& plan, void* grouped, float* part,
-                           unsigned long long* status, int64_t T, int64_t E, int64_t I,
-                           int64_t O, int64_t K, const SwigluTiles& swiglu,
-                           cudaStream_t stream, int counter_word = kMetaUnitCounter);
+// The B operand rows of the tensor-core kernel, in the routing lists'
+// (expert-grouped) order: f16 copies scaled per row by 2^sigma
+// (launch_group_tokens; tiles may then take the f16 operand mode), or plain
+// bf16 rows (every tile takes the bf16 mode).
+struct TcTokens {
+  const void* rows = nullptr;     // [nrows, I]
+  const int* sigma = nullptr;     // [nrows] (f16 rows)
+  bool f16 = false;
+  int64_t nrows = 0;
+};
+size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I);
+
+// xg[p] = f16(x[t] 2^sigma) for t = pair_list[p] / K (max |x_t| 2^sigma in
+// [2^14, 2^15)), sigma[p] its power of two; also resets the tensor-core
+// kernel's unit counters; zero_ids (T*K ints) or nullptr: also set to 0
+// (gate/up tiles).
+cudaError_t launch_group_tokens(const void* x, const RoutePlan& plan, __half* xg, int* sigma,
+                                int64_t T, int64_t I, int64_t K, int32_t* zero_ids,
+                                cudaStream_t stream);
+// Operand modes of the tensor-core kernel's row tiles (launch_tile_scan):
+// tile_mode [E][gemm_tc_row_tiles(O, F)] (1: f16 operands hold every weight
+// of the tile exactly) and row_off [E*O] (each weight row's offset r). With
+// null pointers every tile takes the bf16 mode.
+struct TcTileModes {
+  const uint8_t* tile_mode = nullptr;
+  const int16_t* row_off = nullptr;
+};
+int64_t gemm_tc_row_tiles(int64_t O, int64_t F);
+cudaError_t launch_tile_scan(const uint8_t* scales, int64_t E, int64_t I, int64_t O, int64_t F,
+                             uint8_t* tile_mode, int16_t* row_off, cudaStream_t stream);
+cudaError_t launch_gemm_tc(const TcTokens& tokens, const TcTileModes& modes, const uint8_t* packed,
+                           const uint8_t* scales, const RoutePlan& plan, float* part,
+                           unsigned long long* status, int64_t E, int64_t I, int64_t O,
+                           int64_t K, const SwigluTiles& swiglu, cudaStream_t stream,
+                           int counter_word = kMetaUnitCounter);
 
 // Argument checks shared by every routed-linear entry point (api.cu):
 // MXFP4EL_OK or the first error, in the order the public header documents.

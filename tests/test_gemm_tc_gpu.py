@@ -102,3 +102,55 @@ def test_more_experts_than_the_tensor_core_lists_take_the_gemv(monkeypatch):
     rows = np.arange(0, T, 37)
     want, absm, _ = oracle_rows(wl, rows=rows)
     assert_parity(out[torch.from_numpy(rows).cuda()], want, absm, wl.dtype, "E=600")
+
+
+def test_gemm_operand_modes_agree(monkeypatch):
+    # Scale bytes 118..124 let every tile take the f16 operands; the knob
+    # keeps the bf16 operands. Products are exact in both and accumulate in
+    # float32: the results agree with the oracle and with each other.
+    T, E, K, I, O = 256, 4, 2, 2880, 384
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, seed=77)
+    want, absm, _ = oracle_rows(wl)
+    out_f16 = run_gpu(wl)
+    monkeypatch.setenv("MXFP4EL_TC_MODE", "bf16")
+    out_bf16 = run_gpu(wl)
+    torch.cuda.synchronize()
+    assert wait_timeouts() == 0
+    assert_parity(out_f16, want, absm, wl.dtype, "f16 operands")
+    assert_parity(out_bf16, want, absm, wl.dtype, "bf16 operands")
+    same = float((out_f16 == out_bf16).float().mean())
+    print(f"[gemm modes] identical outputs: {same:.6f}")
+    assert same > 0.999
+
+
+@pytest.mark.parametrize("lo,hi", [(0, 255), (100, 140)])
+def test_gemm_wide_scale_spans_take_bf16_tiles(lo, hi):
+    # Rows whose scale bytes span more than 26 binades cannot be held exactly
+    # by f16 operands: their tiles take the bf16 mode. (0, 255): every tile;
+    # (100, 140): some rows span up to 40, most tiles mix both kinds of rows.
+    T, E, K, I, O = 96, 3, 2, 256, 260
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, scale_lo=lo, scale_hi=hi,
+                        seed=lo + hi)
+    # Keep every result inside the bf16 range (scale bytes up to 170: weights
+    # up to 6 * 2^43); the exhaustive scale tests cover the bytes beyond.
+    wl.scales.clamp_(2, 170)
+    out = run_gpu(wl)
+    torch.cuda.synchronize()
+    assert wait_timeouts() == 0
+    want, absm, _ = oracle_rows(wl)
+    assert_parity(out, want, absm, wl.dtype, f"scales {lo}..{hi}")
+
+
+def test_gemm_mixed_tiles_in_one_call():
+    # Expert 0's rows span 116..124 (f16 tiles), expert 1's rows one byte
+    # 90 and the rest 124 (bf16 tiles): one launch holds both modes.
+    T, E, K, I, O = 160, 2, 1, 512, 256
+    wl = workloads.make(T, E, K, I, O, dtype=torch.bfloat16, scale_lo=116, scale_hi=124,
+                        seed=5)
+    wl.scales[1, :, 0] = 90
+    sel = torch.from_numpy((np.arange(T) % 2).reshape(T, 1).astype(np.int32))
+    out = run_gpu(wl, sel=sel)
+    torch.cuda.synchronize()
+    assert wait_timeouts() == 0
+    want, absm, _ = oracle_rows(wl, sel=sel)
+    assert_parity(out, want, absm, wl.dtype, "mixed tiles")

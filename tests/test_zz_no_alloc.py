@@ -54,7 +54,7 @@ CASES = [
     (dict(T=40, E=24, K=4, I=320, O=200, dtype=torch.bfloat16, seed=73),
      {"MXFP4EL_ROUTE": "bucketer"}),
     # The tensor-core GEMM: 256 pairs over 4 experts (64 tokens per expert),
-    # grouped tokens and partial results in the array.
+    # the f16 token copy and partial results in the array.
     (dict(T=128, E=4, K=2, I=256, O=192, dtype=torch.bfloat16, seed=74),
      {"MXFP4EL_PATH": "gemm"}),
 ]
