@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--configs", default="all",
                     help="other workloads measured in the same run and reported under "
                          "'configs': 'all', 'none' or a comma-separated list")
+    ap.add_argument("--weights", choices=["plain", "prepared"], default="plain",
+                    help="weights as given (plain) or laid out once for the kernels before "
+                         "timing (prepared: mxfp4_expert_linear_prepare, load-time work)")
     ap.add_argument("--cpu-budget", type=float, default=6.0,
                     help="seconds of oracle time per workload for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -442,21 +445,36 @@ def measure_workload(name, args, lib, dev, rank, world):
     import torch
     import torch.distributed as dist
 
-    from mxfp4_routed_expert_route_gb300 import (_native, mxfp4_expert_linear, workloads,
+    from mxfp4_routed_expert_route_gb300 import (_native, mxfp4_expert_linear,
+                                                 mxfp4_expert_linear_prepared, prepare_weights,
+                                                 prepared_workspace_size, workloads,
                                                  workspace_size)
 
     wl = workloads.named(name)
     U = workloads.experts_touched(wl.sel, wl.E)
     d = wl.device_tensors(dev)
     out = torch.empty((wl.T, wl.O), dtype=wl.dtype, device=dev)
-    ws = torch.empty(max(1, workspace_size(wl.T, wl.E, wl.I, wl.O, wl.K, wl.dtype)),
-                     dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if args.weights == "prepared":
+        # Load-time work, before any timing: the weights laid out for the
+        # kernels once; every step then reads the prepared copy.
+        pw = prepare_weights(d["packed"], d["scales"])
+        ws = torch.empty(max(1, prepared_workspace_size(wl.T, wl.E, wl.I, wl.O, wl.K,
+                                                        wl.dtype)),
+                         dtype=torch.uint8, device=dev)
+
+        def call(x, sel, p, ys, o):
+            mxfp4_expert_linear_prepared(x, pw, sel, p, ys, out=o, workspace=ws)
+    else:
+        ws = torch.empty(max(1, workspace_size(wl.T, wl.E, wl.I, wl.O, wl.K, wl.dtype)),
+                         dtype=torch.uint8, device=dev)
+
+        def call(x, sel, p, ys, o):
+            mxfp4_expert_linear(x, d["packed"], d["scales"], sel, p, ys, out=o, workspace=ws)
 
     def step():
-        mxfp4_expert_linear(d["x"], d["packed"], d["scales"], d["sel"], d["p"],
-                            d["y_shared"], out=out, workspace=ws)
+        call(d["x"], d["sel"], d["p"], d["y_shared"], out)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -552,8 +570,7 @@ def measure_workload(name, args, lib, dev, rank, world):
             stream.wait_event(h2d_ev[b])
             if i >= 2:
                 stream.wait_event(d2h_ev[b])                # step i-2's result is read back
-            mxfp4_expert_linear(x_d, d["packed"], d["scales"], sel_d, p_d, ys_d, out=out_d,
-                                workspace=ws)
+            call(x_d, sel_d, p_d, ys_d, out_d)
             comp_ev[b].record(stream)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(comp_ev[b])
@@ -616,6 +633,9 @@ def measure_workload(name, args, lib, dev, rank, world):
         "value": value, "unit": unit, "ms_per_step": ms_step,
         "dtype": linear_dtype_label(wl, gemm),
         "config": workload_config(wl, U, world),
+        "weights_layout": ("prepared once before timing (mxfp4_expert_linear_prepare, "
+                           "load-time work)" if args.weights == "prepared"
+                           else "plain layout as given"),
         "linear": "tensor-core grouped GEMM" if gemm else "CUDA-core GEMV",
         "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)",
         "gbps": gbps, "tflops": tflops,

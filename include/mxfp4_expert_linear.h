@@ -179,6 +179,82 @@ int mxfp4_expert_linear_with_workspace(const void* latent_tokens,
                                        void* stream);
 
 /*
+ * Prepared weights -- a load-time copy of (packed_weights, scale_bytes) laid
+ * out for the kernels ("MoE Expert Kernels: Grouped Prefill and Mixed-Quant
+ * Compact Experts", section 2, the weight preparation built once at load
+ * time). It holds the same values; calls on it give the same bits as
+ * mxfp4_expert_linear on the plain layout.
+ *
+ * Layout (mtiles = ceil(O / 128), nk = ceil(G / 2), G = I / 32), one
+ * 4352-byte block per (expert e, 128-row tile mt, 64-wide K chunk kc) at
+ * byte ((e * mtiles + mt) * nk + kc) * 4352:
+ *   bytes 32 m .. 32 m + 31: row o = 128 mt + m, the packed bytes of groups
+ *     2kc and 2kc+1, the two 16-byte halves swapped when bit 2 of m is set;
+ *   bytes 4096 + 2 m, 4097 + 2 m: its scale bytes of those groups.
+ * Rows past O hold zero codes and the scale bytes of row O - 1; for odd G the
+ * missing group G holds zero codes and the scale byte of group G - 1. Then,
+ * each part starting 256-byte aligned: int16 [E][O] and uint8 [E][mtiles]
+ * values that the tensor-core kernel derives from the scale bytes (per-row
+ * offsets and per-tile flags of its exact f16 operand mode).
+ *
+ * mxfp4_expert_linear_prepared_bytes: bytes of the copy, or (size_t)-1 for
+ * invalid sizes or I > 15360 (the prepared calls' limit).
+ */
+size_t mxfp4_expert_linear_prepared_bytes(int64_t E, int64_t I, int64_t O);
+
+/*
+ * mxfp4_expert_linear_prepare -- writes the prepared copy of the weights into
+ * `prepared`, a caller-owned device buffer of at least `prepared_bytes`
+ * (>= mxfp4_expert_linear_prepared_bytes) bytes, 256-byte aligned, that
+ * overlaps neither input. Stream-ordered on `stream`; the kernels start only
+ * after earlier work on the stream has finished, so a buffer that an earlier
+ * call on the same stream still reads may be refilled. packed_weights must be
+ * 16-byte aligned. Returns MXFP4EL_OK, MXFP4EL_ERR_INVALID_ARGUMENT (null
+ * pointer, negative size, I % 32 != 0), MXFP4EL_ERR_TOO_LARGE,
+ * MXFP4EL_ERR_WORKSPACE (buffer too small or misaligned), MXFP4EL_ERR_ALIAS
+ * or MXFP4EL_ERR_CUDA. E == 0 or O == 0 enqueues nothing.
+ */
+int mxfp4_expert_linear_prepare(const uint8_t* packed_weights,
+                                const uint8_t* scale_bytes,
+                                int64_t E, int64_t I, int64_t O,
+                                void* prepared, size_t prepared_bytes,
+                                void* stream);
+
+/*
+ * mxfp4_expert_linear_prepared -- mxfp4_expert_linear on prepared weights:
+ * `prepared` (256-byte aligned, written by mxfp4_expert_linear_prepare for
+ * the same E, I, O) replaces packed_weights and scale_bytes; every other
+ * argument, the scratch and the errors are as mxfp4_expert_linear, plus
+ * MXFP4EL_ERR_TOO_LARGE for I > 15360. The _with_workspace form takes
+ * caller-owned scratch of mxfp4_expert_linear_prepared_workspace_size(...)
+ * bytes, as mxfp4_expert_linear_with_workspace does.
+ */
+int mxfp4_expert_linear_prepared(const void* latent_tokens,
+                                 const void* prepared,
+                                 const void* selected_experts,
+                                 const float* mixture_weights,
+                                 const void* shared_output,
+                                 void* out,
+                                 int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                                 int token_dtype, int index_dtype,
+                                 void* stream);
+size_t mxfp4_expert_linear_prepared_workspace_size(int64_t T, int64_t E, int64_t I,
+                                                   int64_t O, int64_t K,
+                                                   int token_dtype);
+int mxfp4_expert_linear_prepared_with_workspace(const void* latent_tokens,
+                                                const void* prepared,
+                                                const void* selected_experts,
+                                                const float* mixture_weights,
+                                                const void* shared_output,
+                                                void* out,
+                                                int64_t T, int64_t E, int64_t I,
+                                                int64_t O, int64_t K,
+                                                int token_dtype, int index_dtype,
+                                                void* workspace,
+                                                size_t workspace_bytes,
+                                                void* stream);
+
+/*
  * mxfp4_swiglu_expert -- the whole routed SwiGLU expert with MXFP4 weights
  * ("MoE Expert Kernels: Grouped Prefill and Mixed-Quant Compact Experts",
  * section 1, the expert shape: down(silu(gate(x)) * up(x)) per routed expert,

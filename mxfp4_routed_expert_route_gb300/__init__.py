@@ -22,7 +22,9 @@ from . import _native
 
 __all__ = ["mxfp4_expert_linear", "workspace_size", "device_errors", "wait_timeouts",
            "LibraryNotBuilt", "MXFP4Error", "router_topk", "mxfp4_expert_linear_routed",
-           "mxfp4_swiglu_expert", "swiglu_workspace_size"]
+           "mxfp4_swiglu_expert", "swiglu_workspace_size", "PreparedWeights",
+           "prepare_weights", "prepared_bytes", "mxfp4_expert_linear_prepared",
+           "prepared_workspace_size"]
 
 LibraryNotBuilt = _native.LibraryNotBuilt
 MXFP4Error = _native.MXFP4Error
@@ -106,6 +108,113 @@ def mxfp4_expert_linear(latent_tokens: torch.Tensor, packed_weights: torch.Tenso
             T, E, I, O, K, _TOKEN_DTYPES[x.dtype], _INDEX_DTYPES[sel.dtype],
             _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream))
     _native.check(rc, "mxfp4_expert_linear")
+    return out
+
+
+def prepared_bytes(E: int, I: int, O: int) -> int:
+    """Bytes of the prepared copy of (E, O, I/32) experts' weights."""
+    n = _native.load().mxfp4_expert_linear_prepared_bytes(E, I, O)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("sizes rejected by the library")
+    return n
+
+
+class PreparedWeights:
+    """The experts' weights laid out once for the kernels.
+
+    ``buffer`` is the uint8 device tensor the library wrote (see
+    ``mxfp4_expert_linear_prepare`` in the header for the layout); E, I, O
+    are the sizes it was prepared for.
+    """
+
+    def __init__(self, buffer: torch.Tensor, E: int, I: int, O: int):
+        self.buffer, self.E, self.I, self.O = buffer, E, I, O
+
+    @property
+    def device(self):
+        return self.buffer.device
+
+
+def prepare_weights(packed_weights: torch.Tensor, scale_bytes: torch.Tensor) -> PreparedWeights:
+    """Lay out packed_weights (E, O, I/32, 16) and scale_bytes (E, O, I/32)
+    for :func:`mxfp4_expert_linear_prepared`, on the current stream."""
+    w, s = packed_weights, scale_bytes
+    if not w.is_cuda or s.device != w.device:
+        raise ValueError("packed_weights and scale_bytes must be on one CUDA device")
+    if w.dtype != torch.uint8 or s.dtype != torch.uint8:
+        raise TypeError("packed_weights and scale_bytes must be uint8")
+    if w.dim() != 4 or s.dim() != 3 or w.shape[3] != 16 or tuple(s.shape) != tuple(w.shape[:3]):
+        raise ValueError("expected packed (E,O,G,16) and scales (E,O,G)")
+    E, O, G, _ = w.shape
+    I = 32 * G
+    w, s = w.contiguous(), s.contiguous()
+    nbytes = prepared_bytes(E, I, O)
+    buf = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=w.device)
+    stream = torch.cuda.current_stream(w.device).cuda_stream
+    with torch.cuda.device(w.device):
+        rc = _native.load().mxfp4_expert_linear_prepare(
+            _ptr(w), _ptr(s), E, I, O, _ptr(buf), buf.numel(), ctypes.c_void_p(stream))
+    _native.check(rc, "mxfp4_expert_linear_prepare")
+    return PreparedWeights(buf, E, I, O)
+
+
+def prepared_workspace_size(T: int, E: int, I: int, O: int, K: int,
+                            dtype: torch.dtype = torch.bfloat16) -> int:
+    """Bytes of scratch a call on prepared weights of these sizes needs."""
+    n = _native.load().mxfp4_expert_linear_prepared_workspace_size(
+        T, E, I, O, K, _TOKEN_DTYPES[dtype])
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("sizes rejected by the library")
+    return n
+
+
+def mxfp4_expert_linear_prepared(latent_tokens: torch.Tensor, prepared: PreparedWeights,
+                                 selected_experts: torch.Tensor,
+                                 mixture_weights: torch.Tensor, shared_output: torch.Tensor,
+                                 out: torch.Tensor | None = None,
+                                 workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """:func:`mxfp4_expert_linear` on weights from :func:`prepare_weights`:
+    the same result, bit for bit."""
+    x, sel, p, ys = latent_tokens, selected_experts, mixture_weights, shared_output
+    if not x.is_cuda:
+        raise ValueError("latent_tokens must be a CUDA tensor")
+    dev = x.device
+    for name, t in (("prepared", prepared.buffer), ("selected_experts", sel),
+                    ("mixture_weights", p), ("shared_output", ys)):
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, tokens on {dev}")
+    if x.dtype not in _TOKEN_DTYPES:
+        raise TypeError(f"unsupported token dtype {x.dtype}")
+    if ys.dtype != x.dtype:
+        raise TypeError("shared_output must have the token dtype")
+    if sel.dtype not in _INDEX_DTYPES:
+        raise TypeError(f"unsupported index dtype {sel.dtype}")
+    if p.dtype != torch.float32:
+        raise TypeError("mixture_weights must be float32")
+    if x.dim() != 2 or sel.dim() != 2:
+        raise ValueError("expected x (T,I) and sel (T,K)")
+    T, I = x.shape
+    E, O, K = prepared.E, prepared.O, sel.shape[1]
+    if I != prepared.I:
+        raise ValueError("the weights were prepared for another token width")
+    if tuple(sel.shape) != (T, K) or tuple(p.shape) != (T, K) or tuple(ys.shape) != (T, O):
+        raise ValueError("routing or shared-output shape mismatch")
+    x, sel, p, ys = (t.contiguous() for t in (x, sel, p, ys))
+    if out is None:
+        out = torch.empty((T, O), dtype=x.dtype, device=dev)
+    elif out.shape != (T, O) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous (T, O) tensor of the token dtype")
+    lib = _native.load()
+    ws_bytes = prepared_workspace_size(T, E, I, O, K, x.dtype)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        rc = lib.mxfp4_expert_linear_prepared_with_workspace(
+            _ptr(x), _ptr(prepared.buffer), _ptr(sel), _ptr(p), _ptr(ys), _ptr(out),
+            T, E, I, O, K, _TOKEN_DTYPES[x.dtype], _INDEX_DTYPES[sel.dtype],
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream))
+    _native.check(rc, "mxfp4_expert_linear_prepared")
     return out
 
 

@@ -65,6 +65,15 @@ SIGNATURES = {
     "mxfp4_swiglu_expert_with_workspace": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64,
                                                   _I64, _I64, _I64, _I64, _I64, _INT, _INT,
                                                   _P, _SZ, _P]),
+    "mxfp4_expert_linear_prepared_bytes": (_SZ, [_I64, _I64, _I64]),
+    "mxfp4_expert_linear_prepare": (_INT, [_P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "mxfp4_expert_linear_prepared": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                            _I64, _INT, _INT, _P]),
+    "mxfp4_expert_linear_prepared_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64,
+                                                          _INT]),
+    "mxfp4_expert_linear_prepared_with_workspace": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64,
+                                                           _I64, _I64, _I64, _INT, _INT, _P,
+                                                           _SZ, _P]),
 }
 
 _lock = threading.Lock()

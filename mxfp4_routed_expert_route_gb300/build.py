@@ -21,7 +21,7 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libmxfp4_expert_linear.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "route.cu", "gemv.cu", "gemm_tc.cu", "combine.cu", "static_scratch.cu",
-           "router.cu", "swiglu.cu"]
+           "router.cu", "swiglu.cu", "prepare.cu"]
 
 
 def nvcc() -> str:

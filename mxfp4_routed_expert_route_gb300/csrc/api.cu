@@ -86,6 +86,37 @@ int validate_linear(const void* x, const uint8_t* packed, const uint8_t* scales,
   return MXFP4EL_OK;
 }
 
+// The same checks for the call on prepared weights: the prepared copy
+// (mxfp4_expert_linear_prepared_bytes(E, I, O) bytes, 256-byte aligned) in
+// place of the packed weights and scale bytes.
+int validate_prepared(const void* x, const void* prepared, const void* sel, const float* p,
+                      const void* ys, void* out, int64_t T, int64_t E, int64_t I, int64_t O,
+                      int64_t K, int token_dtype, int index_dtype) {
+  if (token_dtype != MXFP4EL_DTYPE_F32 && token_dtype != MXFP4EL_DTYPE_BF16)
+    return MXFP4EL_ERR_UNSUPPORTED_DTYPE;
+  if (index_dtype != MXFP4EL_INDEX_I32 && index_dtype != MXFP4EL_INDEX_I64)
+    return MXFP4EL_ERR_UNSUPPORTED_DTYPE;
+  if (T < 0 || E < 0 || O < 0 || K < 0 || I <= 0 || I % 32 != 0)
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (!sizes_ok(T, E, I, O, K) || !gemv_uses_stream(I, true)) return MXFP4EL_ERR_TOO_LARGE;
+  if (T == 0 || O == 0) return MXFP4EL_OK;
+  if (ys == nullptr || out == nullptr) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (K > 0 && (x == nullptr || sel == nullptr || p == nullptr))
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (K > 0 && E > 0 && prepared == nullptr) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(prepared) % 256)
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  const size_t tb = token_dtype == MXFP4EL_DTYPE_BF16 ? 2 : 4;
+  const size_t ib = index_dtype == MXFP4EL_INDEX_I64 ? 8 : 4;
+  const size_t out_bytes = (size_t)T * O * tb;
+  const void* inputs[] = {x, prepared, sel, p, ys};
+  const size_t sizes[] = {(size_t)T * I * tb, prepared_bytes(E, I, O), (size_t)T * K * ib,
+                          (size_t)T * K * 4, (size_t)T * O * tb};
+  for (int i = 0; i < 5; ++i)
+    if (overlaps(out, out_bytes, inputs[i], sizes[i])) return MXFP4EL_ERR_ALIAS;
+  return MXFP4EL_OK;
+}
+
 LinearPath choose_path(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype) {
   const bool tc_ok = token_dtype == MXFP4EL_DTYPE_BF16 && E > 0 && gemm_tc_supported(E, I, O);
   // Test knob: MXFP4EL_PATH=gemv or gemm forces a kernel where it applies.
@@ -112,10 +143,12 @@ namespace {
 
 // Route and linear for K > 0: the float32 partial results land in ws.part
 // (linear_partial_columns() columns per pair).
+// prep: the weights as prepared blocks (packed and scales then unused).
 cudaError_t run_linear(const void* x, const uint8_t* packed, const uint8_t* scales,
                        const void* sel, int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
                        int token_dtype, int index_dtype, const Workspace& ws,
-                       cudaStream_t stream, const SwigluTiles& swiglu = SwigluTiles{}) {
+                       cudaStream_t stream, const SwigluTiles& swiglu = SwigluTiles{},
+                       const PreparedView* prep_w = nullptr) {
   unsigned long long* status = device_status_words();
   if (status == nullptr) return cudaErrorUnknown;
   if (E == 0) {
@@ -129,11 +162,13 @@ cudaError_t run_linear(const void* x, const uint8_t* packed, const uint8_t* scal
   }
   const bool gemm = choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
   // Small batches on the GEMV: each GEMV CTA routes for itself.
-  const bool self = !gemm && gemv_self_route(T, E, I, O, K);
-  const bool prep = !gemm && !self && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I);
+  const bool pw = prep_w != nullptr;
+  const bool self = !gemm && gemv_self_route(T, E, I, O, K, pw);
+  const bool prep =
+      !gemm && !self && token_dtype == MXFP4EL_DTYPE_BF16 && gemv_uses_stream(I, pw);
   const bool prep_in_route = prep && prep_fits_route(T, I);
   TokenPrep tp = {prep_in_route ? x : nullptr, ws.x16, ws.sigma, I};
-  const UnitSplit split = gemm ? UnitSplit{0, 0, 0, 1000} : gemv_unit_split(T, E, I, O, K);
+  const UnitSplit split = gemm ? UnitSplit{0, 0, 0, 1000} : gemv_unit_split(T, E, I, O, K, pw);
   mark(MXFP4EL_STAGE_ROUTE, true, stream);
   cudaError_t err = cudaSuccess;
   if (!self)
@@ -144,7 +179,8 @@ cudaError_t run_linear(const void* x, const uint8_t* packed, const uint8_t* scal
   if (err != cudaSuccess) return err;
   if (gemm) {
     mark(MXFP4EL_STAGE_GATHER, true, stream);
-    err = launch_tile_scan(scales, E, I, O, swiglu.F, ws.tile_mode, ws.row_off, stream);
+    // Prepared weights carry their tile modes and row offsets.
+    if (!pw) err = launch_tile_scan(scales, E, I, O, swiglu.F, ws.tile_mode, ws.row_off, stream);
     if (err == cudaSuccess)
       err = launch_group_tokens(x, ws.plan, ws.grouped, ws.gsigma, T, I, K, swiglu.sel2, stream);
     mark(MXFP4EL_STAGE_GATHER, false, stream);
@@ -158,13 +194,13 @@ cudaError_t run_linear(const void* x, const uint8_t* packed, const uint8_t* scal
     tok.f16 = true;
     tok.nrows = T * K;
     TcTileModes modes;
-    modes.tile_mode = ws.tile_mode;
-    modes.row_off = ws.row_off;
+    modes.tile_mode = pw ? prep_w->tile_mode : ws.tile_mode;
+    modes.row_off = pw ? prep_w->row_off : ws.row_off;
     err = launch_gemm_tc(tok, modes, packed, scales, ws.plan, ws.part, status, E, I, O, K, swiglu,
-                         stream);
+                         stream, kMetaUnitCounter, pw ? prep_w->blocks : nullptr);
   } else
     err = launch_gemv(x, token_dtype, ws.x16, ws.sigma, sel, index_dtype, packed, scales,
-                      ws.plan, ws.part, status, T, E, I, O, K, stream);
+                      ws.plan, ws.part, status, T, E, I, O, K, stream, prep_w);
   mark(MXFP4EL_STAGE_LINEAR, false, stream);
   return err;
 }
@@ -172,9 +208,10 @@ cudaError_t run_linear(const void* x, const uint8_t* packed, const uint8_t* scal
 int run(const void* x, const uint8_t* packed, const uint8_t* scales,
         const void* sel, const float* p, const void* ys, void* out, int64_t T,
         int64_t E, int64_t I, int64_t O, int64_t K, int token_dtype,
-        int index_dtype, const Workspace& ws, cudaStream_t stream) {
+        int index_dtype, const Workspace& ws, cudaStream_t stream,
+        const PreparedView* prep_w = nullptr) {
   if (K > 0 && run_linear(x, packed, scales, sel, T, E, I, O, K, token_dtype, index_dtype, ws,
-                          stream) != cudaSuccess)
+                          stream, SwigluTiles{}, prep_w) != cudaSuccess)
     return MXFP4EL_ERR_CUDA;
   mark(MXFP4EL_STAGE_COMBINE, true, stream);
   // With K > 0 and E > 0 a linear kernel of the library ran just before
@@ -377,7 +414,7 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
                      int64_t K, int token_dtype, Workspace* ws, bool with_part,
-                     int64_t tiles_F) {
+                     int64_t tiles_F, bool prepared) {
   const int64_t P = T * K;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -391,19 +428,21 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
   ws->plan.active = reinterpret_cast<int*>(take((size_t)E * sizeof(int)));
   ws->plan.pair_list = reinterpret_cast<int*>(take((size_t)P * sizeof(int)));
   const bool gemm = K > 0 && choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
-  const bool self = K > 0 && !gemm && gemv_self_route(T, E, I, O, K);
+  const bool self = K > 0 && !gemm && gemv_self_route(T, E, I, O, K, prepared);
   const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && K > 0 && !gemm && !self;
-  const bool prep_in_route = prep && gemv_uses_stream(I) && prep_fits_route(T, I);
+  const bool prep_in_route = prep && gemv_uses_stream(I, prepared) && prep_fits_route(T, I);
   const size_t wc_words = route_global_counter_words(T, K, E, prep_in_route);
   ws->wc_global = wc_words ? reinterpret_cast<int*>(take(wc_words * sizeof(int))) : nullptr;
   ws->x16 = prep ? reinterpret_cast<__half*>(take((size_t)T * I * sizeof(__half))) : nullptr;
   ws->sigma = prep ? reinterpret_cast<int*>(take((size_t)T * sizeof(int))) : nullptr;
   ws->grouped = gemm ? reinterpret_cast<__half*>(take(gemm_tc_grouped_bytes(T, K, I))) : nullptr;
   ws->gsigma = gemm ? reinterpret_cast<int*>(take((size_t)P * sizeof(int))) : nullptr;
-  ws->tile_mode = gemm ? reinterpret_cast<uint8_t*>(
+  // Prepared weights carry their own tile modes and row offsets.
+  const bool scan = gemm && !prepared;
+  ws->tile_mode = scan ? reinterpret_cast<uint8_t*>(
                              take((size_t)E * (size_t)gemm_tc_row_tiles(O, tiles_F)))
                        : nullptr;
-  ws->row_off = gemm ? reinterpret_cast<int16_t*>(take((size_t)E * O * sizeof(int16_t))) : nullptr;
+  ws->row_off = scan ? reinterpret_cast<int16_t*>(take((size_t)E * O * sizeof(int16_t))) : nullptr;
   ws->plan.unit_begin =
       K > 0 && !gemm ? reinterpret_cast<int*>(take((kMaxSplitCtas + 1) * sizeof(int))) : nullptr;
   const size_t ncol = (size_t)linear_partial_columns(T, E, I, O, K, token_dtype);
@@ -475,6 +514,89 @@ extern "C" int mxfp4_expert_linear(const void* latent_tokens,
   return run(latent_tokens, packed_weights, scale_bytes, selected_experts,
              mixture_weights, shared_output, out, T, E, I, O, K, token_dtype,
              index_dtype, ws, s);
+}
+
+extern "C" size_t mxfp4_expert_linear_prepared_bytes(int64_t E, int64_t I, int64_t O) {
+  if (E < 0 || O < 0 || I <= 0 || I % 32 != 0) return (size_t)-1;
+  if (!sizes_ok(0, E, I, O, 0) || !gemv_uses_stream(I, true)) return (size_t)-1;
+  return prepared_bytes(E, I, O);
+}
+
+extern "C" int mxfp4_expert_linear_prepare(const uint8_t* packed_weights,
+                                           const uint8_t* scale_bytes, int64_t E, int64_t I,
+                                           int64_t O, void* prepared, size_t prepared_bytes_,
+                                           void* stream) {
+  if (E < 0 || O < 0 || I <= 0 || I % 32 != 0) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (!sizes_ok(0, E, I, O, 0) || !gemv_uses_stream(I, true)) return MXFP4EL_ERR_TOO_LARGE;
+  if (E == 0 || O == 0) return MXFP4EL_OK;
+  if (packed_weights == nullptr || scale_bytes == nullptr || prepared == nullptr)
+    return MXFP4EL_ERR_INVALID_ARGUMENT;
+  if (reinterpret_cast<uintptr_t>(packed_weights) % 16) return MXFP4EL_ERR_INVALID_ARGUMENT;
+  const size_t need = prepared_bytes(E, I, O);
+  if (prepared_bytes_ < need || reinterpret_cast<uintptr_t>(prepared) % 256 != 0)
+    return MXFP4EL_ERR_WORKSPACE;
+  const size_t G = (size_t)I / 32;
+  if (overlaps(prepared, need, packed_weights, (size_t)E * O * G * 16) ||
+      overlaps(prepared, need, scale_bytes, (size_t)E * O * G))
+    return MXFP4EL_ERR_ALIAS;
+  return launch_prepare(packed_weights, scale_bytes, E, I, O, prepared,
+                        static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MXFP4EL_OK
+             : MXFP4EL_ERR_CUDA;
+}
+
+extern "C" int mxfp4_expert_linear_prepared_with_workspace(
+    const void* latent_tokens, const void* prepared, const void* selected_experts,
+    const float* mixture_weights, const void* shared_output, void* out, int64_t T, int64_t E,
+    int64_t I, int64_t O, int64_t K, int token_dtype, int index_dtype, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  int rc = validate_prepared(latent_tokens, prepared, selected_experts, mixture_weights,
+                             shared_output, out, T, E, I, O, K, token_dtype, index_dtype);
+  if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
+  Workspace ws;
+  carve_workspace(nullptr, T, E, I, O, K, token_dtype, &ws, true, 0, true);
+  if (workspace == nullptr || workspace_bytes < ws.bytes ||
+      reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return MXFP4EL_ERR_WORKSPACE;
+  carve_workspace(workspace, T, E, I, O, K, token_dtype, &ws, true, 0, true);
+  const PreparedView v = prepared_view(prepared, E, I, O);
+  return run(latent_tokens, nullptr, nullptr, selected_experts, mixture_weights, shared_output,
+             out, T, E, I, O, K, token_dtype, index_dtype, ws, static_cast<cudaStream_t>(stream),
+             &v);
+}
+
+extern "C" size_t mxfp4_expert_linear_prepared_workspace_size(int64_t T, int64_t E, int64_t I,
+                                                              int64_t O, int64_t K,
+                                                              int token_dtype) {
+  if (token_dtype != MXFP4EL_DTYPE_F32 && token_dtype != MXFP4EL_DTYPE_BF16)
+    return (size_t)-1;
+  if (T < 0 || E < 0 || O < 0 || K < 0 || I <= 0 || I % 32 != 0) return (size_t)-1;
+  if (!sizes_ok(T, E, I, O, K) || !gemv_uses_stream(I, true)) return (size_t)-1;
+  if (T == 0 || O == 0) return 0;
+  Workspace ws;
+  carve_workspace(nullptr, T, E, I, O, K, token_dtype, &ws, true, 0, true);
+  return ws.bytes;
+}
+
+extern "C" int mxfp4_expert_linear_prepared(const void* latent_tokens, const void* prepared,
+                                            const void* selected_experts,
+                                            const float* mixture_weights,
+                                            const void* shared_output, void* out, int64_t T,
+                                            int64_t E, int64_t I, int64_t O, int64_t K,
+                                            int token_dtype, int index_dtype, void* stream) {
+  int rc = validate_prepared(latent_tokens, prepared, selected_experts, mixture_weights,
+                             shared_output, out, T, E, I, O, K, token_dtype, index_dtype);
+  if (rc != MXFP4EL_OK || T == 0 || O == 0) return rc;
+  Workspace ws;
+  carve_workspace(nullptr, T, E, I, O, K, token_dtype, &ws, true, 0, true);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* base = nullptr;
+  rc = cached_workspace(ws.bytes, s, &base);
+  if (rc != MXFP4EL_OK) return rc;
+  carve_workspace(base, T, E, I, O, K, token_dtype, &ws, true, 0, true);
+  const PreparedView v = prepared_view(prepared, E, I, O);
+  return run(latent_tokens, nullptr, nullptr, selected_experts, mixture_weights, shared_output,
+             out, T, E, I, O, K, token_dtype, index_dtype, ws, s, &v);
 }
 
 extern "C" int mxfp4_router_topk(const float* router_logits, const float* router_bias,

@@ -38,19 +38,21 @@
 //   warp 0      producer of scales and packed weights (lane 0) and TMEM
 //               allocation; takes each next unit from the counter and hands
 //               its index to the other roles through a shared-memory ring
-//   warp 1      MMA issuer (the whole warp waits, one elected lane issues)
+//   warp 1      MMA issuer (the whole warp waits for each chunk's readiness,
+//               one elected lane issues)
 //   warp 2      per-expert lists at start
 //   warp 3      producer of token tiles (lane 0)
-//   warps 4-19  dequantize, in four teams of 4 warps: team t owns TMEM A
-//               buffer t and takes chunks t, t+4, ...; thread m decodes both
-//               groups of the chunk for weight row m
+//   warps 4-19  dequantize, in four teams of 4 warps: team t takes chunks t,
+//               t+4, ...; thread m decodes both groups of the chunk for
+//               weight row m into TMEM A buffer (chunk mod 4), once the
+//               chunk's token rows have landed and the buffer is free
 //   warps 20-23 epilogue: TMEM -> registers (mode scaling) -> shared memory
 //               (transposed) -> float32 partial results
 // Every wait is bounded; a role whose wait gives up records it, stops, and
 // the CTA still waits (bounded) for its own copies and MMAs before freeing
 // TMEM.
 //
-// Gate/up tiles (gemm_tc_kernel<SB, true>, the SwiGLU expert's stacked
+// Gate/up tiles (gemm_tc_kernel<true, false>, the SwiGLU expert's stacked
 // gate/up projection, 2F rows with the gate rows first): a tile's 128 rows
 // are 64 gate rows f0.. and the matching 64 up rows F + f0.. (two 64-row TMA
 // boxes into one stage, two scale spans), so the epilogue holds g and u of
@@ -75,26 +77,35 @@ constexpr int kTcThreads = 768;
 constexpr int kBM = 128;                    // weight rows per tile
 constexpr int kBK = 64;                     // K elements per chunk (two groups)
 constexpr int kNMax = 192;                  // token columns per block (TMEM accumulator width)
-constexpr int kABufs = 4;                   // TMEM A buffers (one per dequantizer team)
+constexpr int kABufs = 4;                   // TMEM A buffers: chunk c uses buffer c % kABufs
+constexpr int kTeams = 4;                   // dequantizer teams: chunk c goes to team c % kTeams
 constexpr int kStagesAMax = 16;             // packed-weight ring (from HBM)
-constexpr int kStagesBMax = 6;              // token stages, as shared memory allows
+constexpr int kStagesBMax = 8;              // token stages, as shared memory allows
 constexpr uint32_t kStageA = kBM * 32;      // packed bytes of a chunk, 32 B per row
+// A chunk block of the prepared layout: the chunk's packed bytes as the plain
+// layout's stage holds them, then two scale bytes per row (rows in order).
+constexpr uint32_t kStagePrep = kPrepBlockBytes;
+static_assert(kPrepRows == kBM && kPrepPackedBytes == kStageA, "prepared blocks are tiles");
 static_assert(kStageA % 1024 == 0, "stages keep 1024-byte alignment");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 0;               // two accumulators of kNMax columns
 constexpr uint32_t kACol = 2 * kNMax;       // kABufs A buffers of 32 columns
 static_assert(kACol + kABufs * 32 <= kTmemCols, "TMEM budget");
+// A chunk's A buffer is rewritten kABufs chunks later, once its MMAs are done;
+// the MMAs of the kABufs - 1 chunks between cover the dequantizer's wake-up,
+// TMEM stores and signal. (Measured: 192-column accumulators and 4 buffers
+// beat 160 columns and 6 buffers, 525 against 535 us at the prefill shape.)
 constexpr int kMaxExpertsTc = 512;          // per-expert lists kept in shared memory
 constexpr uint32_t kEpiStage = 16 * 32 * 4; // epilogue staging per warp: 16 columns x 32 rows
 constexpr int kUnitRing = 4;                // unit indices handed from producer A
 constexpr int kListWarp = 2, kProdBWarp = 3;
-constexpr int kNumLoads = kNMax / 16;       // token-box heights: 16, 32, ..., 192 rows
+constexpr int kNumLoads = kNMax / 16;       // token-box heights: 16, 32, ..., kNMax rows
 __host__ __device__ constexpr int load_rows(int l) { return 16 * (l + 1); }
 constexpr int kDequantWarp0 = 4, kDequantWarps = 16, kTeamWarps = 4, kEpiWarp0 = 20;
 // Readers of the unit ring, one arrival each: producer B (one thread), the
 // MMA warp, the dequantizer warps and the epilogue warps.
 constexpr int kUnitReaders = 2 + kDequantWarps + (kTcThreads / 32 - kEpiWarp0);
-static_assert(kDequantWarps == kABufs * kTeamWarps, "one team per A buffer");
+static_assert(kDequantWarps == kTeams * kTeamWarps, "four teams of four warps");
 // The widest span of scale bytes within one row that f16 operands hold
 // exactly: LUT values 0.5..6 times 2^d are normal f16 numbers for
 // -13 <= d <= 13.
@@ -109,7 +120,10 @@ struct TcArgs {
   const int* sigma;              // per grouped row: the power of two of its f16 copy
   int G, O, K;
   int mtiles;                    // ceil(O / 128) (or ceil(F / 64) for gate/up tiles)
-  int stages_a;
+  int stages_a;                  // packed-weight ring depth
+  int stages_b;                  // token ring depth (4 .. kStagesBMax)
+  uint32_t stage_a;              // bytes per packed-weight stage (kStageA, or kStagePrep)
+  const unsigned char* prep;     // prepared chunk blocks [E][mtiles][G/2], or null
   int nmax;                      // token columns per block (<= kNMax)
   uint32_t stage_b;              // bytes per token stage: nmax rows x 128 B
   uint32_t scale_cap;            // bytes per scale buffer
@@ -140,14 +154,19 @@ struct __align__(16) TcShared {
   uint64_t full_a[kStagesAMax], empty_a[kStagesAMax];
   // Chunk c uses token stage c % SB and TMEM A buffer c % kABufs.
   uint64_t b_full[kStagesBMax];  // the chunk's token rows have landed
-  uint64_t a_full[kABufs];       // A buffer written (and, for bf16 tiles on f16
-                                 // token rows, the chunk's token rows converted)
   uint64_t done[kStagesBMax];    // the chunk's MMAs finished: its stage and A buffer free
   uint64_t d_full[2], d_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t drain;
   uint64_t u_full[kUnitRing], u_empty[kUnitRing];
   int unit_ring[kUnitRing];      // unit indices in the order this CTA takes them; -1 ends
+  // Per A buffer: completes once the team's kTeamWarps warps have stored the
+  // chunk's A columns and seen its token rows land (and, for bf16 tiles on
+  // f16 token rows, converted them). One wait per chunk for the MMA warp,
+  // which suspends in the barrier: polling a counter instead kept 32 lanes
+  // spinning beside the dequantizer and epilogue warps of its sub-partition
+  // and measured 6 to 8 % slower.
+  uint64_t a_full[kABufs];
   uint32_t tmem_base;
   int scale_off[2];              // per scale buffer: offset of the tile's first byte, or -1
   int scale_off_up[2];           // per scale buffer: offset of the up rows' first byte
@@ -365,48 +384,48 @@ __device__ __forceinline__ bool elect_one() {
   return e != 0;
 }
 
-// A dequantizer team's place in the chunk sequence of its CTA: the global
-// index of its next chunk (chunks of earlier tiles included) and that
-// chunk's packed stage and phase.
-struct TeamPos {
-  int next;
-  int stage;
-  uint32_t stage_phase;
-};
-
 // The dequantizer's chunk loop for one tile whose chunks have global indices
 // base .. base+nk-1: thread m of team t decodes groups 2kc and 2kc+1 of row m
-// into A buffer t for each of the team's chunks kc. The packed tile arrives
-// with the 32-byte swizzle: the two 16-byte halves of row m are exchanged
-// when bit 2 of m is set, so eight consecutive rows read eight different
-// bank groups. scale(g) returns the row's scale byte of group g; f16 selects
+// into A buffer (base + kc) % kABufs for each of the team's chunks kc (those
+// with base + kc = t mod kTeams; `next` is the team's next global chunk).
+// Chunk c's packed bytes are in weight stage c % stages_a with the 32-byte
+// swizzle: the two 16-byte halves of row m are exchanged when bit 2 of m is
+// set, so eight consecutive rows read eight different bank groups. Scale
+// bytes: kPrep, the two after the packed bytes of the stage (row m at byte
+// kStageA + 2m); else scale(g), the row's scale byte of group g. f16 selects
 // the f16 decode with row offset r; convert: the chunk's token rows are f16
 // and this tile runs on bf16 operands. Returns false if a wait gave up.
-template <int SB, typename ScaleFn>
+template <bool kPrep, typename ScaleFn>
 __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* ring_a,
-                                             unsigned char* ring_b, uint32_t stage_b,
-                                             int stages_a, uint32_t tmem, uint32_t lane_base,
-                                             int team, int m, int lane, int tid, int base, int nk,
-                                             int nmma, TeamPos& tp, ScaleFn scale, bool f16,
-                                             int r, bool convert) {
+                                             uint32_t stage_a, int stages_a,
+                                             unsigned char* ring_b, uint32_t stage_b, int SB,
+                                             uint32_t tmem, uint32_t lane_base, int m, int lane,
+                                             int tid, int base, int nk, int nmma, int& next,
+                                             ScaleFn scale, bool f16, int r, bool convert) {
   const uint32_t sw = (uint32_t)(m >> 2) & 1u;
   const uint32_t off0 = (uint32_t)m * 32u + sw * 16u, off1 = (uint32_t)m * 32u + (sw ^ 1u) * 16u;
-  const uint32_t a_col = tmem + lane_base + kACol + (uint32_t)team * 32;
-  for (; tp.next < base + nk; tp.next += kABufs) {
-    const int kc = tp.next - base;
-    if (!mbar_wait_warp(&sh.full_a[tp.stage], tp.stage_phase)) return false;
-    const unsigned char* stage = ring_a + (size_t)tp.stage * kStageA;
+  const uint32_t a_cols = tmem + lane_base + kACol;
+  // The wait that frees this chunk's A buffer and token stage (see below).
+  const int back = min(SB, kABufs);
+  for (; next < base + nk; next += kTeams) {
+    const int kc = next - base;
+    const int sa = next % stages_a;
+    if (!mbar_wait_warp(&sh.full_a[sa], (uint32_t)(next / stages_a) & 1u)) return false;
+    const unsigned char* stage = ring_a + (size_t)sa * stage_a;
     const uint4 pk0 = *reinterpret_cast<const uint4*>(stage + off0);
     const uint4 pk1 = *reinterpret_cast<const uint4*>(stage + off1);
-    const uint32_t s0 = scale(2 * kc), s1 = scale(2 * kc + 1);
-    fence_proxy_async_smem();                             // before the refill's TMA writes
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.empty_a[tp.stage]);   // packed bytes consumed
-    tp.stage += kABufs;                                   // stages_a is a multiple of kABufs
-    if (tp.stage >= stages_a) {
-      tp.stage -= stages_a;
-      tp.stage_phase ^= 1u;
+    uint32_t s0, s1;
+    if constexpr (kPrep) {
+      const uint32_t s01 = *reinterpret_cast<const uint16_t*>(stage + kStageA + 2 * m);
+      s0 = s01 & 0xffu;
+      s1 = s01 >> 8;
+    } else {
+      s0 = scale(2 * kc);
+      s1 = scale(2 * kc + 1);
     }
+    fence_proxy_async_smem();                             // before the refill's copy lands
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty_a[sa]);         // packed bytes consumed
     uint32_t v0[16], v1[16];
     if (f16) {
       dequant_group_f16(pk0, s0, r, v0);
@@ -415,19 +434,27 @@ __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* 
       dequant_group_bf16(pk0, s0, v0);
       dequant_group_bf16(pk1, s1, v1);
     }
-    // The buffer is free once the MMAs of this team's previous chunk finished
-    // (chunk next - kABufs, whose token stage is (next - kABufs) % SB).
-    if (tp.next >= kABufs) {
-      const int pc = tp.next - kABufs;
+    // Wait for the MMAs of chunk pc = next - min(SB, kABufs). In-order MMA
+    // completion makes that cover what this chunk needs before its A columns
+    // may be written: A buffer next % kABufs was last used by chunk
+    // next - kABufs <= pc; chunk next - SB <= pc, which used this chunk's
+    // token stage, had its token rows landed, so the stage's barrier is now
+    // on this chunk's phase (a parity wait cannot tell that phase from an
+    // unfinished earlier one); and the barrier of pc's stage cannot have
+    // moved two phases past pc (its next use, pc + SB >= next, needs this
+    // chunk). The MMAs of the chunks in between cover the rest of this path.
+    // Then this chunk's token rows must have landed before the team reports
+    // it ready. bf16 tiles on f16 token rows: convert them in place, each of
+    // the team's 128 threads a share of the 16-byte pieces (f16 -> bf16 is
+    // exact for these values, which came from bf16), and make the writes
+    // visible to the tensor cores' reads.
+    if (next >= back) {
+      const int pc = next - back;
       if (!mbar_wait_warp(&sh.done[pc % SB], (uint32_t)(pc / SB) & 1u)) return false;
     }
-    // bf16 tiles on f16 token rows: once the chunk's rows have landed,
-    // convert them in place, each of the team's 128 threads a share of the
-    // 16-byte pieces (f16 -> bf16 is exact for these values, which came from
-    // bf16), then make the writes visible to the tensor cores' reads.
-    const int st = tp.next % SB;
+    const int st = next % SB;
+    if (!mbar_wait_warp(&sh.b_full[st], (uint32_t)(next / SB) & 1u)) return false;
     if (convert) {
-      if (!mbar_wait_warp(&sh.b_full[st], (uint32_t)(tp.next / SB) & 1u)) return false;
       uint4* sb_base = reinterpret_cast<uint4*>(ring_b + (size_t)st * stage_b);
       for (int i = tid; i < nmma * 8; i += kTeamWarps * 32) {
         uint4 v = sb_base[i];
@@ -443,13 +470,15 @@ __device__ __forceinline__ bool dequant_tile(TcShared& sh, const unsigned char* 
       fence_proxy_async_smem();
       __syncwarp();
     }
+    const uint32_t buf = (uint32_t)(next % kABufs);
+    const uint32_t a_col = a_cols + buf * 32;
     tc_fence_after_sync();
     tmem_st16(a_col, v0);
     tmem_st16(a_col + 16, v1);
     tmem_wait_st();
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.a_full[team]);
+    if (lane == 0) mbar_arrive(&sh.a_full[buf]);
   }
   return true;
 }
@@ -533,17 +562,21 @@ __device__ bool swiglu_epilogue(const TcArgs& a, const Unit& w, uint32_t d_cols,
   return true;
 }
 
-// kSplit: gate/up tiles of the SwiGLU expert (see TcArgs::F).
-template <int SB, bool kSplit>
+// kSplit: gate/up tiles of the SwiGLU expert (see TcArgs::F). kPrep: the
+// weights come as prepared chunk blocks (TcArgs::prep), one bulk copy per
+// chunk with the chunk's scale bytes inside, instead of tiled loads of the
+// packed rows and a copy of each tile's scale bytes.
+template <bool kSplit, bool kPrep>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
-  static_assert(SB >= kABufs && SB <= kStagesBMax, "token ring depth");
+  static_assert(!(kSplit && kPrep), "gate/up tiles read the plain layout");
+  const int SB = a.stages_b;     // token ring depth, kTeams .. kStagesBMax (checked by the host)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // Token stages need 1024-byte alignment (128-byte swizzle atoms).
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* ring_b = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   unsigned char* ring_a = ring_b + (size_t)SB * a.stage_b;
-  unsigned char* scale_buf = ring_a + (size_t)a.stages_a * kStageA;
+  unsigned char* scale_buf = ring_a + (size_t)a.stages_a * a.stage_a;
   TcShared& sh = *reinterpret_cast<TcShared*>(scale_buf + 2 * a.scale_cap);
   float* epi_stage = reinterpret_cast<float*>(&sh + 1);   // 16-byte aligned (TcShared is)
 
@@ -638,6 +671,23 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         next = atomicAdd(counter, 1);
         const Unit w = unit_at<kSplit>(a, sh, idx);
         if (w.ntok <= 0) { --it; continue; }
+        if constexpr (kPrep) {
+          // The tile's chunk blocks are consecutive: one bulk copy each.
+          const unsigned char* blk =
+              a.prep + ((size_t)w.e * a.mtiles + w.mt) * (size_t)nk * kStagePrep;
+          for (int kc = 0; kc < nk; ++kc, ++issued) {
+            if (!mbar_wait(&sh.empty_a[pa.idx], pa.phase ^ 1u)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sh.full_a[pa.idx], kStagePrep);
+            bulk_copy_g2s(ring_a + (size_t)pa.idx * kStagePrep, blk + (size_t)kc * kStagePrep,
+                          kStagePrep, &sh.full_a[pa.idx], pol);
+            pa.next(a.stages_a);
+          }
+          if (!ok) break;
+          continue;
+        }
         // The tile's scale bytes, by one bulk copy of the aligned span that
         // holds them when it stays inside the scales buffer.
         const int sb = it & 1;
@@ -695,8 +745,9 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         if (idx < 0) { idx += a.stages_a; ph ^= 1u; }
         if (!mbar_wait(&sh.full_a[idx], ph)) break;
       }
-      for (int k = max(0, it - 2); k < it; ++k)
-        if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)(k >> 1) & 1u)) break;
+      if constexpr (!kPrep)
+        for (int k = max(0, it - 2); k < it; ++k)
+          if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)(k >> 1) & 1u)) break;
     }
     __syncwarp();
   } else if (warp == kProdBWarp) {
@@ -741,7 +792,8 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     // synchronisation bracketed by the tcgen05 fences: the issuing lane
     // fences before the warp synchronises, every lane after its waits.
     int it = 0, idx;
-    RingPos pr, pb, pu;               // A buffer, token stage, unit ring
+    uint32_t chunk = 0;               // chunks issued so far: chunk c uses A buffer c % kABufs
+    RingPos pb, pu;                   // token stage, unit ring
     for (; ok; ++it) {
       if (!pop_unit<true>(sh, pu, lane, &idx)) { ok = false; break; }
       if (idx < 0) break;
@@ -753,14 +805,17 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const uint32_t d_tmem = tmem + kDCol + (uint32_t)db * kNMax;
       const uint32_t idesc = mma_idesc(kBM, w.nmma, tile_f16(a, w));
       for (int kc = 0; kc < nk; ++kc) {
-        if (!mbar_wait(&sh.b_full[pb.idx], pb.phase) ||
-            !mbar_wait(&sh.a_full[pr.idx], pr.phase)) {
+        // Ready once all kTeamWarps warps of the team arrived for this
+        // chunk: a warp arrives for its next chunk in this buffer only after
+        // these MMAs finished, so the barrier cannot run a phase ahead.
+        const uint32_t buf = chunk % kABufs;
+        if (!mbar_wait(&sh.a_full[buf], (chunk / kABufs) & 1u)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t b_addr = smem_addr(ring_b + (size_t)pb.idx * a.stage_b);
-        const uint32_t a_tmem = tmem + kACol + (uint32_t)pr.idx * 32;
+        const uint32_t a_tmem = tmem + kACol + buf * 32;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
@@ -771,7 +826,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
           tc_fence_before_sync();
         }
         __syncwarp();
-        pr.next(kABufs);
+        ++chunk;
         pb.next(SB);
       }
       if (!ok) break;
@@ -788,7 +843,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     const int q = warp & 3;                          // TMEM lane quarter
     const int m = 32 * q + lane;                     // weight row in the tile
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    TeamPos tp{team, team, 0u};                      // chunk `team` is the team's first
+    int next = team;                                 // chunk `team` is the team's first
     int it = 0, base = 0, idx;
     RingPos pu;
     for (; ok; ++it) {
@@ -797,7 +852,10 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const Unit w = unit_at<kSplit>(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int sb = it & 1;
-      if (!mbar_wait_warp(&sh.s_full[sb], (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
+      if (!kPrep && !mbar_wait_warp(&sh.s_full[sb], (uint32_t)(it >> 1) & 1u)) {
+        ok = false;
+        break;
+      }
       // Row m's place in its span: gate/up tiles hold two spans of rows
       // (m < 64: gate row f0 + m; else up row F + f0 + m - 64).
       const bool up = kSplit && m >= kBM / 2;
@@ -806,27 +864,36 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const int r = f16 ? a.row_off[(size_t)w.e * O + (up ? a.F : 0) + w.m0 + hrow] : 0;
       const bool convert = !f16 && a.b_f16 != 0;     // bf16 tile on f16 token rows
       const int tid = (sub % kTeamWarps) * 32 + lane;
-      const int soff = up ? sh.scale_off_up[sb] : sh.scale_off[sb];
-      // The choice of scale source is the same for the whole tile: take it
-      // once, so the chunk loop holds no global load.
-      if (soff >= 0) {
-        const unsigned char* srow =
-            scale_buf + (size_t)sb * a.scale_cap + soff + (size_t)hrow * G;
-        ok = dequant_tile<SB>(sh, ring_a, ring_b, a.stage_b, a.stages_a, tmem, lane_base, team,
-                              m, lane, tid, base, nk, w.nmma, tp,
-                              [&](int g) { return (uint32_t)srow[g]; }, f16, r, convert);
+      if constexpr (kPrep) {
+        ok = dequant_tile<true>(sh, ring_a, a.stage_a, a.stages_a, ring_b, a.stage_b, SB, tmem,
+                                lane_base, m, lane, tid, base, nk, w.nmma, next,
+                                [](int) { return 0u; }, f16, r, convert);
       } else {
-        const uint8_t* grow =
-            a.scales + ((size_t)w.e * O + (up ? a.F : 0) + w.m0 + hrow) * G;
-        ok = dequant_tile<SB>(sh, ring_a, ring_b, a.stage_b, a.stages_a, tmem, lane_base, team,
-                              m, lane, tid, base, nk, w.nmma, tp,
-                              [&](int g) { return (uint32_t)__ldg(grow + g); }, f16, r, convert);
+        // The choice of scale source is the same for the whole tile: take it
+        // once, so the chunk loop holds no global load.
+        const int soff = up ? sh.scale_off_up[sb] : sh.scale_off[sb];
+        if (soff >= 0) {
+          const unsigned char* srow =
+              scale_buf + (size_t)sb * a.scale_cap + soff + (size_t)hrow * G;
+          ok = dequant_tile<false>(sh, ring_a, a.stage_a, a.stages_a, ring_b, a.stage_b, SB, tmem,
+                                   lane_base, m, lane, tid, base, nk, w.nmma, next,
+                                   [&](int g) { return (uint32_t)srow[g]; }, f16, r, convert);
+        } else {
+          const uint8_t* grow =
+              a.scales + ((size_t)w.e * O + (up ? a.F : 0) + w.m0 + hrow) * G;
+          ok = dequant_tile<false>(sh, ring_a, a.stage_a, a.stages_a, ring_b, a.stage_b, SB, tmem,
+                                   lane_base, m, lane, tid, base, nk, w.nmma, next,
+                                   [&](int g) { return (uint32_t)__ldg(grow + g); }, f16, r,
+                                   convert);
+        }
       }
       base += nk;
       if (!ok) break;
-      fence_proxy_async_smem();                      // scale bytes read: the next copy may land
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
+      if constexpr (!kPrep) {
+        fence_proxy_async_smem();                    // scale bytes read: the next copy may land
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
+      }
     }
     if (!ok && lane == 0) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
   } else if (warp >= kEpiWarp0) {
@@ -1076,31 +1143,36 @@ int num_sms_tc() {
   return cached[dev];
 }
 
-size_t tc_shared_bytes(int stages_a, int stages_b, uint32_t stage_b, uint32_t scale_cap) {
-  return 1024 + (size_t)stages_b * stage_b + (size_t)stages_a * kStageA + 2 * (size_t)scale_cap +
+size_t tc_shared_bytes(int stages_a, uint32_t stage_a, int stages_b, uint32_t stage_b,
+                       uint32_t scale_cap) {
+  return 1024 + (size_t)stages_b * stage_b + (size_t)stages_a * stage_a + 2 * (size_t)scale_cap +
          sizeof(TcShared) + (kTcThreads / 32 - kEpiWarp0) * (size_t)kEpiStage;
 }
 
 constexpr size_t kSmemLimit = 227 * 1024;
 
 // Ring sizes and block width for one launch: as many token stages (up to
-// kStagesBMax, at least 4) of the widest block (192, else 128 token columns)
-// as fit beside eight packed-weight stages, then as deep a packed-weight ring
-// as shared memory allows (a multiple of kABufs: each dequantizer team keeps
-// to its own stages). Returns false if nothing fits.
+// kStagesBMax, at least kTeams) of the widest block (kNMax, else 128 token
+// columns) as fit beside eight packed-weight stages of stage_a bytes, then as
+// deep a packed-weight ring as shared memory allows (a multiple of kTeams:
+// each dequantizer team keeps to its own stages, so the last use of a stage
+// is always its own). Token refills wait for the MMAs of the chunk SB back,
+// so the token ring's depth is what hides their latency. Returns false if
+// nothing fits.
 struct TcConfig {
   int nmax;
   int stages_b;
   int stages_a;
   uint32_t stage_b;
 };
-bool tc_config(uint32_t scale_cap, TcConfig* c) {
+bool tc_config(uint32_t scale_cap, uint32_t stage_a, TcConfig* c) {
   for (int nmax : {kNMax, 128}) {
     const uint32_t sbytes = (uint32_t)nmax * 128u;
-    for (int sb = kStagesBMax; sb >= 4; --sb) {
-      if (tc_shared_bytes(2 * kABufs, sb, sbytes, scale_cap) > kSmemLimit) continue;
+    for (int sb = kStagesBMax; sb >= kTeams; --sb) {
+      if (tc_shared_bytes(2 * kTeams, stage_a, sb, sbytes, scale_cap) > kSmemLimit) continue;
       int sa = kStagesAMax;
-      while (sa > kABufs && tc_shared_bytes(sa, sb, sbytes, scale_cap) > kSmemLimit) sa -= kABufs;
+      while (sa > kTeams && tc_shared_bytes(sa, stage_a, sb, sbytes, scale_cap) > kSmemLimit)
+        sa -= kTeams;
       *c = TcConfig{nmax, sb, sa, sbytes};
       return true;
     }
@@ -1108,7 +1180,7 @@ bool tc_config(uint32_t scale_cap, TcConfig* c) {
   return false;
 }
 
-template <int SB, bool kSplit>
+template <bool kSplit, bool kPrep>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& args, size_t smem, cudaStream_t stream) {
   static std::mutex mu;
   static size_t opted[64] = {};
@@ -1117,17 +1189,19 @@ cudaError_t launch_tc(const TcMaps& maps, const TcArgs& args, size_t smem, cudaS
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && opted[dev] < smem) {
-      cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel<SB, kSplit>,
+      cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel<kSplit, kPrep>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (err != cudaSuccess) return err;
       opted[dev] = smem;
     }
   }
-  return launch_after_previous(gemm_tc_kernel<SB, kSplit>, dim3((unsigned)num_sms_tc()),
+  return launch_after_previous(gemm_tc_kernel<kSplit, kPrep>, dim3((unsigned)num_sms_tc()),
                                dim3(kTcThreads), smem, stream, maps, args);
 }
 
 }  // namespace
+
+void* tensor_map_encoder() { return reinterpret_cast<void*>(encode_fn()); }
 
 cudaError_t launch_group_tokens(const void* x, const RoutePlan& plan, __half* xg, int* sigma,
                                 int64_t T, int64_t I, int64_t K, int32_t* zero_ids,
@@ -1148,13 +1222,15 @@ int64_t gemm_tc_row_tiles(int64_t O, int64_t F) {
   return F > 0 ? (F + kBM / 2 - 1) / (kBM / 2) : (O + kBM - 1) / kBM;
 }
 
+bool tile_scan_fits(int64_t I) { return (size_t)kBM * (I / 32) + 64 <= 48 * 1024; }
+
 cudaError_t launch_tile_scan(const uint8_t* scales, int64_t E, int64_t I, int64_t O, int64_t F,
                              uint8_t* tile_mode, int16_t* row_off, cudaStream_t stream) {
   const int64_t mtiles = gemm_tc_row_tiles(O, F);
   if (E <= 0 || mtiles <= 0) return cudaSuccess;
   const dim3 grid((unsigned)mtiles, (unsigned)E);
   const size_t smem = (size_t)kBM * (I / 32) + 64;   // a tile's scale bytes, two windows
-  if (smem > 48 * 1024) return cudaErrorInvalidValue;
+  if (!tile_scan_fits(I)) return cudaErrorInvalidValue;
   if (F > 0)
     return launch_after_previous(tile_scan_kernel<true>, grid, dim3(128), smem, stream, scales,
                                  (int)(I / 32), (int)O, (int)F, (int)mtiles, tile_mode, row_off);
@@ -1174,32 +1250,36 @@ bool gemm_tc_supported(int64_t E, int64_t I, int64_t O) {
   if (G % 2 != 0) return false;                    // chunks of whole group pairs
   if (E > kMaxExpertsTc || E * O > 0x7fffffff) return false;
   TcConfig c;
-  return tc_config(tc_scale_cap(G, false), &c);
+  return tc_config(tc_scale_cap(G, false), kStageA, &c) && tc_config(0u, kStagePrep, &c);
 }
 
 bool gemm_tc_swiglu_supported(int64_t E, int64_t I, int64_t F) {
   TcConfig c;
   return F > 0 && F % 32 == 0 && gemm_tc_supported(E, I, 2 * F) &&
-         tc_config(tc_scale_cap(I / 32, true), &c);
+         tc_config(tc_scale_cap(I / 32, true), kStageA, &c);
 }
 
 cudaError_t launch_gemm_tc(const TcTokens& tok, const TcTileModes& modes, const uint8_t* packed,
                            const uint8_t* scales, const RoutePlan& plan, float* part,
                            unsigned long long* status, int64_t E, int64_t I, int64_t O,
                            int64_t K, const SwigluTiles& swiglu, cudaStream_t stream,
-                           int counter_word) {
+                           int counter_word, const uint8_t* prepared) {
   if (swiglu.F > 0 && (O != 2 * swiglu.F || !gemm_tc_swiglu_supported(E, I, swiglu.F)))
     return cudaErrorInvalidValue;
+  const bool prep = prepared != nullptr;
+  if (prep && swiglu.F > 0) return cudaErrorInvalidValue;
   const int64_t G = I / 32;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   TcConfig cfg;
-  const uint32_t scale_cap = tc_scale_cap(G, swiglu.F > 0);
-  if (!tc_config(scale_cap, &cfg)) return cudaErrorInvalidValue;
+  const uint32_t scale_cap = prep ? 0u : tc_scale_cap(G, swiglu.F > 0);
+  const uint32_t stage_a = prep ? kStagePrep : kStageA;
+  if (!tc_config(scale_cap, stage_a, &cfg)) return cudaErrorInvalidValue;
 
-  // Tensor maps.
+  // Tensor maps (the prepared layout needs none for the weights).
   TcMaps maps;
-  {
+  std::memset(&maps, 0, sizeof(maps));
+  if (!prep) {
     const cuuint64_t dims[2] = {(cuuint64_t)(G * 16), (cuuint64_t)(E * O)};
     const cuuint64_t strides[1] = {(cuuint64_t)(G * 16)};
     const cuuint32_t box[2] = {32, (cuuint32_t)kBM};
@@ -1228,8 +1308,10 @@ cudaError_t launch_gemm_tc(const TcTokens& tok, const TcTileModes& modes, const 
 
   TcArgs args;
   args.plan = plan;
-  args.scales = scales;
-  args.scales_end = scales + (size_t)E * O * G;
+  args.scales = prep ? nullptr : scales;
+  args.scales_end = prep ? nullptr : scales + (size_t)E * O * G;
+  args.prep = prepared;
+  args.stage_a = stage_a;
   args.part = part;
   args.status = status;
   args.sigma = tok.sigma;
@@ -1253,18 +1335,12 @@ cudaError_t launch_gemm_tc(const TcTokens& tok, const TcTileModes& modes, const 
   args.nmax = cfg.nmax;
   args.stage_b = cfg.stage_b;
   args.stages_a = cfg.stages_a;
-  const size_t smem = tc_shared_bytes(cfg.stages_a, cfg.stages_b, cfg.stage_b, scale_cap);
-  switch (cfg.stages_b) {
-    case 6:
-      return swiglu.F > 0 ? launch_tc<6, true>(maps, args, smem, stream)
-                          : launch_tc<6, false>(maps, args, smem, stream);
-    case 5:
-      return swiglu.F > 0 ? launch_tc<5, true>(maps, args, smem, stream)
-                          : launch_tc<5, false>(maps, args, smem, stream);
-    default:
-      return swiglu.F > 0 ? launch_tc<4, true>(maps, args, smem, stream)
-                          : launch_tc<4, false>(maps, args, smem, stream);
-  }
+  args.stages_b = cfg.stages_b;
+  const size_t smem =
+      tc_shared_bytes(cfg.stages_a, stage_a, cfg.stages_b, cfg.stage_b, scale_cap);
+  if (prep) return launch_tc<false, true>(maps, args, smem, stream);
+  return swiglu.F > 0 ? launch_tc<true, false>(maps, args, smem, stream)
+                      : launch_tc<false, false>(maps, args, smem, stream);
 }
 
 }  // namespace mxfp4el

@@ -35,6 +35,8 @@
 //
 // gemv_direct_kernel: the same arithmetic in float32 straight from global
 // memory (no staging), for rows too wide for a shared-memory stage.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include <cstdlib>
@@ -196,6 +198,19 @@ struct StreamArgs {
   // time from *pool once their own range is done.
   int static_permille;
   int* pool;                     // claim counter (workspace), reset by CTA 0
+  // Stage layout. Plain weights: header at 0, the tile's packed rows (16 G
+  // bytes each) at 128, its scale span after them. Prepared weights (prep):
+  // one slab per K chunk of rows_per_tile rows x 32 bytes (groups 2kc and
+  // 2kc+1 of a row, in that order) at pk_off = 0, one slab per chunk of 2
+  // scale bytes per row at sc_off, the header at hdr_off; tiles then never
+  // cross a 128-row block of the layout (rows_per_tile divides 128).
+  int prep;
+  int mtiles, nk;                // prepared: 128-row tiles per expert, K chunks
+  uint32_t hdr_off, pk_off, sc_off;
+  uint32_t prow;                 // stage bytes between a group's rows: 16 G, or 32
+  uint32_t srow;                 // stage bytes between a scale's rows: G, or 2
+  CUtensorMap pmap;              // prepared: packed slabs, box {32, rows_per_tile, nk}
+  CUtensorMap smap;              // prepared: scale slabs, box {2 rows_per_tile, nk}
 };
 
 // Written by the producer into each stage before its copies are issued.
@@ -500,7 +515,7 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
   constexpr int V = Pow2Ceil<RWS * NTA>::value;
   constexpr int L = Log2<V>::value;
   const int G = a.G, O = a.O;
-  const uint32_t prow = (uint32_t)G * 16u;      // bytes per packed row
+  const uint32_t prow = a.prow;                  // stage bytes between rows
   const float2* lut = scale_lut();
   float acc[V];
 #pragma unroll
@@ -520,7 +535,7 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
       for (int j = 0; j < NTA; ++j) acc[r * NTA + j] = apply_scale(xt[j].dot(w), sb, lut + soff[j]);
     }
     pa += prow;
-    sa += (uint32_t)G;
+    sa += a.srow;
     if (!kScalesStaged) ga += G;
   }
   const float total = warp_reduce_scatter<V>(acc, lane);
@@ -593,13 +608,17 @@ __device__ __forceinline__ void load_pass(const StreamArgs& a, const SelfPlan& s
 
 template <typename Elem, int RWS, int NT, bool kSelf>
 __global__ void __launch_bounds__(kStreamThreads, 1)
-gemv_stream_kernel(const StreamArgs a) {
+gemv_stream_kernel(const __grid_constant__ StreamArgs a) {
   static_assert(NT == 1 || NT == 2, "one or two tokens per pass");
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
   unsigned char* route_area = smem + kStreamHeadBytes;
   unsigned char* stage_base = route_area + (kSelf ? a.route_bytes : 0u);
+  // Prepared weights arrive through the 32-byte swizzle, whose pattern
+  // follows the shared-memory address: stages start 1024-byte aligned (the
+  // launch adds the slack).
+  if (a.prep) stage_base += (1024u - (smem_addr(stage_base) & 1023u)) & 1023u;
   const SelfPlan rp = self_plan(route_area, a.E, a.P, a.T);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -679,7 +698,7 @@ gemv_stream_kernel(const StreamArgs a) {
       }
       if (unit < 0) {
         if (!mbar_wait(&empty[st], (round & 1u) ^ 1u)) { ok = false; break; }
-        reinterpret_cast<StageHeader*>(stage_base + (size_t)st * a.stage_bytes)->e = -1;
+        reinterpret_cast<StageHeader*>(stage_base + (size_t)st * a.stage_bytes + a.hdr_off)->e = -1;
         mbar_arrive(&full[st]);
         ++issued;
         break;
@@ -688,6 +707,27 @@ gemv_stream_kernel(const StreamArgs a) {
       if (u != cached_u) { e = kSelf ? rp.active[u] : a.plan.active[u]; cached_u = u; }
       const int o0 = tile * a.rows_per_tile;
       const int rows = min(a.rows_per_tile, O - o0);
+      if (a.prep) {
+        // The tile's slabs: packed rows o0 % 128 .. of every K chunk of
+        // 128-row tile o0 / 128, and their scale bytes. The swizzled load
+        // undoes the layout's swap of 16-byte halves (bit 2 of the row is
+        // bit 7 of the stage address), so a slab row holds groups 2kc,
+        // 2kc+1 in order.
+        if (!mbar_wait(&empty[st], (round & 1u) ^ 1u)) { ok = false; break; }
+        unsigned char* dst = stage_base + (size_t)st * a.stage_bytes;
+        StageHeader* h = reinterpret_cast<StageHeader*>(dst + a.hdr_off);
+        h->e = e;
+        h->o0 = o0;
+        h->rows = rows;
+        h->scale_off = 0;
+        const int blk = (e * a.mtiles + o0 / kPrepRows) * a.nk;
+        const int r0 = o0 % kPrepRows;
+        const uint32_t pbytes = (uint32_t)a.nk * (uint32_t)a.rows_per_tile * 32u;
+        const uint32_t sbytes = (uint32_t)a.nk * (uint32_t)a.rows_per_tile * 2u;
+        mbar_arrive_expect_tx(&full[st], pbytes + sbytes);     // releases the header
+        tma_load_3d(dst + a.pk_off, &a.pmap, 0, r0, blk, &full[st], policy);
+        tma_load_2d(dst + a.sc_off, &a.smap, 2 * r0, blk, &full[st], policy);
+      } else {
       const size_t row0 = (size_t)e * O + o0;
       const uint32_t pbytes = (uint32_t)rows * G * 16;
       // The tile's scale bytes: copy the 16-byte-aligned span that holds
@@ -711,6 +751,7 @@ gemv_stream_kernel(const StreamArgs a) {
       if (sbytes)
         bulk_copy_g2s(dst + sizeof(StageHeader) + a.packed_stage_bytes,
                       reinterpret_cast<const void*>(c_lo), sbytes, &full[st], policy);
+      }
       ++unit;                       // past uend (pool units lie after every range): claim
       // Slow start: the first stage goes out alone and lands before the
       // rest of the ring is requested. With every CTA's whole ring
@@ -769,11 +810,11 @@ gemv_stream_kernel(const StreamArgs a) {
     }
     const unsigned char* hp = stage_base + (size_t)st * a.stage_bytes;
     // The header in one 16-byte load: expert, first row, rows, scale offset.
-    const int4 hv = *reinterpret_cast<const int4*>(hp);
+    const int4 hv = *reinterpret_cast<const int4*>(hp + a.hdr_off);
     const int e = hv.x;
     if (e < 0) break;
     const int o0 = hv.y, rows = hv.z, scale_off = hv.w;
-    const unsigned char* sp = hp + sizeof(StageHeader);
+    const unsigned char* sp = hp + a.pk_off;
 
     if (working && rbase < rows) {
       if (e != cached_e) {                    // new expert: its first pass
@@ -782,11 +823,17 @@ gemv_stream_kernel(const StreamArgs a) {
         seg_end = kSelf ? rp.off[e + 1] : a.plan.offsets[e + 1];
         load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, g);
       }
-      // This lane's group in row rbase of the tile: packed bytes and scale.
+      // This lane's group in row rbase of the tile: packed bytes and scale
+      // (prepared: in the slab of chunk gc / 2, half gc % 2 of the row).
+      const uint32_t rpt = (uint32_t)a.rows_per_tile;
       const uint32_t sp_lane =
-          smem_addr(sp) + ((uint32_t)rbase * (uint32_t)G + (uint32_t)gc) * 16u;
+          a.prep ? smem_addr(sp) + ((uint32_t)gc >> 1) * rpt * 32u + (uint32_t)rbase * 32u +
+                       ((uint32_t)gc & 1u) * 16u
+                 : smem_addr(sp) + ((uint32_t)rbase * (uint32_t)G + (uint32_t)gc) * 16u;
       const uint32_t ss_lane =
-          smem_addr(sp) + a.packed_stage_bytes + (uint32_t)(scale_off + rbase * G + gc);
+          a.prep ? smem_addr(hp + a.sc_off) + ((uint32_t)gc >> 1) * rpt * 2u +
+                       (uint32_t)rbase * 2u + ((uint32_t)gc & 1u)
+                 : smem_addr(sp) + a.packed_stage_bytes + (uint32_t)(scale_off + rbase * G + gc);
       const bool staged = scale_off >= 0;
       for (int base = seg_beg;;) {
         if (seg_end - base >= NT) {
@@ -947,12 +994,41 @@ size_t stage_bytes_for(size_t rows, int64_t G) {
   return 128 + rows * G * 16 + ((rows * G + 15) / 16) * 16 + 16;
 }
 
-StreamShape stream_shape(int64_t G) {
+// A stage of prepared weights: nk slabs of rows x 32 packed bytes, nk slabs
+// of rows x 2 scale bytes, the header; 1024-byte multiples.
+uint32_t prep_stage_bytes(size_t rows, int64_t nk, uint32_t* sc_off, uint32_t* hdr_off) {
+  const size_t sc = (size_t)nk * rows * 32;
+  const size_t hdr = (sc + (size_t)nk * rows * 2 + 127) / 128 * 128;
+  if (sc_off) *sc_off = (uint32_t)sc;
+  if (hdr_off) *hdr_off = (uint32_t)hdr;
+  return (uint32_t)((hdr + sizeof(StageHeader) + 1023) / 1024 * 1024);
+}
+
+// Prepared weights: tiles must not cross a 128-row block of the layout, so
+// their height (nsub * rws, warps per column a power of two) divides 128, and
+// the scale slab's rows (2 bytes each) must fill 16-byte units: at least 8
+// rows. The copies' boxes take at most 256 K chunks.
+StreamShape stream_shape(int64_t G, bool prep = false) {
   StreamShape sh;
   const int64_t ncol = (G + 31) / 32;
   if (ncol > kConsumerWarps) return sh;
   sh.ncol = (int)ncol;
   sh.nsub = kConsumerWarps / sh.ncol;
+  if (prep) {
+    const int64_t nk = (G + 1) / 2;
+    if (nk > 256) return sh;
+    int n = 1;
+    while (2 * n <= sh.nsub) n *= 2;
+    sh.nsub = n;
+    for (int rws = 8; rws >= 1; rws /= 2) {
+      const size_t rows = (size_t)sh.nsub * rws;
+      if (rows >= 8 && prep_stage_bytes(rows, nk, nullptr, nullptr) <= kMaxStageBytes) {
+        sh.rws = rws;
+        return sh;
+      }
+    }
+    return sh;
+  }
   for (int rws = 8; rws >= 1; rws /= 2) {
     if (stage_bytes_for((size_t)sh.nsub * rws, G) <= kMaxStageBytes) {
       sh.rws = rws;
@@ -986,11 +1062,11 @@ int64_t stream_row_tiles(const StreamShape& sh, int64_t O) {
 #define MXFP4EL_GEMV_STATIC_PERMILLE 900
 #endif
 
-bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
+bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, bool prep) {
   // Test knob: MXFP4EL_ROUTE=bucketer keeps the separate bucketer launch.
   if (const char* env = std::getenv("MXFP4EL_ROUTE"))
     if (std::strcmp(env, "bucketer") == 0) return false;
-  const StreamShape sh = stream_shape(I / 32);
+  const StreamShape sh = stream_shape(I / 32, prep);
   const int64_t P = T * K;
   if (sh.rws == 0 || P <= 0 || O <= 0 || P > kSelfMaxPairs || E > kSelfMaxExperts ||
       T > kSelfMaxTokens)
@@ -1001,9 +1077,9 @@ bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
   return stream_row_tiles(sh, O) * max_cost <= ((int64_t)1 << 40);
 }
 
-UnitSplit gemv_unit_split(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K) {
+UnitSplit gemv_unit_split(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, bool prep) {
   UnitSplit sp{0, 0, 0, 1000};
-  const StreamShape sh = stream_shape(I / 32);
+  const StreamShape sh = stream_shape(I / 32, prep);
   if (sh.rws == 0 || T * K == 0 || O == 0) return sp;
   const int64_t rt = stream_row_tiles(sh, O);
   const int64_t bound_units = std::min<int64_t>(E, T * K) * rt;
@@ -1027,7 +1103,7 @@ int gemv_partial_columns(int64_t I) {
   return sh.rws > 0 ? sh.ncol : 1;
 }
 
-bool gemv_uses_stream(int64_t I) { return stream_shape(I / 32).rws > 0; }
+bool gemv_uses_stream(int64_t I, bool prep) { return stream_shape(I / 32, prep).rws > 0; }
 
 cudaError_t launch_prep_tokens(const void* x, __half* x16, int* sigma, int64_t T, int64_t I,
                                cudaStream_t stream) {
@@ -1041,9 +1117,10 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
                         const void* sel, int index_dtype, const uint8_t* packed,
                         const uint8_t* scales, const RoutePlan& plan, float* part,
                         unsigned long long* status, int64_t T, int64_t E, int64_t I, int64_t O,
-                        int64_t K, cudaStream_t stream) {
+                        int64_t K, cudaStream_t stream, const PreparedView* prep) {
   const int64_t G = I / 32;
-  const StreamShape sh = stream_shape(G);
+  const StreamShape sh = stream_shape(G, prep != nullptr);
+  if (sh.rws == 0 && prep != nullptr) return cudaErrorInvalidValue;
   if (sh.rws == 0) {
     if (token_dtype == kTokenBF16)
       return launch_direct(static_cast<const __nv_bfloat16*>(x), packed, scales, plan, part,
@@ -1051,8 +1128,9 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
     return launch_direct(static_cast<const float*>(x), packed, scales, plan, part, T, E, I,
                          O, K, stream);
   }
-  const bool self = gemv_self_route(T, E, I, O, K);
+  const bool self = gemv_self_route(T, E, I, O, K, prep != nullptr);
   StreamArgs a;
+  std::memset(&a, 0, sizeof(a));
   a.x = token_dtype == kTokenBF16 && !self ? static_cast<const void*>(x16) : x;
   a.sigma = token_dtype == kTokenBF16 && !self ? sigma : nullptr;
   a.sel = sel;
@@ -1079,13 +1157,56 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
   a.rows_per_tile = sh.nsub * sh.rws;
   a.row_tiles = (int)stream_row_tiles(sh, O);
   // The bucketer wrote plan.unit_begin only if it was asked for a split.
-  if (gemv_unit_split(T, E, I, O, K).ctas == 0) a.plan.unit_begin = nullptr;
-  a.packed_stage_bytes = (uint32_t)((size_t)a.rows_per_tile * G * 16);
-  a.stage_bytes = (uint32_t)((stage_bytes_for(a.rows_per_tile, G) + 127) / 128 * 128);
+  if (gemv_unit_split(T, E, I, O, K, prep != nullptr).ctas == 0) a.plan.unit_begin = nullptr;
+  size_t slack = 0;
+  if (prep != nullptr) {
+    a.prep = 1;
+    a.packed = nullptr;
+    a.scales = nullptr;
+    a.scales_end = nullptr;
+    a.mtiles = (int)((O + kPrepRows - 1) / kPrepRows);
+    a.nk = (int)((G + 1) / 2);
+    a.pk_off = 0;
+    a.stage_bytes = prep_stage_bytes(a.rows_per_tile, a.nk, &a.sc_off, &a.hdr_off);
+    a.prow = 32;
+    a.srow = 2;
+    a.packed_stage_bytes = 0;
+    slack = 1024;                 // stages start 1024-byte aligned
+    auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t blocks = (cuuint64_t)E * (cuuint64_t)a.mtiles * (cuuint64_t)a.nk;
+    const cuuint64_t pdims[3] = {32, (cuuint64_t)kPrepRows, blocks};
+    const cuuint64_t pstrides[2] = {32, kPrepBlockBytes};
+    const cuuint32_t pbox[3] = {32, (cuuint32_t)a.rows_per_tile, (cuuint32_t)a.nk};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&a.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<unsigned char*>(prep->blocks),
+            pdims, pstrides, pbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    const cuuint64_t sdims[2] = {2 * kPrepRows, blocks};
+    const cuuint64_t sstrides[1] = {kPrepBlockBytes};
+    const cuuint32_t sbox[2] = {(cuuint32_t)(2 * a.rows_per_tile), (cuuint32_t)a.nk};
+    if (enc(&a.smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<unsigned char*>(prep->blocks + kPrepPackedBytes), sdims, sstrides, sbox,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else {
+    a.prep = 0;
+    a.packed_stage_bytes = (uint32_t)((size_t)a.rows_per_tile * G * 16);
+    a.stage_bytes = (uint32_t)((stage_bytes_for(a.rows_per_tile, G) + 127) / 128 * 128);
+    a.hdr_off = 0;
+    a.pk_off = sizeof(StageHeader);
+    a.sc_off = sizeof(StageHeader) + a.packed_stage_bytes;
+    a.prow = (uint32_t)G * 16u;
+    a.srow = (uint32_t)G;
+  }
   a.stages = (int)std::min<size_t>(
-      kMaxStages, (kSmemBudget - kStreamHeadBytes - a.route_bytes) / a.stage_bytes);
+      kMaxStages, (kSmemBudget - kStreamHeadBytes - a.route_bytes - slack) / a.stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = kStreamHeadBytes + a.route_bytes + (size_t)a.stages * a.stage_bytes;
+  const size_t smem =
+      kStreamHeadBytes + a.route_bytes + slack + (size_t)a.stages * a.stage_bytes;
   const int64_t bound_units = std::min<int64_t>(E, T * K) * a.row_tiles;
   if (bound_units > 0x7fffffff) return cudaErrorInvalidConfiguration;
 #define MXFP4EL_STREAM_CASES_SELF(ELEM, SELF)                                    \

@@ -79,7 +79,7 @@ struct Workspace {
 // tile modes then cover 64-row halves).
 bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
                      int64_t K, int token_dtype, Workspace* ws, bool with_part = true,
-                     int64_t tiles_F = 0);
+                     int64_t tiles_F = 0, bool prepared = false);
 
 // Partial results per (pair, row) that the chosen linear kernel writes.
 int linear_partial_columns(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
@@ -112,11 +112,12 @@ bool prep_fits_route(int64_t T, int64_t I);
 
 // True when the rows of width I fit the staged (bulk-copy) GEMV; bf16
 // tokens then need launch_prep_tokens first.
-bool gemv_uses_stream(int64_t I);
+bool gemv_uses_stream(int64_t I, bool prep = false);
 
 // The split the staged GEMV wants for these sizes (ctas == 0: none, the
 // kernel then splits its units evenly).
-UnitSplit gemv_unit_split(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K);
+UnitSplit gemv_unit_split(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                          bool prep = false);
 
 // Partial results per (pair, output row) that the GEMV writes for width I:
 // one per group column of the staged kernel, 1 for the direct kernel. The
@@ -129,14 +130,18 @@ cudaError_t launch_prep_tokens(const void* x, __half* x16, int* sigma, int64_t T
 // True when the staged GEMV routes for itself: few enough pairs that each
 // CTA derives the routing lists and token scales it needs from the ids, and
 // neither the bucketer nor the token prep runs.
-bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K);
+bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K,
+                     bool prep = false);
 
+struct PreparedView;
+// prep: the weights as prepared blocks (packed and scales unused), or null.
 cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16,
                         const int* sigma, const void* sel, int index_dtype,
                         const uint8_t* packed, const uint8_t* scales,
                         const RoutePlan& plan, float* part,
                         unsigned long long* status, int64_t T, int64_t E,
-                        int64_t I, int64_t O, int64_t K, cudaStream_t stream);
+                        int64_t I, int64_t O, int64_t K, cudaStream_t stream,
+                        const PreparedView* prep = nullptr);
 
 // Prefill-regime grouped GEMM on the tensor cores (bf16 tokens).
 bool gemm_tc_supported(int64_t E, int64_t I, int64_t O);
@@ -187,7 +192,30 @@ cudaError_t launch_gemm_tc(const TcTokens& tokens, const TcTileModes& modes, con
                            const uint8_t* scales, const RoutePlan& plan, float* part,
                            unsigned long long* status, int64_t E, int64_t I, int64_t O,
                            int64_t K, const SwigluTiles& swiglu, cudaStream_t stream,
-                           int counter_word = kMetaUnitCounter);
+                           int counter_word = kMetaUnitCounter,
+                           const uint8_t* prepared = nullptr);
+
+// Prepared weights (prepare.cu): one block per (expert, 128-row tile, 64-wide
+// K chunk) of the chunk's packed bytes (32 per row, 16-byte halves swapped
+// when bit 2 of the row is set) and then its scale bytes (2 per row); after
+// the blocks, the tensor-core kernel's f16 row offsets and tile modes.
+constexpr int kPrepRows = 128;
+constexpr uint32_t kPrepPackedBytes = kPrepRows * 32;
+constexpr uint32_t kPrepBlockBytes = kPrepPackedBytes + 2 * kPrepRows;
+struct PreparedView {
+  const unsigned char* blocks = nullptr;   // [E][ceil(O/128)][ceil(G/2)] blocks
+  const int16_t* row_off = nullptr;        // [E][O]
+  const uint8_t* tile_mode = nullptr;      // [E][ceil(O/128)]
+};
+size_t prepared_bytes(int64_t E, int64_t I, int64_t O);
+PreparedView prepared_view(const void* base, int64_t E, int64_t I, int64_t O);
+cudaError_t launch_prepare(const uint8_t* packed, const uint8_t* scales, int64_t E, int64_t I,
+                           int64_t O, void* prepared, cudaStream_t stream);
+// cuTensorMapEncodeTiled from the driver (PFN_cuTensorMapEncodeTiled_v12000),
+// or null.
+void* tensor_map_encoder();
+// Whether the per-tile scan of f16 operand modes handles rows of width I.
+bool tile_scan_fits(int64_t I);
 
 // Argument checks shared by every routed-linear entry point (api.cu):
 // MXFP4EL_OK or the first error, in the order the public header documents.

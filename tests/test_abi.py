@@ -236,3 +236,58 @@ def test_static_scratch_checks_like_the_other_entry_points(lib):
     # Valid for the other entry points, too large only for the fixed array.
     assert static(x, w, s, sel, p, ys, out, *big, n.DTYPE_BF16, n.INDEX_I32,
                   None) == n.ERR_TOO_LARGE
+
+
+def _a256(n):
+    return (n + 255) // 256 * 256
+
+
+def test_prepared_bytes_follow_the_documented_layout(lib):
+    # One 4352-byte block per (expert, 128-row tile, 64-wide K chunk), then the
+    # int16 [E][O] and uint8 [E][mtiles] parts, each 256-byte aligned.
+    for E, I, O in [(1, 32, 1), (3, 96, 200), (128, 2880, 5760), (384, 7168, 4096)]:
+        G = I // 32
+        nk, mt = (G + 1) // 2, (O + 127) // 128
+        want = _a256(E * mt * nk * 4352) + _a256(E * O * 2) + _a256(E * mt)
+        assert lib.mxfp4_expert_linear_prepared_bytes(E, I, O) == want
+    bad = ctypes.c_size_t(-1).value
+    assert lib.mxfp4_expert_linear_prepared_bytes(2, 48, 8) == bad      # I % 32
+    assert lib.mxfp4_expert_linear_prepared_bytes(-1, 64, 8) == bad
+    assert lib.mxfp4_expert_linear_prepared_bytes(2, 15360 + 32, 8) == bad   # beyond the limit
+    assert lib.mxfp4_expert_linear_prepared_bytes(2, 15360, 8) != bad
+
+
+def test_prepared_argument_checks_return_before_gpu_work(lib):
+    from mxfp4_routed_expert_route_gb300 import _native as n
+    prep = lib.mxfp4_expert_linear_prepare
+    w, s = ctypes.c_void_p(1 << 24), ctypes.c_void_p(1 << 28)
+    buf = ctypes.c_void_p(1 << 36)
+    need = lib.mxfp4_expert_linear_prepared_bytes(4, 64, 8)
+    assert prep(w, s, 4, 60, 8, buf, need, None) == n.ERR_INVALID_ARGUMENT
+    assert prep(w, s, 4, 64 * 1024, 8, buf, 1 << 40, None) == n.ERR_TOO_LARGE
+    assert prep(None, s, 4, 64, 8, buf, need, None) == n.ERR_INVALID_ARGUMENT
+    assert prep(w, s, 4, 64, 8, None, need, None) == n.ERR_INVALID_ARGUMENT
+    assert prep(w, s, 0, 64, 8, None, 0, None) == n.OK               # E == 0: no-op
+    assert prep(w, s, 4, 64, 8, buf, need - 1, None) == n.ERR_WORKSPACE
+    assert prep(w, s, 4, 64, 8, ctypes.c_void_p((1 << 36) + 16), need, None) == n.ERR_WORKSPACE
+    assert prep(ctypes.c_void_p((1 << 24) + 4), s, 4, 64, 8, buf, need,
+                None) == n.ERR_INVALID_ARGUMENT
+    assert prep(w, s, 4, 64, 8, ctypes.c_void_p((1 << 24) - 256), need, None) == n.ERR_ALIAS
+    f = lib.mxfp4_expert_linear_prepared
+    fake = ctypes.c_void_p(1 << 20)
+    x, ys, out = ctypes.c_void_p(1 << 32), ctypes.c_void_p(1 << 33), ctypes.c_void_p(1 << 34)
+    assert f(x, buf, fake, fake, ys, out, 4, 4, 60, 8, 2, 0, 0, None) == n.ERR_INVALID_ARGUMENT
+    assert f(x, buf, fake, fake, ys, out, 4, 4, 64, 8, 2, 9, 0, None) == n.ERR_UNSUPPORTED_DTYPE
+    assert f(x, buf, fake, fake, ys, out, 4, 4, 64 * 1024, 8, 2, 0, 0,
+             None) == n.ERR_TOO_LARGE
+    assert f(x, None, fake, fake, ys, out, 4, 4, 64, 8, 2, 0, 0, None) == n.ERR_INVALID_ARGUMENT
+    assert f(x, ctypes.c_void_p((1 << 36) + 16), fake, fake, ys, out, 4, 4, 64, 8, 2, 0, 0,
+             None) == n.ERR_INVALID_ARGUMENT
+    assert f(x, buf, fake, fake, ys, ys, 4, 4, 64, 8, 2, 0, 0, None) == n.ERR_ALIAS
+    assert f(x, buf, fake, fake, ys, out, 0, 4, 64, 8, 2, 0, 0, None) == n.OK
+    g = lib.mxfp4_expert_linear_prepared_with_workspace
+    assert g(x, buf, fake, fake, ys, out, 4, 4, 64, 8, 2, 0, 0, None, 0,
+             None) == n.ERR_WORKSPACE
+    ws = lib.mxfp4_expert_linear_prepared_workspace_size
+    assert ws(4, 4, 64, 8, 2, 0) not in (0, ctypes.c_size_t(-1).value)
+    assert ws(4, 4, 64 * 1024, 8, 2, 0) == ctypes.c_size_t(-1).value
