@@ -131,17 +131,20 @@ KERNEL_SOURCES = {
                     "mxfp4_routed_expert_route_gb300/csrc/internal.h"],
     "gemm_tc_kernel": ["mxfp4_routed_expert_route_gb300/csrc/gemm_tc.cu",
                        "mxfp4_routed_expert_route_gb300/csrc/common.cuh",
-                       "mxfp4_routed_expert_route_gb300/csrc/internal.h"],
+                       "mxfp4_routed_expert_route_gb300/csrc/internal.h",
+                       "mxfp4_routed_expert_route_gb300/csrc/prepare.cu"],
 }
 
 
-def ncu_traffic(kernel, workload):
+def ncu_traffic(kernel, workload, layout="plain"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source and this workload; else None."""
+    on the current kernel source, this workload and this weight layout; else
+    None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
+    key = f"{kernel}/{workload}" + ("/prepared" if layout == "prepared" else "")
     try:
         with open(path) as f:
-            d = json.load(f)[f"{kernel}/{workload}"]
+            d = json.load(f)[key]
     except (OSError, ValueError, KeyError):
         return None
     if d.get("source_sha256") != source_digest(KERNEL_SOURCES[kernel]):
@@ -627,7 +630,7 @@ def measure_workload(name, args, lib, dev, rank, world):
                     "frac": achieved / peaks["hbm_gbs"],
                     "peak_source": f"hbm_gbs of {peaks_src}",
                     "bytes_per_launch": lin_bytes, "launch_us": lin_mean_s * 1e6}
-    roofline["traffic"] = ncu_traffic(kernel, wl.name)
+    roofline["traffic"] = ncu_traffic(kernel, wl.name, args.weights)
     e2e_v = whole_job_rate(bytes_step if hbm_bound else flops_step, K, world, e2e_max)
     res = {
         "value": value, "unit": unit, "ms_per_step": ms_step,
