@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--weights", choices=["plain", "prepared"], default="plain",
                     help="weights as given (plain) or laid out once for the kernels before "
                          "timing (prepared: mxfp4_expert_linear_prepare, load-time work)")
+    ap.add_argument("--no-prepared-leg", action="store_true",
+                    help="with plain weights, skip the extra timing on prepared weights")
     ap.add_argument("--cpu-budget", type=float, default=6.0,
                     help="seconds of oracle time per workload for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -437,6 +439,66 @@ def linear_dtype_label(wl, gemm):
     return "f32"
 
 
+def measure_prepared(wl, d, dev, stream, flush, W, K, lib, world, gemm, bytes_step,
+                     flops_step, t_roof, hbm_bound, plain_roofline):
+    """The same steps on weights laid out once by mxfp4_expert_linear_prepare
+    (load-time work, before timing): whole-step time (L2 flushed between
+    steps) and the routed-linear kernel's CUDA-event time."""
+    import ctypes
+
+    import torch
+
+    from mxfp4_routed_expert_route_gb300 import (_native, mxfp4_expert_linear_prepared,
+                                                 prepare_weights, prepared_workspace_size)
+
+    pw = prepare_weights(d["packed"], d["scales"])
+    ws = torch.empty(max(1, prepared_workspace_size(wl.T, wl.E, wl.I, wl.O, wl.K, wl.dtype)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.T, wl.O), dtype=wl.dtype, device=dev)
+
+    def step():
+        mxfp4_expert_linear_prepared(d["x"], pw, d["sel"], d["p"], d["y_shared"], out=out,
+                                     workspace=ws)
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
+
+    for _ in range(W):
+        flush.zero_()
+        step()
+    steps = [(ev(), ev()) for _ in range(K)]
+    lin = [(ev(), ev()) for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.zero_()
+        steps[i][0].record(stream)
+        step()
+        steps[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.zero_()
+        lib.mxfp4el_set_stage_events(_native.STAGE_LINEAR, ctypes.c_void_p(lin[i][0].cuda_event),
+                                     ctypes.c_void_p(lin[i][1].cuda_event))
+        step()
+    torch.cuda.synchronize(dev)
+    lib.mxfp4el_set_stage_events(_native.STAGE_LINEAR, None, None)
+    t = max_over_ranks(sum(a.elapsed_time(b) for a, b in steps) / 1e3, dev, world)
+    lin_s = sum(a.elapsed_time(b) for a, b in lin) / K / 1e3
+    rate = whole_job_rate(bytes_step if hbm_bound else flops_step, K, world, t)
+    units = plain_roofline.get("flops_per_launch") or plain_roofline.get("bytes_per_launch")
+    achieved = units / lin_s / (1e12 if gemm else 1e9)
+    return {"weights_layout": "prepared once before timing (mxfp4_expert_linear_prepare)",
+            "value": rate / (1e9 if hbm_bound else 1e12), "ms_per_step": t / K * 1e3,
+            "path_roofline_frac": t_roof / (t / K),
+            "kernel": {"launch_us": lin_s * 1e6, "achieved": achieved,
+                       "unit": plain_roofline["unit"],
+                       "frac": achieved / plain_roofline["peak"],
+                       "traffic": ncu_traffic("gemm_tc_kernel" if gemm else "gemv_kernel",
+                                              wl.name, "prepared")}}
+
+
 def measure_workload(name, args, lib, dev, rank, world):
     """Every number of one workload: whole steps (device-timed, L2 flushed),
     the dominant kernel's CUDA-event duration inside the same steps, the
@@ -657,6 +719,9 @@ def measure_workload(name, args, lib, dev, rank, world):
         "clocks": clocks,
         "wall_s": wall,
     }
+    if args.weights == "plain" and not args.no_prepared_leg:
+        res["prepared"] = measure_prepared(wl, d, dev, stream, flush, W, K, lib, world, gemm,
+                                           bytes_step, flops_step, t_roof, hbm_bound, roofline)
     if router is not None:
         res["router"] = router
     if swiglu is not None:

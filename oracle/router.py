@@ -16,10 +16,10 @@ The router feeding the routed expert linear, as the pages define it:
   expert index); the K chosen scores are summed left to right, each is divided
   by that sum plus 1e-20 and multiplied by the routing scaling factor.
 
-Readings (listed in the design notes): the selection is decided in float32,
-the precision the pages compute it in (a float32 sigmoid of the float32 logit,
-plus the float32 bias); the weights are computed here in float64 from those
-float32 scores. Parity: pinned; tests/test_router_oracle.py.
+Readings: the selection is decided in float32, the precision the pages
+compute it in (a float32 sigmoid of the float32 logit, plus the float32
+bias); the weights are computed here in float64 from those float32 scores.
+Parity: pinned; tests/test_router_oracle.py.
 """
 from __future__ import annotations
 
