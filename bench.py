@@ -130,7 +130,8 @@ def source_digest(files):
 KERNEL_SOURCES = {
     "gemv_kernel": ["mxfp4_routed_expert_route_gb300/csrc/gemv.cu",
                     "mxfp4_routed_expert_route_gb300/csrc/common.cuh",
-                    "mxfp4_routed_expert_route_gb300/csrc/internal.h"],
+                    "mxfp4_routed_expert_route_gb300/csrc/internal.h",
+                    "mxfp4_routed_expert_route_gb300/csrc/prepare.cu"],
     "gemm_tc_kernel": ["mxfp4_routed_expert_route_gb300/csrc/gemm_tc.cu",
                        "mxfp4_routed_expert_route_gb300/csrc/common.cuh",
                        "mxfp4_routed_expert_route_gb300/csrc/internal.h",
