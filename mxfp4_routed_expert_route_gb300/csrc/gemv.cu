@@ -201,15 +201,18 @@ struct StreamArgs {
   // Stage layout. Plain weights: header at 0, the tile's packed rows (16 G
   // bytes each) at 128, its scale span after them. Prepared weights (prep):
   // one slab per K chunk of rows_per_tile rows x 32 bytes (groups 2kc and
-  // 2kc+1 of a row, in that order) at pk_off = 0, one slab per chunk of 2
-  // scale bytes per row at sc_off, the header at hdr_off; tiles then never
-  // cross a 128-row block of the layout (rows_per_tile divides 128).
+  // 2kc+1 of a row, swapped on rows with bit 2 set) at pk_off = 0, one slab per chunk of 2
+  // scale bytes per row at sc_off, the header at hdr_off. Tiles never cross
+  // a 128-row block of the layout: each block is cut into tiles_per_block
+  // tiles at multiples of rows_per_tile (a multiple of 8), the last one
+  // shorter when rows_per_tile does not divide 128.
   int prep;
   int mtiles, nk;                // prepared: 128-row tiles per expert, K chunks
+  int tiles_per_block;           // prepared: GEMV tiles per 128-row tile (the last may be short)
   uint32_t hdr_off, pk_off, sc_off;
   uint32_t prow;                 // stage bytes between a group's rows: 16 G, or 32
   uint32_t srow;                 // stage bytes between a scale's rows: G, or 2
-  CUtensorMap pmap;              // prepared: packed slabs, box {32, rows_per_tile, nk}
+  CUtensorMap pmap;              // prepared: packed slabs, box {4 rows_per_tile (8-byte), nk}
   CUtensorMap smap;              // prepared: scale slabs, box {2 rows_per_tile, nk}
 };
 
@@ -511,7 +514,8 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
                                             const int (&pair)[NTA], const int (&soff)[NTA],
                                             uint32_t sp_lane,
                                             uint32_t ss_lane, const uint8_t* gs_lane, int o0,
-                                            int rows, int rbase, int c, int lane) {
+                                            int rows, int rbase, int c, int lane,
+                                            uint32_t flip) {
   constexpr int V = Pow2Ceil<RWS * NTA>::value;
   constexpr int L = Log2<V>::value;
   const int G = a.G, O = a.O;
@@ -529,7 +533,9 @@ __device__ __forceinline__ void stream_pass(const StreamArgs& a, const GroupToke
   for (int r = 0; r < RWS; ++r) {
     if (kFull || rbase + r < rows) {
       uint32_t w[16];
-      decode_group(lds128(pa), w);
+      // Prepared weights: rows 4..7 of an 8-row group hold the row's 16-byte
+      // halves in the other order (flip = +-16; 0 on the plain layout).
+      decode_group(lds128(RWS == 8 && (r & 4) ? pa + flip : pa), w);
       const uint32_t sb = kScalesStaged ? lds_u8(sa) : (uint32_t)__ldg(ga);
 #pragma unroll
       for (int j = 0; j < NTA; ++j) acc[r * NTA + j] = apply_scale(xt[j].dot(w), sb, lut + soff[j]);
@@ -562,17 +568,18 @@ __device__ __forceinline__ void stream_pass_any(const StreamArgs& a,
                                                 const int (&pair)[NTA],
                                                 const int (&soff)[NTA], uint32_t sp_lane,
                                                 uint32_t ss_lane, int e, int gc, bool staged,
-                                                int o0, int rows, int rbase, int c, int lane) {
+                                                int o0, int rows, int rbase, int c, int lane,
+                                                uint32_t flip) {
   if (staged && rbase + RWS <= rows) {
     stream_pass<Elem, RWS, NTA, true, true>(a, xt, pair, soff, sp_lane, ss_lane, nullptr, o0,
-                                            rows, rbase, c, lane);
+                                            rows, rbase, c, lane, flip);
   } else if (staged) {
     stream_pass<Elem, RWS, NTA, true, false>(a, xt, pair, soff, sp_lane, ss_lane, nullptr, o0,
-                                             rows, rbase, c, lane);
+                                             rows, rbase, c, lane, flip);
   } else {
     const uint8_t* gs_lane = a.scales + ((size_t)e * a.O + o0 + rbase) * a.G + gc;
     stream_pass<Elem, RWS, NTA, false, false>(a, xt, pair, soff, sp_lane, ss_lane, gs_lane,
-                                              o0, rows, rbase, c, lane);
+                                              o0, rows, rbase, c, lane, flip);
   }
 }
 
@@ -615,9 +622,8 @@ gemv_stream_kernel(const __grid_constant__ StreamArgs a) {
   uint64_t* empty = full + kMaxStages;
   unsigned char* route_area = smem + kStreamHeadBytes;
   unsigned char* stage_base = route_area + (kSelf ? a.route_bytes : 0u);
-  // Prepared weights arrive through the 32-byte swizzle, whose pattern
-  // follows the shared-memory address: stages start 1024-byte aligned (the
-  // launch adds the slack).
+  // Prepared weights: stages start 1024-byte aligned (the launch adds the
+  // slack), so every slab starts on a 128-byte line.
   if (a.prep) stage_base += (1024u - (smem_addr(stage_base) & 1023u)) & 1023u;
   const SelfPlan rp = self_plan(route_area, a.E, a.P, a.T);
 
@@ -705,14 +711,23 @@ gemv_stream_kernel(const __grid_constant__ StreamArgs a) {
       }
       const int u = unit / a.row_tiles, tile = unit - u * a.row_tiles;
       if (u != cached_u) { e = kSelf ? rp.active[u] : a.plan.active[u]; cached_u = u; }
-      const int o0 = tile * a.rows_per_tile;
-      const int rows = min(a.rows_per_tile, O - o0);
+      int o0 = tile * a.rows_per_tile;
+      int rows = min(a.rows_per_tile, O - o0);
+      if (a.prep) {
+        const int blk128 = tile / a.tiles_per_block, sub = tile - blk128 * a.tiles_per_block;
+        o0 = blk128 * kPrepRows + sub * a.rows_per_tile;
+        rows = min(min(a.rows_per_tile, kPrepRows - sub * a.rows_per_tile), O - o0);
+      }
+      if (rows <= 0) {              // a tile past the last row (prepared, O % 128 != 0)
+        ++unit;
+        --issued;
+        continue;
+      }
       if (a.prep) {
         // The tile's slabs: packed rows o0 % 128 .. of every K chunk of
-        // 128-row tile o0 / 128, and their scale bytes. The swizzled load
-        // undoes the layout's swap of 16-byte halves (bit 2 of the row is
-        // bit 7 of the stage address), so a slab row holds groups 2kc,
-        // 2kc+1 in order.
+        // 128-row tile o0 / 128 (one contiguous run of 32 bytes per row in
+        // each block, the layout's half swap kept), and their scale bytes;
+        // rows past the block read zeros.
         if (!mbar_wait(&empty[st], (round & 1u) ^ 1u)) { ok = false; break; }
         unsigned char* dst = stage_base + (size_t)st * a.stage_bytes;
         StageHeader* h = reinterpret_cast<StageHeader*>(dst + a.hdr_off);
@@ -725,7 +740,7 @@ gemv_stream_kernel(const __grid_constant__ StreamArgs a) {
         const uint32_t pbytes = (uint32_t)a.nk * (uint32_t)a.rows_per_tile * 32u;
         const uint32_t sbytes = (uint32_t)a.nk * (uint32_t)a.rows_per_tile * 2u;
         mbar_arrive_expect_tx(&full[st], pbytes + sbytes);     // releases the header
-        tma_load_3d(dst + a.pk_off, &a.pmap, 0, r0, blk, &full[st], policy);
+        tma_load_2d(dst + a.pk_off, &a.pmap, 4 * r0, blk, &full[st], policy);
         tma_load_2d(dst + a.sc_off, &a.smap, 2 * r0, blk, &full[st], policy);
       } else {
       const size_t row0 = (size_t)e * O + o0;
@@ -824,11 +839,15 @@ gemv_stream_kernel(const __grid_constant__ StreamArgs a) {
         load_pass<Elem, NT, kSelf>(a, rp, x0, pair0, soff0, seg_beg, seg_end, g);
       }
       // This lane's group in row rbase of the tile: packed bytes and scale
-      // (prepared: in the slab of chunk gc / 2, half gc % 2 of the row).
+      // (prepared: in the slab of chunk gc / 2, half gc % 2 of the row, the
+      // halves swapped on rows with bit 2 set; a tile starts at a multiple
+      // of 8 rows of its 128-row block).
       const uint32_t rpt = (uint32_t)a.rows_per_tile;
+      const uint32_t half = ((uint32_t)gc ^ ((uint32_t)rbase >> 2)) & 1u;
+      const uint32_t flip = a.prep ? (half ? 0u - 16u : 16u) : 0u;
       const uint32_t sp_lane =
           a.prep ? smem_addr(sp) + ((uint32_t)gc >> 1) * rpt * 32u + (uint32_t)rbase * 32u +
-                       ((uint32_t)gc & 1u) * 16u
+                       half * 16u
                  : smem_addr(sp) + ((uint32_t)rbase * (uint32_t)G + (uint32_t)gc) * 16u;
       const uint32_t ss_lane =
           a.prep ? smem_addr(hp + a.sc_off) + ((uint32_t)gc >> 1) * rpt * 2u +
@@ -838,13 +857,13 @@ gemv_stream_kernel(const __grid_constant__ StreamArgs a) {
       for (int base = seg_beg;;) {
         if (seg_end - base >= NT) {
           stream_pass_any<Elem, RWS, NT>(a, x0, pair0, soff0, sp_lane, ss_lane, e, gc, staged,
-                                         o0, rows, rbase, c, lane);
+                                         o0, rows, rbase, c, lane, flip);
         } else {                              // one token left (NT == 2)
           stream_pass_any<Elem, RWS, 1>(
               a, reinterpret_cast<const GroupToken<Elem>(&)[1]>(x0[0]),
               reinterpret_cast<const int(&)[1]>(pair0[0]),
               reinterpret_cast<const int(&)[1]>(soff0[0]), sp_lane, ss_lane, e, gc, staged,
-              o0, rows, rbase, c, lane);
+              o0, rows, rbase, c, lane, flip);
         }
         base += NT;
         if (base >= seg_end) break;
@@ -1004,10 +1023,11 @@ uint32_t prep_stage_bytes(size_t rows, int64_t nk, uint32_t* sc_off, uint32_t* h
   return (uint32_t)((hdr + sizeof(StageHeader) + 1023) / 1024 * 1024);
 }
 
-// Prepared weights: tiles must not cross a 128-row block of the layout, so
-// their height (nsub * rws, warps per column a power of two) divides 128, and
-// the scale slab's rows (2 bytes each) must fill 16-byte units: at least 8
-// rows. The copies' boxes take at most 256 K chunks.
+// Prepared weights: a tile's rows must start at a multiple of 8 inside a
+// 128-row block of the layout (the consumers' undoing of the half swap and
+// the scale slab's 16-byte units), so its height is a multiple of 8, and at
+// most 64 (a box row of the packed copy holds at most 256 8-byte elements).
+// The copies' boxes take at most 256 K chunks.
 StreamShape stream_shape(int64_t G, bool prep = false) {
   StreamShape sh;
   const int64_t ncol = (G + 31) / 32;
@@ -1017,14 +1037,22 @@ StreamShape stream_shape(int64_t G, bool prep = false) {
   if (prep) {
     const int64_t nk = (G + 1) / 2;
     if (nk > 256) return sh;
-    int n = 1;
-    while (2 * n <= sh.nsub) n *= 2;
-    sh.nsub = n;
-    for (int rws = 8; rws >= 1; rws /= 2) {
-      const size_t rows = (size_t)sh.nsub * rws;
-      if (rows >= 8 && prep_stage_bytes(rows, nk, nullptr, nullptr) <= kMaxStageBytes) {
-        sh.rws = rws;
-        return sh;
+    // All consumer warps if their tile height is a multiple of 8 (then the
+    // 128-row blocks are cut into tiles at multiples of it), else the
+    // largest power of two of warps per column.
+    for (int pass = 0; pass < 2; ++pass) {
+      if (pass == 1) {
+        int n = 1;
+        while (2 * n <= sh.nsub) n *= 2;
+        sh.nsub = n;
+      }
+      for (int rws = 8; rws >= 1; rws /= 2) {
+        const size_t rows = (size_t)sh.nsub * rws;
+        if (rows % 8 == 0 && rows <= 64 &&
+            prep_stage_bytes(rows, nk, nullptr, nullptr) <= kMaxStageBytes) {
+          sh.rws = rws;
+          return sh;
+        }
       }
     }
     return sh;
@@ -1040,8 +1068,9 @@ StreamShape stream_shape(int64_t G, bool prep = false) {
 
 // Units of the staged kernel: active experts (at most min(E, T*K)) times
 // row tiles; the tile height follows from the stream shape.
-int64_t stream_row_tiles(const StreamShape& sh, int64_t O) {
+int64_t stream_row_tiles(const StreamShape& sh, int64_t O, bool prep = false) {
   const int64_t rows = (int64_t)sh.nsub * sh.rws;
+  if (prep) return (O + kPrepRows - 1) / kPrepRows * ((kPrepRows + rows - 1) / rows);
   return (O + rows - 1) / rows;
 }
 
@@ -1074,14 +1103,14 @@ bool gemv_self_route(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, bool
   // The in-kernel split multiplies costs by the row tiles, 1000 and the
   // grid in int64.
   const int64_t max_cost = std::min<int64_t>(E, P) * MXFP4EL_GEMV_FIXED_COST + P;
-  return stream_row_tiles(sh, O) * max_cost <= ((int64_t)1 << 40);
+  return stream_row_tiles(sh, O, prep) * max_cost <= ((int64_t)1 << 40);
 }
 
 UnitSplit gemv_unit_split(int64_t T, int64_t E, int64_t I, int64_t O, int64_t K, bool prep) {
   UnitSplit sp{0, 0, 0, 1000};
   const StreamShape sh = stream_shape(I / 32, prep);
   if (sh.rws == 0 || T * K == 0 || O == 0) return sp;
-  const int64_t rt = stream_row_tiles(sh, O);
+  const int64_t rt = stream_row_tiles(sh, O, prep);
   const int64_t bound_units = std::min<int64_t>(E, T * K) * rt;
   const int64_t ctas = stream_grid(bound_units);
   const int64_t fixed = MXFP4EL_GEMV_FIXED_COST;
@@ -1155,7 +1184,7 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
   a.ncol = sh.ncol;
   a.nsub = sh.nsub;
   a.rows_per_tile = sh.nsub * sh.rws;
-  a.row_tiles = (int)stream_row_tiles(sh, O);
+  a.row_tiles = (int)stream_row_tiles(sh, O, prep != nullptr);
   // The bucketer wrote plan.unit_begin only if it was asked for a split.
   if (gemv_unit_split(T, E, I, O, K, prep != nullptr).ctas == 0) a.plan.unit_begin = nullptr;
   size_t slack = 0;
@@ -1166,6 +1195,7 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
     a.scales_end = nullptr;
     a.mtiles = (int)((O + kPrepRows - 1) / kPrepRows);
     a.nk = (int)((G + 1) / 2);
+    a.tiles_per_block = (kPrepRows + a.rows_per_tile - 1) / a.rows_per_tile;
     a.pk_off = 0;
     a.stage_bytes = prep_stage_bytes(a.rows_per_tile, a.nk, &a.sc_off, &a.hdr_off);
     a.prow = 32;
@@ -1175,13 +1205,15 @@ cudaError_t launch_gemv(const void* x, int token_dtype, const __half* x16, const
     auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
     if (enc == nullptr) return cudaErrorNotSupported;
     const cuuint64_t blocks = (cuuint64_t)E * (cuuint64_t)a.mtiles * (cuuint64_t)a.nk;
-    const cuuint64_t pdims[3] = {32, (cuuint64_t)kPrepRows, blocks};
-    const cuuint64_t pstrides[2] = {32, kPrepBlockBytes};
-    const cuuint32_t pbox[3] = {32, (cuuint32_t)a.rows_per_tile, (cuuint32_t)a.nk};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&a.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<unsigned char*>(prep->blocks),
+    // Packed bytes as 8-byte elements, so that a tile's rows of one block
+    // (32 * rows contiguous bytes) are one box row: long contiguous reads.
+    const cuuint64_t pdims[2] = {kPrepPackedBytes / 8, blocks};
+    const cuuint64_t pstrides[1] = {kPrepBlockBytes};
+    const cuuint32_t pbox[2] = {(cuuint32_t)(4 * a.rows_per_tile), (cuuint32_t)a.nk};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&a.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<unsigned char*>(prep->blocks),
             pdims, pstrides, pbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     const cuuint64_t sdims[2] = {2 * kPrepRows, blocks};
