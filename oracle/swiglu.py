@@ -22,6 +22,11 @@ The expert as the pages define it:
 
 silu(v) = v * sigmoid(v) = v / (1 + exp(-v)), evaluated in float64.
 
+The intermediate h is the down projection's input, "rounded once to the
+token dtype". ``swiglu_expert(..., h_round="bf16")`` takes that step:
+each exact h is rounded to the nearest bf16 value, ties to even
+(``round_to_bf16``), before the down projection; without it h stays exact.
+
 Besides the result, ``swiglu_expert`` returns the terms the comparison
 tolerance is built from (each summed over the token's slots with |p|):
   abs_terms = |y_shared| + sum_k |p| |Wd| |h|       (the down stage's sum of |terms|)
@@ -46,6 +51,24 @@ def silu(v):
     v = np.asarray(v, dtype=np.float64)
     with np.errstate(over="ignore"):
         return v / (1.0 + np.exp(-v))
+
+
+def round_to_bf16(v):
+    """Round float64 values to the nearest bf16 value, ties to even, in one
+    step from the exact value: 8 significant bits for normal values (exponent
+    down to -126, float32's range), then the subnormal grid 2^-133; values
+    that round to 2^128 or beyond become +-inf; zeros, infinities and NaN
+    pass through."""
+    v = np.asarray(v, dtype=np.float64)
+    out = v.copy()
+    fin = np.isfinite(v) & (v != 0.0)
+    x = v[fin]
+    _, e = np.frexp(x)                          # |x| = m 2^e, 1/2 <= m < 1
+    quantum_exp = np.maximum(e - 8, -133)       # 8 bits: leading bit 2^(e-1) ... 2^(e-8)
+    r = np.ldexp(np.rint(np.ldexp(x, -quantum_exp)), quantum_exp)   # rint: ties to even
+    r = np.where(np.abs(r) >= np.ldexp(1.0, 128), np.copysign(np.inf, r), r)
+    out[fin] = r
+    return out
 
 
 def _pairs(x, sel, rows):
@@ -73,21 +96,26 @@ def projection(tokens, packed, scales, sel_pairs):
 
 
 def swiglu_expert(x, gate_up_packed, gate_up_scales, down_packed, down_scales, sel, p,
-                  y_shared, rows=None):
+                  y_shared, rows=None, h_round=None):
     """The SwiGLU expert for every token (or the token ids in ``rows``).
 
     Shapes: x (T, I); gate_up_packed (E, 2F, I/32, 16) with the gate rows
     first; down_packed (E, O, F/32, 16); sel, p (T, K); y_shared (T, O).
     Returns a dict with ``out`` (n, O) float64, the tolerance terms named in
     the module docstring, ``bad`` (invalid ids seen) and, per pair (n*K rows,
-    slot-major within a token), ``g``, ``u``, ``ag``, ``au`` and ``h``."""
+    slot-major within a token), ``g``, ``u``, ``ag``, ``au`` and ``h`` (the
+    exact h). h_round="bf16" runs the down projection on h rounded to bf16
+    (``h_used``; the tolerance terms then use it too)."""
     tokens, sel_pairs, K = _pairs(x, sel, rows)
     F = gate_up_packed.shape[1] // 2
     gu, gu_abs, bad = projection(tokens, gate_up_packed, gate_up_scales, sel_pairs)
     g, u = gu[:, :F], gu[:, F:]
     ag, au = gu_abs[:, :F], gu_abs[:, F:]
     h = silu(g) * u
-    d, d_abs_h, _ = projection(h, down_packed, down_scales, sel_pairs)
+    if h_round not in (None, "bf16"):
+        raise ValueError(f"unknown h_round {h_round!r}")
+    h_used = round_to_bf16(h) if h_round == "bf16" else h
+    d, d_abs_h, _ = projection(h_used, down_packed, down_scales, sel_pairs)
     # |Wd| v for the non-negative vectors v of the tolerance terms: the linear
     # oracle's sum of |terms| for token v is exactly |Wd| v.
     _, d_first, _ = projection(SILU_SLOPE_MAX * ag * np.abs(u) + np.abs(g) * au,
@@ -114,7 +142,7 @@ def swiglu_expert(x, gate_up_packed, gate_up_scales, down_packed, down_scales, s
         s_second += np.abs(pk) * d_second[j]
     return {"out": out, "abs_terms": np.abs(ys) + s_h, "s_first": s_first,
             "s_second": s_second, "s_h": s_h, "bad": int(bad),
-            "g": g, "u": u, "ag": ag, "au": au, "h": h}
+            "g": g, "u": u, "ag": ag, "au": au, "h": h, "h_used": h_used, "p": p, "K": K}
 
 
 def tolerance(terms, tau, tau1, rho):

@@ -1,14 +1,26 @@
 """GPU parity of the routed MXFP4 SwiGLU expert against the float64 oracle.
 
 Tolerance (elementwise, derived from the arithmetic in oracle/swiglu.py):
-|gpu - oracle| <= tolerance(terms, tau, tau, rho), with tau the linear's
-bound (1e-5 fp32, 8e-3 bf16, relative to the sum of |terms|) for both
-projections and rho the relative error of h = silu(g) u once evaluated in
-float32 and rounded to the token dtype (2^-20 fp32; 2^-9 + 2^-20 bf16).
+|gpu - oracle| <= tolerance(terms, tau, tau1, rho), each projection's bound
+relative to its sum of |terms| and taken from the kernel that runs it:
+  * fp32 tokens (GEMV, exact products, float32 sums): 1e-5;
+  * bf16 tokens on the GEMV: 8 * 2^-11 per group (two f16x2 chains of 8
+    products added in f16) plus G * 2^-24 for the float32 sum of the groups;
+  * bf16 tokens on the tensor cores: exact products summed in float32,
+    width * 2^-24;
+tau (the down projection) also carries the combine's (K + 1) * 2^-24, rho is
+the relative error of h = silu(g) u evaluated in float32 and rounded to the
+token dtype (2^-20 fp32; 2^-9 + 2^-20 bf16), and the output's own rounding
+to the token dtype adds OUT_ROUND |out| (half an ulp: 2^-8 bf16, 2^-24 fp32).
 
-For bf16 that worst-case bound is loose (the gate/up errors are bounded
-relative to their sum of |terms| and pass through the down projection with
-every sign aligned), so bf16 cases are also checked by
+Such a bound holds for every element. Where the tensor cores run both
+projections the roundings of h and of the output dominate it, and it came
+within 1.2 to 3 times the error at the worst element (max err/bound 0.34 to
+0.84 over the gate/up-tile cases). Where the GEMV runs, its f16 chains' bound
+sums |terms|, which for F terms of mixed sign lies about sqrt(F) above the
+error random-signed roundings produce, whatever the constant in front: there
+it came out 25 to 750 times the error. The ratio is printed for every case.
+The bf16 cases are also checked by
   * an exact case: integer-valued tokens and weights that keep every gate/up
     partial sum exact, and a down matrix that copies h to the output, so the
     output is h rounded to bf16: equal to the oracle's h rounded to bf16 but
@@ -28,9 +40,27 @@ from mxfp4_routed_expert_route_gb300 import (_native, device_errors, mxfp4_swigl
 
 pytestmark = pytest.mark.gpu
 
-TAU = {torch.float32: 1e-5, torch.bfloat16: 8e-3}
 RHO = {torch.float32: 2.0 ** -20, torch.bfloat16: 2.0 ** -9 + 2.0 ** -20}
+OUT_ROUND = {torch.float32: 2.0 ** -24, torch.bfloat16: 2.0 ** -8}
 RMS_BF16 = 1e-2
+
+
+def linear_tau(T, E, I, O, K, dtype):
+    """Error bound of one routed projection, relative to its sum of |terms|,
+    for the kernel the library runs at these sizes."""
+    if dtype == torch.float32:
+        return 1e-5
+    lib = _native.load()
+    gemm = lib.mxfp4el_linear_path(T, E, I, O, K, _native.DTYPE_BF16) == _native.PATH_GEMM
+    return I * 2.0 ** -24 if gemm else 8 * 2.0 ** -11 + (I // 32) * 2.0 ** -24
+
+
+def taus(wl):
+    """(tau for the down projection and combine, tau1 for gate/up)."""
+    P = wl.T * wl.K
+    tau1 = linear_tau(wl.T, wl.E, wl.I, 2 * wl.F, wl.K, wl.dtype)
+    tau = linear_tau(P, wl.E, wl.F, wl.O, 1, wl.dtype) + (wl.K + 1) * 2.0 ** -24
+    return tau, tau1
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -51,11 +81,15 @@ def check(out_rows, wl, rows=None, what=""):
     r = osw.swiglu_expert(*wl.args(), rows=rows)
     got = out_rows.detach().cpu().double().numpy()
     assert np.all(np.isfinite(got)), what
-    bound = osw.tolerance(r, TAU[wl.dtype], TAU[wl.dtype], RHO[wl.dtype])
+    tau, tau1 = taus(wl)
+    bound = osw.tolerance(r, tau, tau1, RHO[wl.dtype])
+    bound = bound + OUT_ROUND[wl.dtype] * (np.abs(r["out"]) + bound)
     err = np.abs(got - r["out"])
     ratio = float(np.max(err / np.maximum(bound, np.finfo(np.float64).tiny)))
     rms = float(np.sqrt(np.mean(err ** 2)) / max(np.sqrt(np.mean(r["out"] ** 2)), 1e-300))
-    print(f"[swiglu parity] {what}: max err/bound = {ratio:.3e}, relative RMS = {rms:.3e}")
+    print(f"[swiglu parity] {what}: tau1 {tau1:.2e}, tau {tau:.2e}: max err/bound = "
+          f"{ratio:.3e} (the bound {1.0 / max(ratio, 1e-300):.0f}x the error there), "
+          f"relative RMS = {rms:.3e}")
     assert ratio <= 1.0, f"{what}: max err/bound = {ratio:.3e}"
     if wl.dtype == torch.bfloat16:
         assert rms <= RMS_BF16, f"{what}: relative RMS error {rms:.3e}"

@@ -23,6 +23,7 @@ import sys
 
 import numpy as np
 import pytest
+import torch
 
 import oracle.brute as brute
 import oracle.swiglu as sw
@@ -212,8 +213,55 @@ def check_tolerance_terms_are_tight(mod):
         assert err >= 0.9 * bound, (tau1, rho, err, bound)
 
 
+def check_round_to_bf16_matches_torch(mod):
+    # For float32 inputs one rounding to bf16 is what torch's conversion
+    # (round to nearest, ties to even) does: normals over float32's whole
+    # exponent range, subnormals, values that overflow, signs, ties.
+    rng = np.random.default_rng(3)
+    exps = rng.integers(-149, 128, size=20000)
+    v = np.ldexp(rng.uniform(1.0, 2.0, size=exps.size), exps) * rng.choice([-1, 1], exps.size)
+    v = np.concatenate([v, np.ldexp(np.arange(1, 1025, dtype=np.float64), -24)]).astype(np.float32)
+    want = torch.from_numpy(v).to(torch.bfloat16).double().numpy()
+    got = mod.round_to_bf16(v.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+def check_round_to_bf16_is_one_rounding(mod):
+    # From the exact value, not through float32: 1 + 2^-8 + 2^-40 rounds up
+    # (float32 first would make it the tie 1 + 2^-8, then 1.0).
+    cases = [(1 + 2.0 ** -8 + 2.0 ** -40, 1 + 2.0 ** -7), (1 + 2.0 ** -8, 1.0),
+             (1 + 3 * 2.0 ** -8, 1 + 2.0 ** -6), (-(1 + 2.0 ** -8 + 2.0 ** -40), -(1 + 2.0 ** -7)),
+             ((2 - 2.0 ** -8) * 2.0 ** 127, np.inf),
+             ((2 - 2.0 ** -8 - 2.0 ** -30) * 2.0 ** 127, (2 - 2.0 ** -7) * 2.0 ** 127),
+             (2.0 ** -134, 0.0), (3 * 2.0 ** -134, 2.0 ** -132), (2.0 ** -133, 2.0 ** -133),
+             (0.0, 0.0), (-np.inf, -np.inf)]
+    for v, want in cases:
+        got = float(mod.round_to_bf16(np.array([v]))[0])
+        assert got == want, (v, got, want)
+
+
+def check_h_round_feeds_the_down_projection(mod):
+    # With h rounded, the result moves by exactly p Wd (round(h) - h), the
+    # brute-force expert applied to the difference (its down stage only).
+    x, gu, gus, dn, dns, sel, p, ys = random_case(11)
+    a = mod.swiglu_expert(x, gu, gus, dn, dns, sel, p, ys)
+    b = mod.swiglu_expert(x, gu, gus, dn, dns, sel, p, ys, h_round="bf16")
+    np.testing.assert_array_equal(b["h"], a["h"])
+    np.testing.assert_array_equal(b["h_used"], mod.round_to_bf16(a["h"]))
+    assert np.any(b["h_used"] != a["h"])
+    T, K = sel.shape
+    moved = np.zeros_like(a["out"])
+    for t in range(T):
+        for k in range(K):
+            Wd = brute.dequantize(dn[int(sel[t, k])], dns[int(sel[t, k])])
+            j = t * K + k
+            moved[t] += p[t, k] * (Wd @ (b["h_used"][j] - a["h"][j]))
+    _close(b["out"] - a["out"], moved, rel=1e-9)
+
+
 PINS = [check_closed_form_gate_up, check_tolerance_terms_are_tight, check_silu_library, check_brute_force, check_abs_terms,
-        check_rows_and_invariants, check_tolerance_is_a_bound]
+        check_rows_and_invariants, check_tolerance_is_a_bound, check_round_to_bf16_matches_torch,
+        check_round_to_bf16_is_one_rounding, check_h_round_feeds_the_down_projection]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -238,6 +286,8 @@ MUTATIONS = {
     "sigmoid_not_silu": ("return v / (1.0 + np.exp(-v))", "return 1.0 / (1.0 + np.exp(-v))"),
     "silu_sign": ("return v / (1.0 + np.exp(-v))", "return v / (1.0 + np.exp(v))"),
     "up_dropped": ("h = silu(g) * u", "h = silu(g)"),
+    "h_round_ignored": ('h_used = round_to_bf16(h) if h_round == "bf16" else h', "h_used = h"),
+    "bf16_truncates": ("np.rint(np.ldexp(x, -quantum_exp))", "np.trunc(np.ldexp(x, -quantum_exp))"),
     "gate_dropped": ("h = silu(g) * u", "h = silu(u) * u"),
     "weight_ignored": ("out += pk * d[j]", "out += d[j]"),
     "shared_dropped": ("out = ys.copy()", "out = np.zeros_like(ys)"),
