@@ -580,7 +580,13 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   TcShared& sh = *reinterpret_cast<TcShared*>(scale_buf + 2 * a.scale_cap);
   float* epi_stage = reinterpret_cast<float*>(&sh + 1);   // 16-byte aligned (TcShared is)
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Values that feed tcgen05 and TMA operands (TMEM and shared-memory
+  // addresses, instruction descriptors) go through a lane-0 shuffle, which
+  // the compiler knows to be warp-uniform. Otherwise it has to uniformise
+  // them at every issue, and that happens inside the MMA thread's per-chunk
+  // loop, whose gaps set the tensor pipe's idle time (same bits; prefill GEMM
+  // 1031 -> 1170 TFLOP/s).
+  const int warp = __shfl_sync(kFullMask, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
   pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
@@ -647,7 +653,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = sh.tmem_base;
+  const uint32_t tmem = __shfl_sync(kFullMask, sh.tmem_base, 0);
   const int num_units = sh.num_units;
   const int G = a.G, O = a.O;
   const int nk = G / 2;                              // chunks of 64 = two groups
@@ -800,21 +806,24 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       const Unit w = unit_at<kSplit>(a, sh, idx);
       if (w.ntok <= 0) { --it; continue; }
       const int db = it & 1;
-      if (!mbar_wait(&sh.d_empty[db], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
+      if (!mbar_wait_warp(&sh.d_empty[db], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem + kDCol + (uint32_t)db * kNMax;
-      const uint32_t idesc = mma_idesc(kBM, w.nmma, tile_f16(a, w));
+      const uint32_t idesc = __shfl_sync(kFullMask, mma_idesc(kBM, w.nmma, tile_f16(a, w)), 0);
       for (int kc = 0; kc < nk; ++kc) {
         // Ready once all kTeamWarps warps of the team arrived for this
         // chunk: a warp arrives for its next chunk in this buffer only after
         // these MMAs finished, so the barrier cannot run a phase ahead.
+        // (Every lane gives up together, so that the warp stays converged
+        // for the shuffle and elect.sync below.)
         const uint32_t buf = chunk % kABufs;
-        if (!mbar_wait(&sh.a_full[buf], (chunk / kABufs) & 1u)) {
+        if (!mbar_wait_warp(&sh.a_full[buf], (chunk / kABufs) & 1u)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t b_addr = smem_addr(ring_b + (size_t)pb.idx * a.stage_b);
+        const uint32_t b_addr =
+            __shfl_sync(kFullMask, smem_addr(ring_b + (size_t)pb.idx * a.stage_b), 0);
         const uint32_t a_tmem = tmem + kACol + buf * 32;
         if (elect_one()) {
 #pragma unroll
