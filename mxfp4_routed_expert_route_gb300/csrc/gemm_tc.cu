@@ -203,6 +203,7 @@ struct Unit {
   int nmma;       // MMA N: ntok rounded up to 16
   int load;       // token box: load_rows(load) >= nmma
   int mt;         // row tile index
+  int nblk;       // the expert's token blocks: its tiles are read once per block
 };
 
 template <bool kSplit>
@@ -231,6 +232,7 @@ __device__ __forceinline__ Unit unit_at(const TcArgs& a, const TcShared& sh, int
   // Gate/up tiles: m0 is the first gate row f0, rows the valid rows of each half.
   constexpr int tm = kSplit ? kBM / 2 : kBM;
   w.mt = mt;
+  w.nblk = nblk;
   w.m0 = mt * tm;
   w.rows = min(tm, (kSplit ? a.F : a.O) - w.m0);
   return w;
@@ -662,7 +664,12 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   if (warp == 0) {
     // ---------------------------------------- producer A: scales + weights
     if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();     // weights: read once
+      // Weights: evict-first when the expert has one token block (each
+      // tile read once); with several blocks every tile is read again for
+      // each block, a wave or so later, so those keep the normal priority
+      // and are not re-read from DRAM (skewed prefill 1 % faster).
+      const uint64_t pol_once = l2_evict_first_policy();
+      const uint64_t pol_reuse = l2_evict_normal_policy();
       int it = 0, issued = 0;
       RingPos pa, pu;
       int* counter = &a.plan.meta[a.counter_word];
@@ -677,6 +684,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         next = atomicAdd(counter, 1);
         const Unit w = unit_at<kSplit>(a, sh, idx);
         if (w.ntok <= 0) { --it; continue; }
+        const uint64_t pol = w.nblk > 1 ? pol_reuse : pol_once;
         if constexpr (kPrep) {
           // The tile's chunk blocks are consecutive: one bulk copy each.
           const unsigned char* blk =
