@@ -428,6 +428,7 @@ bool carve_workspace(void* base, int64_t T, int64_t E, int64_t I, int64_t O,
   ws->plan.active = reinterpret_cast<int*>(take((size_t)E * sizeof(int)));
   ws->plan.pair_list = reinterpret_cast<int*>(take((size_t)P * sizeof(int)));
   const bool gemm = K > 0 && choose_path(T, E, I, O, K, token_dtype) == LinearPath::kGemm;
+  ws->plan.pos_of_pair = gemm ? reinterpret_cast<int*>(take((size_t)P * sizeof(int))) : nullptr;
   const bool self = K > 0 && !gemm && gemv_self_route(T, E, I, O, K, prepared);
   const bool prep = token_dtype == MXFP4EL_DTYPE_BF16 && K > 0 && !gemm && !self;
   const bool prep_in_route = prep && gemv_uses_stream(I, prepared) && prep_fits_route(T, I);

@@ -1040,11 +1040,15 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
 
 // Token rows grouped by expert for the tensor-core kernel: row p of xg is
 // token t = pair_list[p] / K as f16(x[t] 2^sigma) with max |x_t| 2^sigma in
-// [2^14, 2^15), sigma[p] its power of two; one warp per row. Also resets the
-// kernel's unit counters and, for gate/up tiles, the down projection's ids.
+// [2^14, 2^15), sigma[p] its power of two (the computation of prep_token
+// with top = 14). One warp per token: it reads and converts the token's row
+// once and writes it to the positions of its valid pairs (pos_of_pair), so
+// a token picked by K experts costs one conversion and K row stores. Also
+// resets the kernel's unit counters and, for gate/up tiles, the down
+// projection's ids.
 __global__ void __launch_bounds__(256)
 group_tokens_kernel(const __nv_bfloat16* __restrict__ x, __half* __restrict__ xg,
-                    int* __restrict__ sigma, RoutePlan plan, int I, int K,
+                    int* __restrict__ sigma, RoutePlan plan, int T, int I, int K,
                     int32_t* __restrict__ zero_ids, int64_t nzero) {
   pdl_launch_dependents();
   pdl_wait();                    // the bucketer's lists are ready
@@ -1058,14 +1062,58 @@ group_tokens_kernel(const __nv_bfloat16* __restrict__ x, __half* __restrict__ xg
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nzero;
        i += (int64_t)gridDim.x * blockDim.x)
     zero_ids[i] = 0;
-  const int npairs = plan.meta[kMetaNumPairs];
-  const int warps = blockDim.x / 32;
-  for (int pos = blockIdx.x * warps + (threadIdx.x >> 5); pos < npairs;
-       pos += gridDim.x * warps) {
-    const int t = plan.pair_list[pos] / K;
-    // prep_token addresses row `t` of its arguments: point them at the
-    // token's row and the grouped row, as row 0.
-    prep_token(x + (size_t)t * I, xg + (size_t)pos * I, sigma + pos, 0, I, threadIdx.x & 31, 14);
+  constexpr int kSlots = 8;                        // pair positions held per pass
+  const int lane = threadIdx.x & 31, warps = blockDim.x / 32, nvec = I / 8;
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
+    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * I);
+    int s = -1;                                    // computed once, on the first valid slot
+    float up = 0.f;
+    for (int k0 = 0; k0 < K; k0 += kSlots) {
+      int pos[kSlots];
+      bool any = false;
+#pragma unroll
+      for (int j = 0; j < kSlots; ++j) {
+        pos[j] = k0 + j < K ? plan.pos_of_pair[(size_t)t * K + k0 + j] : -1;
+        any |= pos[j] >= 0;
+      }
+      if (!any) continue;
+      if (s < 0) {
+        uint32_t m = 0;                            // max |x| as float32 bits
+        for (int i = lane; i < nvec; i += 32) {
+          const uint4 v = __ldg(row + i);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            m = max(m, (w[k] << 16) & 0x7fffffffu);
+            m = max(m, w[k] & 0x7fff0000u);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(kFullMask, m, o));
+        const int ex = (int)(m >> 23);
+        s = 0;
+        if (m != 0 && ex < 255) s = min(126, 127 + 14 - ex);
+        up = __uint_as_float((uint32_t)(s + 127) << 23);
+      }
+      for (int i = lane; i < nvec; i += 32) {
+        const uint4 v = __ldg(row + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __half2 p = __floats2half2_rn(__uint_as_float(w[k] << 16) * up,
+                                              __uint_as_float(w[k] & 0xffff0000u) * up);
+          h[k] = *reinterpret_cast<const uint32_t*>(&p);
+        }
+        const uint4 hv = make_uint4(h[0], h[1], h[2], h[3]);
+#pragma unroll
+        for (int j = 0; j < kSlots; ++j)
+          if (pos[j] >= 0) reinterpret_cast<uint4*>(xg + (size_t)pos[j] * I)[i] = hv;
+      }
+#pragma unroll
+      for (int j = 0; j < kSlots; ++j)
+        if (lane == j && pos[j] >= 0) sigma[pos[j]] = s;
+    }
   }
 }
 
@@ -1223,11 +1271,12 @@ void* tensor_map_encoder() { return reinterpret_cast<void*>(encode_fn()); }
 cudaError_t launch_group_tokens(const void* x, const RoutePlan& plan, __half* xg, int* sigma,
                                 int64_t T, int64_t I, int64_t K, int32_t* zero_ids,
                                 cudaStream_t stream) {
+  if (plan.pos_of_pair == nullptr) return cudaErrorInvalidValue;
   const int64_t P = T * K;
-  const int64_t blocks = std::min<int64_t>((P + 7) / 8, (int64_t)num_sms_tc() * 8);
+  const int64_t blocks = std::min<int64_t>((T + 7) / 8, (int64_t)num_sms_tc() * 8);
   return launch_after_previous(group_tokens_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)),
                                dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x), xg,
-                               sigma, plan, (int)I, (int)K, zero_ids,
+                               sigma, plan, (int)T, (int)I, (int)K, zero_ids,
                                zero_ids != nullptr ? P : (int64_t)0);
 }
 

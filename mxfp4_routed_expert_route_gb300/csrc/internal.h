@@ -39,6 +39,8 @@ struct RoutePlan {
   int* offsets;     // [E + 1] start of each expert's segment in pair_list
   int* active;      // [E]     ascending ids of experts with count > 0
   int* pair_list;   // [T*K]   pair ids t*K + k grouped by expert, stable
+  int* pos_of_pair; // [T*K] or null: each pair's position in pair_list, -1 for an
+                    // out-of-range id (written by the bucketer when not null)
   int* unit_begin;  // [kMaxSplitCtas + 1] first GEMV unit of each CTA, when
                     // the bucketer was asked for a cost-balanced split
 };
@@ -171,9 +173,10 @@ struct TcTokens {
 size_t gemm_tc_grouped_bytes(int64_t T, int64_t K, int64_t I);
 
 // xg[p] = f16(x[t] 2^sigma) for t = pair_list[p] / K (max |x_t| 2^sigma in
-// [2^14, 2^15)), sigma[p] its power of two; also resets the tensor-core
-// kernel's unit counters; zero_ids (T*K ints) or nullptr: also set to 0
-// (gate/up tiles).
+// [2^14, 2^15)), sigma[p] its power of two, one warp per token through
+// plan.pos_of_pair (required: cudaErrorInvalidValue without it); also resets
+// the tensor-core kernel's unit counters; zero_ids (T*K ints) or nullptr:
+// also set to 0 (gate/up tiles).
 cudaError_t launch_group_tokens(const void* x, const RoutePlan& plan, __half* xg, int* sigma,
                                 int64_t T, int64_t I, int64_t K, int32_t* zero_ids,
                                 cudaStream_t stream);

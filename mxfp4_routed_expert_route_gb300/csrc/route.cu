@@ -186,6 +186,8 @@ route_kernel(const Idx* __restrict__ sel, int64_t P, int E, int* wc_global,
       plan.pair_list[start + __popc(peers & lanes_below)] = (int)i;
       if ((peers & lanes_below) == 0) my_wc[e] = start + __popc(peers);
     }
+    if (in && plan.pos_of_pair != nullptr)
+      plan.pos_of_pair[i] = valid ? start + __popc(peers & lanes_below) : -1;
     __syncwarp();
   }
 
@@ -352,6 +354,8 @@ route_scatter_kernel(const Idx* __restrict__ sel, int64_t P, int E,
       plan.pair_list[start + __popc(peers & lanes_below)] = (int)i;
       if ((peers & lanes_below) == 0) my_wc[e] = start + __popc(peers);
     }
+    if (in && plan.pos_of_pair != nullptr)
+      plan.pos_of_pair[i] = valid ? start + __popc(peers & lanes_below) : -1;
     __syncwarp();
   }
 }
