@@ -1150,7 +1150,17 @@ tile_scan_kernel(const uint8_t* __restrict__ scales, int G, int O, int F, int mt
     const uintptr_t w0 = lo & ~(uintptr_t)15, w1 = (lo + (uintptr_t)n * G + 15) & ~(uintptr_t)15;
     uint4* dst = reinterpret_cast<uint4*>(span + (size_t)h * (kSpanRows * G + 32));
     const uint4* src = reinterpret_cast<const uint4*>(w0);
-    for (int i = m; i < (int)((w1 - w0) / 16); i += blockDim.x) dst[i] = __ldg(src + i);
+    // Eight loads in flight per thread before their stores.
+    const int nv = (int)((w1 - w0) / 16), step = blockDim.x;
+    int i = m;
+    for (; i + 7 * step < nv; i += 8 * step) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldg(src + i + j * step);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[i + j * step] = v[j];
+    }
+    for (; i < nv; i += step) dst[i] = __ldg(src + i);
     if (m == 0) off[h] = h * (kSpanRows * G + 32) + (int)(lo - w0);
   }
   __syncthreads();
@@ -1165,11 +1175,16 @@ tile_scan_kernel(const uint8_t* __restrict__ scales, int G, int O, int F, int mt
   uint32_t lo = 255, hi = 0;
   if (row >= 0) {
     const uint8_t* p = span + off[kSplit && m >= kSpanRows ? 1 : 0] + (size_t)(m % kSpanRows) * G;
+    // Rows are G bytes apart: each thread starts at its own byte m mod G,
+    // so that a warp's reads spread over the banks instead of piling onto
+    // the few that G-byte strides hit.
+    int g = m % G;
 #pragma unroll 8
-    for (int g = 0; g < G; ++g) {
+    for (int n = 0; n < G; ++n) {
       const uint32_t v = p[g];
       lo = min(lo, v);
       hi = max(hi, v);
+      g = g + 1 == G ? 0 : g + 1;
     }
     fits = (int)(hi - lo) <= kF16Span;
   }
