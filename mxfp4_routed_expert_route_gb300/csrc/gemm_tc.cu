@@ -35,13 +35,13 @@
 // Warp roles in a CTA of 24 warps (one CTA per SM, persistent over units
 // (expert, token block, 128-row tile), which CTAs take from a global counter
 // as they go):
-//   warp 0      producer of scales and packed weights (lane 0) and TMEM
+//   warp 0      producer of scales and packed weights (elected lane) and TMEM
 //               allocation; takes each next unit from the counter and hands
 //               its index to the other roles through a shared-memory ring
 //   warp 1      MMA issuer (the whole warp waits for each chunk's readiness,
 //               one elected lane issues)
 //   warp 2      per-expert lists at start
-//   warp 3      producer of token tiles (lane 0)
+//   warp 3      producer of token tiles (elected lane)
 //   warps 4-19  dequantize, in four teams of 4 warps: team t takes chunks t,
 //               t+4, ...; thread m decodes both groups of the chunk for
 //               weight row m into TMEM A buffer (chunk mod 4), once the
@@ -102,8 +102,8 @@ constexpr int kListWarp = 2, kProdBWarp = 3;
 constexpr int kNumLoads = kNMax / 16;       // token-box heights: 16, 32, ..., kNMax rows
 __host__ __device__ constexpr int load_rows(int l) { return 16 * (l + 1); }
 constexpr int kDequantWarp0 = 4, kDequantWarps = 16, kTeamWarps = 4, kEpiWarp0 = 20;
-// Readers of the unit ring, one arrival each: producer B (one thread), the
-// MMA warp, the dequantizer warps and the epilogue warps.
+// Readers of the unit ring, one arrival each: the producer B warp, the MMA
+// warp, the dequantizer warps and the epilogue warps.
 constexpr int kUnitReaders = 2 + kDequantWarps + (kTcThreads / 32 - kEpiWarp0);
 static_assert(kDequantWarps == kTeams * kTeamWarps, "four teams of four warps");
 // The widest span of scale bytes within one row that f16 operands hold
@@ -663,7 +663,11 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
 
   if (warp == 0) {
     // ---------------------------------------- producer A: scales + weights
-    if (lane == 0) {
+    // The whole warp runs the loop and its waits; lane 0 takes the units,
+    // and one elected lane issues each copy. (Issuing copies from a loop
+    // that lane 0 runs alone measured 3 % slower per plain-layout prefill
+    // step, like the MMA issue: code under elect.sync issues better.)
+    {
       // Weights: evict-first when the expert has one token block (each
       // tile read once); with several blocks every tile is read again for
       // each block, a wave or so later, so those keep the normal priority
@@ -673,15 +677,20 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
       int it = 0, issued = 0;
       RingPos pa, pu;
       int* counter = &a.plan.meta[a.counter_word];
-      int next = atomicAdd(counter, 1);                  // one unit ahead
+      int next = 0;
+      if (lane == 0) next = atomicAdd(counter, 1);       // one unit ahead
+      next = __shfl_sync(kFullMask, next, 0);
       for (;; ++it) {
         const int idx = next < num_units ? next : -1;
-        if (!mbar_wait(&sh.u_empty[pu.idx], pu.phase ^ 1u)) { ok = false; break; }
-        sh.unit_ring[pu.idx] = idx;
-        mbar_arrive(&sh.u_full[pu.idx]);                 // releases the index
+        if (!mbar_wait_warp(&sh.u_empty[pu.idx], pu.phase ^ 1u)) { ok = false; break; }
+        if (lane == 0) {
+          sh.unit_ring[pu.idx] = idx;
+          mbar_arrive(&sh.u_full[pu.idx]);               // releases the index
+        }
         pu.next(kUnitRing);
         if (idx < 0) break;
-        next = atomicAdd(counter, 1);
+        if (lane == 0) next = atomicAdd(counter, 1);
+        next = __shfl_sync(kFullMask, next, 0);
         const Unit w = unit_at<kSplit>(a, sh, idx);
         if (w.ntok <= 0) { --it; continue; }
         const uint64_t pol = w.nblk > 1 ? pol_reuse : pol_once;
@@ -690,13 +699,15 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
           const unsigned char* blk =
               a.prep + ((size_t)w.e * a.mtiles + w.mt) * (size_t)nk * kStagePrep;
           for (int kc = 0; kc < nk; ++kc, ++issued) {
-            if (!mbar_wait(&sh.empty_a[pa.idx], pa.phase ^ 1u)) {
+            if (!mbar_wait_warp(&sh.empty_a[pa.idx], pa.phase ^ 1u)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&sh.full_a[pa.idx], kStagePrep);
-            bulk_copy_g2s(ring_a + (size_t)pa.idx * kStagePrep, blk + (size_t)kc * kStagePrep,
-                          kStagePrep, &sh.full_a[pa.idx], pol);
+            if (elect_one()) {
+              mbar_arrive_expect_tx(&sh.full_a[pa.idx], kStagePrep);
+              bulk_copy_g2s(ring_a + (size_t)pa.idx * kStagePrep, blk + (size_t)kc * kStagePrep,
+                            kStagePrep, &sh.full_a[pa.idx], pol);
+            }
             pa.next(a.stages_a);
           }
           if (!ok) break;
@@ -705,7 +716,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         // The tile's scale bytes, by one bulk copy of the aligned span that
         // holds them when it stays inside the scales buffer.
         const int sb = it & 1;
-        if (!mbar_wait(&sh.s_empty[sb], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
+        if (!mbar_wait_warp(&sh.s_empty[sb], ((uint32_t)(it >> 1) & 1u) ^ 1u)) { ok = false; break; }
         const size_t row0 = (size_t)w.e * O + w.m0;
         const uintptr_t s_lo = reinterpret_cast<uintptr_t>(a.scales + row0 * G);
         const uintptr_t s_hi = s_lo + (uintptr_t)w.rows * G;
@@ -719,80 +730,91 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         const uint32_t bytes2 = kSplit ? (uint32_t)(d_hi - d_lo) : 0u;
         const bool copy = c_hi <= end && (!kSplit || d_hi <= end) &&
                           (size_t)bytes1 + bytes2 <= a.scale_cap;
-        sh.scale_off[sb] = copy ? (int)(s_lo - c_lo) : -1;
-        if constexpr (kSplit) sh.scale_off_up[sb] = copy ? (int)(bytes1 + (u_lo - d_lo)) : -1;
-        if (copy) {
-          unsigned char* dst = scale_buf + (size_t)sb * a.scale_cap;
-          mbar_arrive_expect_tx(&sh.s_full[sb], bytes1 + bytes2);
-          bulk_copy_g2s(dst, reinterpret_cast<const void*>(c_lo), bytes1, &sh.s_full[sb], pol);
-          if (bytes2)
-            bulk_copy_g2s(dst + bytes1, reinterpret_cast<const void*>(d_lo), bytes2,
-                          &sh.s_full[sb], pol);
-        } else {
-          mbar_arrive(&sh.s_full[sb]);
+        if (elect_one()) {
+          sh.scale_off[sb] = copy ? (int)(s_lo - c_lo) : -1;
+          if constexpr (kSplit) sh.scale_off_up[sb] = copy ? (int)(bytes1 + (u_lo - d_lo)) : -1;
+          if (copy) {
+            unsigned char* dst = scale_buf + (size_t)sb * a.scale_cap;
+            mbar_arrive_expect_tx(&sh.s_full[sb], bytes1 + bytes2);
+            bulk_copy_g2s(dst, reinterpret_cast<const void*>(c_lo), bytes1, &sh.s_full[sb], pol);
+            if (bytes2)
+              bulk_copy_g2s(dst + bytes1, reinterpret_cast<const void*>(d_lo), bytes2,
+                            &sh.s_full[sb], pol);
+          } else {
+            mbar_arrive(&sh.s_full[sb]);
+          }
         }
         for (int kc = 0; kc < nk; ++kc, ++issued) {
-          if (!mbar_wait(&sh.empty_a[pa.idx], pa.phase ^ 1u)) {
+          if (!mbar_wait_warp(&sh.empty_a[pa.idx], pa.phase ^ 1u)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sh.full_a[pa.idx], kStageA);
-          unsigned char* stage = ring_a + (size_t)pa.idx * kStageA;
-          if constexpr (kSplit) {
-            // 64 gate rows, then the 64 matching up rows (same swizzle phase:
-            // the second box starts 2048 bytes in).
-            tma_load_2d(stage, &maps.a_half, kc * 32, (int)row0, &sh.full_a[pa.idx], pol);
-            tma_load_2d(stage + kStageA / 2, &maps.a_half, kc * 32, (int)(row0 + a.F),
-                        &sh.full_a[pa.idx], pol);
-          } else {
-            tma_load_2d(stage, &maps.a, kc * 32, (int)row0, &sh.full_a[pa.idx], pol);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&sh.full_a[pa.idx], kStageA);
+            unsigned char* stage = ring_a + (size_t)pa.idx * kStageA;
+            if constexpr (kSplit) {
+              // 64 gate rows, then the 64 matching up rows (same swizzle
+              // phase: the second box starts 2048 bytes in).
+              tma_load_2d(stage, &maps.a_half, kc * 32, (int)row0, &sh.full_a[pa.idx], pol);
+              tma_load_2d(stage + kStageA / 2, &maps.a_half, kc * 32, (int)(row0 + a.F),
+                          &sh.full_a[pa.idx], pol);
+            } else {
+              tma_load_2d(stage, &maps.a, kc * 32, (int)row0, &sh.full_a[pa.idx], pol);
+            }
           }
           pa.next(a.stages_a);
         }
       }
-      if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
-      // Wait (bounded) until the copies this thread issued have landed: the
+      if (!ok && lane == 0) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+      // Wait (bounded) until the copies the warp issued have landed: the
       // last min(issued, stages) uses of the ring, walking back from pa.
-      for (int k = 0; k < min(issued, a.stages_a); ++k) {
-        int idx = pa.idx - 1 - k;
-        uint32_t ph = pa.phase;
-        if (idx < 0) { idx += a.stages_a; ph ^= 1u; }
-        if (!mbar_wait(&sh.full_a[idx], ph)) break;
+      if (lane == 0) {
+        for (int k = 0; k < min(issued, a.stages_a); ++k) {
+          int idx = pa.idx - 1 - k;
+          uint32_t ph = pa.phase;
+          if (idx < 0) { idx += a.stages_a; ph ^= 1u; }
+          if (!mbar_wait(&sh.full_a[idx], ph)) break;
+        }
+        if constexpr (!kPrep)
+          for (int k = max(0, it - 2); k < it; ++k)
+            if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)(k >> 1) & 1u)) break;
       }
-      if constexpr (!kPrep)
-        for (int k = max(0, it - 2); k < it; ++k)
-          if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)(k >> 1) & 1u)) break;
     }
     __syncwarp();
   } else if (warp == kProdBWarp) {
     // ------------------------------------------------------ producer B: tokens
-    if (lane == 0) {
+    // Like producer A: the whole warp waits, one elected lane issues.
+    {
       const uint64_t pol = l2_evict_last_policy();      // tokens: reread per tile
       int issued = 0, idx;
       RingPos pr, pu;
       while (ok) {
-        if (!pop_unit<false>(sh, pu, 0, &idx)) { ok = false; break; }
+        if (!pop_unit<true>(sh, pu, lane, &idx)) { ok = false; break; }
         if (idx < 0) break;
         const Unit w = unit_at<kSplit>(a, sh, idx);
         if (w.ntok <= 0) continue;
         const uint32_t box = (uint32_t)load_rows(w.load) * 128u;
         for (int kc = 0; kc < nk; ++kc, ++issued) {
-          if (!mbar_wait(&sh.done[pr.idx], pr.phase ^ 1u)) {
+          if (!mbar_wait_warp(&sh.done[pr.idx], pr.phase ^ 1u)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sh.b_full[pr.idx], box);
-          tma_load_2d(ring_b + (size_t)pr.idx * a.stage_b, &maps.b[w.load], kc * kBK, w.tok0,
-                      &sh.b_full[pr.idx], pol);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&sh.b_full[pr.idx], box);
+            tma_load_2d(ring_b + (size_t)pr.idx * a.stage_b, &maps.b[w.load], kc * kBK, w.tok0,
+                        &sh.b_full[pr.idx], pol);
+          }
           pr.next(SB);
         }
       }
-      if (!ok) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
-      for (int k = 0; k < min(issued, SB); ++k) {
-        int ridx = pr.idx - 1 - k;
-        uint32_t ph = pr.phase;
-        if (ridx < 0) { ridx += SB; ph ^= 1u; }
-        if (!mbar_wait(&sh.b_full[ridx], ph)) break;
+      if (!ok && lane == 0) atomicAdd(&a.status[kStatusWaitTimeouts], 1ull);
+      if (lane == 0) {
+        for (int k = 0; k < min(issued, SB); ++k) {
+          int ridx = pr.idx - 1 - k;
+          uint32_t ph = pr.phase;
+          if (ridx < 0) { ridx += SB; ph ^= 1u; }
+          if (!mbar_wait(&sh.b_full[ridx], ph)) break;
+        }
       }
     }
     __syncwarp();
