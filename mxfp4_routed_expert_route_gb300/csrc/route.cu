@@ -272,21 +272,32 @@ route_scan_kernel(int* __restrict__ cta_counts, int nctas, int E, RoutePlan plan
   pdl_wait();                                    // the counts are complete
   __shared__ int warp_buf[33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // Per expert (one warp each): exclusive prefix over CTAs, in place.
+  // Per expert (one warp each): exclusive prefix over CTAs, in place. The
+  // counts of 128 CTAs are loaded before any is scanned, so that a warp
+  // waits for one load per 128 CTAs instead of one per 32.
+  constexpr int kBatch = 4;
   for (int e = warp; e < E; e += kRouteWarps) {
     int* row = cta_counts + (size_t)e * nctas;
     int run = 0;
-    for (int c0 = 0; c0 < nctas; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < nctas ? row[c] : 0;
-      int incl = v;
+    for (int c0 = 0; c0 < nctas; c0 += 32 * kBatch) {
+      int v[kBatch];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int n = __shfl_up_sync(kFullMask, incl, off);
-        if (lane >= off) incl += n;
+      for (int j = 0; j < kBatch; ++j) {
+        const int c = c0 + 32 * j + lane;
+        v[j] = c < nctas ? row[c] : 0;
       }
-      if (c < nctas) row[c] = run + incl - v;
-      run += __shfl_sync(kFullMask, incl, 31);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int c = c0 + 32 * j + lane;
+        int incl = v[j];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int n = __shfl_up_sync(kFullMask, incl, off);
+          if (lane >= off) incl += n;
+        }
+        if (c < nctas) row[c] = run + incl - v[j];
+        run += __shfl_sync(kFullMask, incl, 31);
+      }
     }
     if (lane == 0) plan.counts[e] = run;
   }
